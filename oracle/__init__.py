@@ -1,0 +1,145 @@
+"""Oracle for the indexer top-k + transform: test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. The library under
+``sparse_attention_top_row_gb300`` never does.
+
+The arithmetic lives in ``topk_oracle.cpp`` (plain single-threaded C++17,
+sorted windows). This module only compiles it with g++ and marshals numpy
+arrays through ctypes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "topk_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIBS: dict[int, ctypes.CDLL] = {}
+
+RAGGED = 0
+PAGED = 1
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (or one planted-mistake variant) into ``_build/``."""
+    out = lib_path(mutant)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-std=c++17", "-O2", "-shared", "-fPIC", f"-DORACLE_MUTANT={mutant}", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _load(mutant: int = 0) -> ctypes.CDLL:
+    with _LOCK:
+        if mutant not in _LIBS:
+            lib = ctypes.CDLL(build(mutant))
+            fn = lib.oracle_topk_transform
+            fn.restype = ctypes.c_int64
+            fn.argtypes = [
+                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p,
+            ]
+            _LIBS[mutant] = lib
+        return _LIBS[mutant]
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def topk_transform(mode, scores, score_stride, row_starts, seq_lens, k, *,
+                   out_offsets=None, page_table=None, page_table_stride=0, page_size=1,
+                   batch=None, mutant: int = 0):
+    """Run the oracle on host arrays.
+
+    ``scores`` is a flat (or any contiguous) float32 array; row ``b``'s window
+    begins at element ``b*score_stride + row_starts[b]``. Returns
+    ``(out, out_raw, n_error_rows)`` with ``out``/``out_raw`` int32 ``[batch, k]``.
+    Selected positions are listed in ascending order, then ``-1`` padding.
+    """
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    seq_lens = _i32(seq_lens)
+    row_starts = _i32(row_starts)
+    out_offsets = _i32(out_offsets)
+    page_table = _i32(page_table)
+    if batch is None:
+        batch = int(seq_lens.shape[0])
+    if mode == RAGGED and out_offsets is None:
+        raise ValueError("RAGGED mode needs out_offsets")
+    if mode == PAGED and page_table is None:
+        raise ValueError("PAGED mode needs page_table")
+    out = np.empty((batch, k), dtype=np.int32)
+    out_raw = np.empty((batch, k), dtype=np.int32)
+    errors = _load(mutant).oracle_topk_transform(
+        int(mode), _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens),
+        _ptr(out_offsets), _ptr(page_table), int(page_table_stride), int(page_size),
+        int(batch), int(k), _ptr(out), _ptr(out_raw))
+    return out, out_raw, int(errors)
+
+
+def run_workload(w, rows=None, mutant: int = 0):
+    """Run the oracle on a workload dict (see the package's ``workloads``
+    module), optionally on a subset of rows. Arrays may be torch tensors on any
+    device; they are copied to host numpy first."""
+    def host(x):
+        if x is None:
+            return None
+        if hasattr(x, "detach"):
+            return x.detach().cpu().numpy()
+        return np.asarray(x)
+
+    seq_lens = host(w["seq_lens"])
+    row_starts = host(w.get("row_starts"))
+    out_offsets = host(w.get("out_offsets"))
+    page_table = host(w.get("page_table"))
+    if page_table is not None:
+        page_table = page_table.reshape(-1)
+    scores = host(w["scores"]).reshape(-1)
+    stride = int(w["score_stride"])
+    k = int(w["k"])
+    mode = PAGED if w["mode"] == "paged" else RAGGED
+    if rows is None:
+        return topk_transform(mode, scores, stride, row_starts, seq_lens, k,
+                              out_offsets=out_offsets, page_table=page_table,
+                              page_table_stride=int(w.get("page_table_stride", 0)),
+                              page_size=int(w.get("page_size", 1)), mutant=mutant)
+    rows = np.asarray(rows, dtype=np.int64)
+    outs, raws, errs = [], [], 0
+    for b in rows:
+        b = int(b)
+        base = b * stride
+        o, r, e = topk_transform(
+            mode, scores[base:], 0,
+            None if row_starts is None else row_starts[b:b + 1], seq_lens[b:b + 1], k,
+            out_offsets=None if out_offsets is None else out_offsets[b:b + 1],
+            page_table=None if page_table is None else
+            page_table[b * int(w["page_table_stride"]):(b + 1) * int(w["page_table_stride"])],
+            page_table_stride=int(w.get("page_table_stride", 0)),
+            page_size=int(w.get("page_size", 1)), mutant=mutant)
+        outs.append(o)
+        raws.append(r)
+        errs += e
+    return np.concatenate(outs), np.concatenate(raws), errs

@@ -1,0 +1,163 @@
+// Oracle for the sparse-attention indexer's per-row top-k with its output
+// transform. TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+// benchmark's CPU-baseline leg load it; the library's product path never does.
+//
+// Plain, slow, single-threaded C++17. It shares no code, header, table or
+// helper with the CUDA library. Every step is the plain definition of the
+// result, written out:
+//
+//   * The window of row b is the positions p = 0 .. L-1 of
+//     scores[b * score_stride + row_start + p], with L = seq_lens[b] and
+//     row_start = row_starts[b] (0 when row_starts is null).
+//     (sglang PR #35175 page, "Implementation breakdown" item 2 and the
+//     topk_ragged_kernel snippet: select top-k inside
+//     [row_starts[b], row_starts[b] + seq_lens[b]).)
+//   * When L <= k every position is emitted and no score is read (same
+//     snippet, the "trivial path").
+//   * Otherwise the window is sorted by (score descending, position ascending)
+//     and the first k entries are kept. Scores are ordered by their fp32 bit
+//     pattern mapped to an order-preserving unsigned 32-bit key, a total order
+//     in which -0.0 sorts below +0.0. Equal scores go to the lowest position,
+//     which is the deterministic reading of the tie rule (the PR #26788 page's
+//     test snippet accepts any swap of equal scores; the PR #33006 report names
+//     a deterministic tie-break flag without giving its value).
+//   * RAGGED emit: p + out_offsets[b] (PR #35175 page, "Key source snippets",
+//     TopKProblem::emit adds the bias to every selected index).
+//   * PAGED emit: page_table[b * pt_stride + p / page_size] * page_size
+//     + p % page_size (PR #35175 page, TopKProblem::transform_output through
+//     page_to_indices; page_size = 1 << page_bits).
+//   * Slots past the selected count hold -1, never biased or transformed
+//     (PR #35175 page, "Review highlights": the trivial path cannot reuse a
+//     helper whose -1 padding would pick up the bias).
+//   * Selected positions are written in ascending position order (a canonical
+//     form; the pages do not fix an output order).
+//   * A row with seq_len < 0, or with row_start < 0, is a data error: it is
+//     treated as an empty row (all -1) and counted in the return value (the
+//     PR #35175 page states seq_lens must be non-negative).
+//
+// Parity pins (tests/test_oracle_pins.py): brute-force rank counting on tiny
+// rows, an exhaustive sweep over short vectors with ties and signed zeros,
+// invariants on every workload shape, numpy's partition on the tie-free
+// special case, an independent page-table expansion, and hand-built examples
+// under tests/golden/.
+//
+// ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; it
+// exists only so that a test can show each pin family catches that mistake.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+namespace {
+
+// Order-preserving map from fp32 bits to uint32: a larger float gives a larger
+// key. Negative values have every bit flipped, non-negative values only the
+// sign bit set.
+uint32_t order_key(float x) {
+    uint32_t bits;
+    std::memcpy(&bits, &x, sizeof(bits));
+#if ORACLE_MUTANT == 3
+    // mutant: order by float comparison only (loses -0.0 < +0.0)
+    if (x == 0.0f) bits = 0u;
+#endif
+    if (bits & 0x80000000u) return ~bits;
+    return bits | 0x80000000u;
+}
+
+struct Entry {
+    uint32_t key;
+    int32_t pos;
+};
+
+bool before(const Entry& a, const Entry& b) {
+    if (a.key != b.key) return a.key > b.key;  // larger score first
+#if ORACLE_MUTANT == 1
+    return a.pos > b.pos;  // mutant: ties go to the highest position
+#else
+    return a.pos < b.pos;  // ties go to the lowest position
+#endif
+}
+
+int32_t ragged_index(int32_t p, int32_t offset) { return p + offset; }
+
+int32_t paged_index(const int32_t* pt_row, int32_t page_size, int32_t p) {
+#if ORACLE_MUTANT == 2
+    return pt_row[p / page_size] * page_size + (p + 1) % page_size;  // mutant
+#else
+    return pt_row[p / page_size] * page_size + p % page_size;
+#endif
+}
+
+}  // namespace
+
+extern "C" {
+
+// mode: 0 = RAGGED (out_offsets used), 1 = PAGED (page_table used).
+// scores: host fp32; row b's window starts at scores + b*score_stride + row_start.
+// out, out_raw: [batch, k] int32 (out_raw may be null).
+// Returns the number of rows with a data error (seq_len < 0 or row_start < 0).
+int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_stride,
+                              const int32_t* row_starts, const int32_t* seq_lens,
+                              const int32_t* out_offsets, const int32_t* page_table,
+                              int64_t page_table_stride, int32_t page_size, int32_t batch,
+                              int32_t k, int32_t* out, int32_t* out_raw) {
+    int64_t errors = 0;
+    std::vector<Entry> window;
+    std::vector<int32_t> selected;
+    for (int32_t b = 0; b < batch; ++b) {
+        int32_t L = seq_lens[b];
+        const int32_t start = row_starts ? row_starts[b] : 0;
+        if (L < 0 || start < 0) {
+            ++errors;
+            L = 0;
+        }
+#if ORACLE_MUTANT == 4
+        const float* row = scores + (int64_t)b * score_stride;  // mutant: start ignored
+#else
+        const float* row = scores + (int64_t)b * score_stride + start;
+#endif
+        selected.clear();
+        if (L <= k) {
+            for (int32_t p = 0; p < L; ++p) selected.push_back(p);
+        } else {
+            window.clear();
+#if ORACLE_MUTANT == 5
+            for (int32_t p = 0; p < L - 1; ++p) window.push_back({order_key(row[p]), p});
+#else
+            for (int32_t p = 0; p < L; ++p) window.push_back({order_key(row[p]), p});
+#endif
+            std::sort(window.begin(), window.end(), before);
+            for (int32_t t = 0; t < k && t < (int32_t)window.size(); ++t)
+                selected.push_back(window[t].pos);
+            std::sort(selected.begin(), selected.end());
+        }
+        int32_t* o = out + (int64_t)b * k;
+        int32_t* r = out_raw ? out_raw + (int64_t)b * k : nullptr;
+        for (int32_t t = 0; t < k; ++t) {
+            int32_t value = -1;
+            int32_t raw = -1;
+            if (t < (int32_t)selected.size()) {
+                raw = selected[t];
+                if (mode == 1)
+                    value = paged_index(page_table + (int64_t)b * page_table_stride, page_size, raw);
+                else
+                    value = ragged_index(raw, out_offsets[b]);
+            }
+#if ORACLE_MUTANT == 6
+            else if (mode == 0) {
+                value = -1 + out_offsets[b];  // mutant: padding picks up the bias
+            }
+#endif
+            o[t] = value;
+            if (r) r[t] = raw;
+        }
+    }
+    return errors;
+}
+
+}  // extern "C"

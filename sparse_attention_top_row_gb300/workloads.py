@@ -1,0 +1,261 @@
+"""Seeded synthetic inputs for the indexer top-k + transform.
+
+This module only draws random inputs; it holds none of the selection or
+transform arithmetic. The tests feed the same tensors to the CUDA library and
+to the CPU oracle, and the benchmark times the library on them.
+
+Every generator takes a ``device`` (``"cpu"`` or ``"cuda"``) and a seed; a
+seeded ``torch.Generator`` on that device draws the values, so a given
+(device, seed) always yields the same bytes. Seeds follow
+``20260000 + workload_id * 100 + sub_id``.
+
+A workload is a plain dict:
+
+    mode            "paged" | "ragged"
+    k               int, 1..2048
+    scores          float32 tensor; row b's window begins at element
+                    b*score_stride + row_starts[b] of its flattened storage
+    score_stride    int (elements; a multiple of 4, 0 = all rows share one buffer)
+    row_starts      int32 [B] or None (None = every window starts at 0)
+    seq_lens        int32 [B]
+    out_offsets     int32 [B] (RAGGED) or None
+    page_table      int32 [B, P] (PAGED) or None
+    page_table_stride, page_size
+    batch           B
+    name            short description
+
+Scores outside every window hold the sentinel 1e3, so a window leak would win
+the selection (the sentinel design of the sglang PR #35175 page's tests).
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+SENTINEL = 1.0e3
+SEED_BASE = 20260000
+
+
+def seed_for(workload_id: int, sub_id: int = 0) -> int:
+    return SEED_BASE + workload_id * 100 + sub_id
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _i32(x):
+    return x.to(torch.int32).contiguous()
+
+
+def ragged_tiny(device="cpu", sub_id=0, batch=8, k=512, max_len=4096):
+    """Eight windows packed back to back in one fp32 buffer (stride 0).
+
+    seq_lens ~ U{1..max_len}; row_starts = exclusive prefix sum (so the
+    residues mod 4 vary); out_offsets = row_starts; N(0,1) scores inside the
+    windows; the 1e3 sentinel after the last window, padding the buffer to a
+    multiple of 4 plus 64 floats of slack.
+    """
+    g = _gen(device, seed_for(1, sub_id))
+    seq_lens = torch.randint(1, max_len + 1, (batch,), generator=g, device=device)
+    starts = torch.zeros(batch, dtype=torch.int64, device=device)
+    starts[1:] = torch.cumsum(seq_lens, 0)[:-1]
+    total = int(seq_lens.sum().item())
+    n = (total + 3) // 4 * 4 + 64
+    scores = torch.full((n,), SENTINEL, dtype=torch.float32, device=device)
+    scores[:total] = torch.randn(total, generator=g, device=device)
+    return dict(name=f"ragged tiny B={batch} k={k}", mode="ragged", k=k, scores=scores,
+                score_stride=0, row_starts=_i32(starts), seq_lens=_i32(seq_lens),
+                out_offsets=_i32(starts), page_table=None, page_table_stride=0,
+                page_size=1, batch=batch)
+
+
+def paged_decode(device="cpu", sub_id=0, batch=128, seq_len=8192, k=2048, page_size=64):
+    """[batch, seq_len] N(0,1) scores, one full window per row, and a page
+    table holding a seeded random permutation of batch*seq_len/page_size
+    physical pages."""
+    g = _gen(device, seed_for(2, sub_id))
+    scores = torch.randn(batch, seq_len, generator=g, device=device)
+    pages = seq_len // page_size
+    table = torch.randperm(batch * pages, generator=g, device=device).view(batch, pages)
+    seq_lens = torch.full((batch,), seq_len, dtype=torch.int32, device=device)
+    return dict(name=f"paged decode B={batch} L={seq_len} k={k} ps={page_size}", mode="paged",
+                k=k, scores=scores, score_stride=seq_len, row_starts=None, seq_lens=seq_lens,
+                out_offsets=None, page_table=_i32(table), page_table_stride=pages,
+                page_size=page_size, batch=batch)
+
+
+def ragged_extend(device="cpu", chunk=0, rows_per_chunk=1024, n_req=4, prefix=28672, new=4096,
+                  k=2048, outlier_frac=0.01, outlier_value=4.0):
+    """One chunk of a prefill-extend problem.
+
+    ``n_req`` requests, each with a ``prefix``-token cached prefix and ``new``
+    new tokens, give ``n_req*new`` causal query rows. Query i of request r has
+    seq_len = prefix+i+1 and row_start = r*(prefix+new) in a flattened KV row
+    space of n_req*(prefix+new) columns (the row stride). out_offsets =
+    row_start. Window scores are N(0,1) with ``outlier_frac`` of them set to
+    exactly ``outlier_value``; every other column holds the 1e3 sentinel.
+    Chunk c covers global rows c*rows_per_chunk ... and is generated from its
+    own seed, so any chunk can be drawn alone.
+    """
+    g = _gen(device, seed_for(3, chunk))
+    stride = n_req * (prefix + new)
+    rows = torch.arange(chunk * rows_per_chunk, (chunk + 1) * rows_per_chunk, device=device)
+    req = rows // new
+    qi = rows % new
+    seq_lens = prefix + qi + 1
+    starts = req * (prefix + new)
+    cols = torch.arange(stride, device=device)
+    inside = (cols[None, :] >= starts[:, None]) & (cols[None, :] < (starts + seq_lens)[:, None])
+    vals = torch.randn(rows_per_chunk, stride, generator=g, device=device)
+    outl = torch.rand(rows_per_chunk, stride, generator=g, device=device) < outlier_frac
+    vals = torch.where(outl, torch.full_like(vals, outlier_value), vals)
+    scores = torch.where(inside, vals, torch.full_like(vals, SENTINEL))
+    del vals, outl, inside
+    return dict(name=f"ragged extend chunk={chunk} rows={rows_per_chunk} req={n_req} "
+                     f"prefix={prefix} new={new} k={k}",
+                mode="ragged", k=k, scores=scores, score_stride=stride, row_starts=_i32(starts),
+                seq_lens=_i32(seq_lens), out_offsets=_i32(starts), page_table=None,
+                page_table_stride=0, page_size=1, batch=rows_per_chunk)
+
+
+def paged_long(device="cpu", sub_id=0, batch=1, seq_len=131072, k=2048, page_size=64, scale=0.1):
+    """Few long PAGED rows whose scores are 0.1*N(0,1) rounded to
+    bf16-representable values (heavy exact ties near the threshold)."""
+    g = _gen(device, seed_for(4, sub_id))
+    scores = (scale * torch.randn(batch, seq_len, generator=g, device=device))
+    scores = scores.to(torch.bfloat16).to(torch.float32)
+    pages = seq_len // page_size
+    table = torch.randperm(batch * pages, generator=g, device=device).view(batch, pages)
+    seq_lens = torch.full((batch,), seq_len, dtype=torch.int32, device=device)
+    return dict(name=f"paged long B={batch} L={seq_len} k={k} bf16 ties", mode="paged", k=k,
+                scores=scores, score_stride=seq_len, row_starts=None, seq_lens=seq_lens,
+                out_offsets=None, page_table=_i32(table), page_table_stride=pages,
+                page_size=page_size, batch=batch)
+
+
+BOUNDARY_LENGTHS = (8192, 8193, 16384, 16385, 65535, 65536, 65537)
+
+
+def boundary_lengths(k):
+    return (k, k + 1) + BOUNDARY_LENGTHS
+
+
+def mixed(device="cpu", mode="paged", k=2048, batch=129, sub_id=0, max_len=131072, min_len=256,
+          page_size=64, boundary=True, boundary_index=None):
+    """Mixed-length sweep in one launch.
+
+    seq_lens are log-uniform in [min_len, max_len]; rows 0..min(9,B)-1 are
+    overwritten with the boundary lengths k, k+1, 8192, 8193, 16384, 16385,
+    65535, 65536, 65537 (clipped to max_len). With ``boundary_index`` set the
+    single row takes that boundary length. PAGED: stride max_len, windows start
+    at 0, page table [B, max_len/page_size] = a random permutation. RAGGED:
+    stride max_len+4, row_starts ~ U{0..3}, out_offsets = b*stride + row_start.
+    N(0,1) inside windows, the 1e3 sentinel outside.
+    """
+    g = _gen(device, seed_for(5, sub_id))
+    u = torch.rand(batch, generator=g, device=device, dtype=torch.float64)
+    lo, hi = math.log(min_len), math.log(max_len)
+    seq_lens = torch.round(torch.exp(lo + u * (hi - lo))).to(torch.int64)
+    blen = [min(x, max_len) for x in boundary_lengths(k)]
+    if boundary_index is not None:
+        seq_lens[0] = blen[boundary_index]
+    elif boundary:
+        n = min(len(blen), batch)
+        seq_lens[:n] = torch.tensor(blen[:n], device=device)
+    if mode == "paged":
+        stride = max_len
+        starts = torch.zeros(batch, dtype=torch.int64, device=device)
+    else:
+        stride = max_len + 4
+        starts = torch.randint(0, 4, (batch,), generator=g, device=device)
+    cols = torch.arange(stride, device=device)
+    inside = (cols[None, :] >= starts[:, None]) & (cols[None, :] < (starts + seq_lens)[:, None])
+    vals = torch.randn(batch, stride, generator=g, device=device)
+    scores = torch.where(inside, vals, torch.full_like(vals, SENTINEL))
+    del vals, inside
+    w = dict(name=f"mixed {mode} B={batch} k={k} max_len={max_len}", mode=mode, k=k,
+             scores=scores, score_stride=stride, seq_lens=_i32(seq_lens), batch=batch,
+             page_size=page_size)
+    if mode == "paged":
+        pages = (max_len + page_size - 1) // page_size
+        table = torch.randperm(batch * pages, generator=g, device=device).view(batch, pages)
+        w.update(row_starts=None, out_offsets=None, page_table=_i32(table),
+                 page_table_stride=pages)
+    else:
+        offs = torch.arange(batch, device=device) * stride + starts
+        w.update(row_starts=_i32(starts), out_offsets=_i32(offs), page_table=None,
+                 page_table_stride=0, page_size=1)
+    return w
+
+
+def custom(mode, k, rows, *, device="cpu", score_stride=None, row_starts=None, out_offsets=None,
+           page_size=1, page_table=None, seed=0):
+    """Build a workload from explicit per-row score lists (small edge cases).
+
+    ``rows`` is a list of float lists; row b's window is rows[b] placed at
+    row_starts[b] (default 0) of a row of ``score_stride`` elements (default:
+    the longest window + start, rounded up to a multiple of 4). Outside the
+    windows the sentinel is stored. PAGED without a table gets a seeded random
+    permutation.
+    """
+    B = len(rows)
+    starts = list(row_starts) if row_starts is not None else [0] * B
+    need = max([s + len(r) for s, r in zip(starts, rows)] + [1])
+    if score_stride is None:
+        score_stride = (need + 3) // 4 * 4
+    flat = torch.full((max(B, 1) * score_stride + 64,), SENTINEL, dtype=torch.float32)
+    for b, (s, r) in enumerate(zip(starts, rows)):
+        if len(r):
+            base = b * score_stride + max(s, 0)
+            flat[base:base + len(r)] = torch.tensor(r, dtype=torch.float32)
+    seq_lens = torch.tensor([len(r) for r in rows], dtype=torch.int32)
+    w = dict(name="custom", mode=mode, k=k, scores=flat.to(device), score_stride=score_stride,
+             seq_lens=seq_lens.to(device), batch=B, page_size=page_size,
+             row_starts=torch.tensor(starts, dtype=torch.int32, device=device)
+             if row_starts is not None else None)
+    if mode == "paged":
+        pages = max((need + page_size - 1) // page_size, 1)
+        if page_table is None:
+            g = _gen("cpu", seed)
+            page_table = torch.randperm(B * pages, generator=g).view(B, pages)
+        page_table = torch.as_tensor(page_table, dtype=torch.int32)
+        w.update(page_table=page_table.contiguous().to(device),
+                 page_table_stride=int(page_table.shape[1]), out_offsets=None)
+    else:
+        offs = out_offsets if out_offsets is not None else [0] * B
+        w.update(out_offsets=torch.tensor(offs, dtype=torch.int32, device=device),
+                 page_table=None, page_table_stride=0)
+    return w
+
+
+def to_device(w, device):
+    """Copy every tensor of a workload to ``device``."""
+    return {key: (val.to(device) if isinstance(val, torch.Tensor) else val) for key, val in w.items()}
+
+
+def select_rows(w, rows):
+    """A workload holding only ``rows`` of ``w`` (each row's slice of the
+    score storage is copied, with the sentinel-filled remainder of its
+    stride). Stride-0 workloads keep the whole shared buffer."""
+    rows = [int(r) for r in rows]
+    idx = torch.tensor(rows, dtype=torch.long, device=w["seq_lens"].device)
+    stride = int(w["score_stride"])
+    flat = w["scores"].reshape(-1)
+    if stride == 0:
+        scores = flat.clone()
+    else:
+        scores = torch.stack([flat[r * stride:(r + 1) * stride] for r in rows]).reshape(-1)
+    out = dict(w)
+    out.update(scores=scores, batch=len(rows), seq_lens=w["seq_lens"][idx].clone(),
+               name=w["name"] + f" rows={rows[:4]}...")
+    for key in ("row_starts", "out_offsets"):
+        if w.get(key) is not None:
+            out[key] = w[key][idx].clone()
+    if w.get("page_table") is not None:
+        out["page_table"] = w["page_table"][idx].clone()
+    return out

@@ -1,0 +1,195 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+* hand-built examples worked from the pages' definitions (tests/golden/);
+* brute-force rank counting on random tiny rows, both modes;
+* an exhaustive sweep of short vectors over {-1, -0.0, 0.0, 1, 2} (ties and
+  signed zeros) for every k up to the length;
+* numpy.partition on tie-free rows (a library routine on a special case);
+* an independent page-table expansion for the PAGED transform;
+* invariants on scaled-down versions of every workload shape;
+* planted mistakes in the oracle (compiled variants) are each caught.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_top_row_gb300 import workloads as wl
+from topk_checks import HostWorkload, brute_force_select, check_row_invariants, expand_page_table
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
+
+
+def _golden_workload(case):
+    mode = case["mode"]
+    if "buffer" in case:
+        buf = np.asarray(case["buffer"], dtype=np.float32)
+        return dict(mode=mode, k=case["k"], scores=torch.from_numpy(buf),
+                    score_stride=case["score_stride"],
+                    row_starts=torch.tensor(case["row_starts"], dtype=torch.int32),
+                    seq_lens=torch.tensor(case["seq_lens"], dtype=torch.int32),
+                    out_offsets=torch.tensor(case["out_offsets"], dtype=torch.int32),
+                    page_table=None, page_table_stride=0, page_size=1,
+                    batch=len(case["seq_lens"]), name=case["name"])
+    return wl.custom(mode, case["k"], case["rows"], page_size=case.get("page_size", 1),
+                     page_table=case.get("page_table"))
+
+
+def golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+# ------------------------------------------------------------------ pin families
+
+def pin_golden(mutant=0):
+    for case in golden_cases():
+        w = _golden_workload(case)
+        out, raw, _ = oracle.run_workload(w, mutant=mutant)
+        assert np.sort(out, axis=1).tolist() == case["det"], case["name"]
+        assert np.sort(raw, axis=1).tolist() == case["det_raw"], case["name"]
+
+
+def pin_bruteforce(mutant=0, seed=1, n_rows=300):
+    rng = np.random.default_rng(seed)
+    for trial in range(6):
+        mode = "paged" if trial % 2 else "ragged"
+        k = int(rng.choice([1, 2, 3, 5, 8, 16, 33, 64]))
+        rows, starts = [], []
+        for _ in range(n_rows // 6):
+            L = int(rng.integers(0, 65))
+            if trial % 3 == 0:
+                vals = rng.choice([-2.0, -1.0, -0.0, 0.0, 0.5, 1.0, 3.0], size=L)
+            else:
+                vals = rng.standard_normal(L).astype(np.float32)
+            rows.append([float(v) for v in vals])
+            starts.append(int(rng.integers(0, 7)))
+        offs = [int(x) for x in rng.integers(-5, 1000, size=len(rows))]
+        ps = int(rng.choice([1, 2, 4, 8]))
+        w = wl.custom(mode, k, rows, row_starts=starts, out_offsets=offs, page_size=ps,
+                      seed=seed + trial)
+        hw = HostWorkload(w)
+        out, raw, err = oracle.run_workload(w, mutant=mutant)
+        assert err == 0
+        for b, r in enumerate(rows):
+            L = len(r)
+            if L == 0:
+                expect = np.zeros(0, dtype=np.int64)
+            else:
+                expect = np.nonzero(brute_force_select(np.asarray([hw.window(b)]), k)[0])[0]
+            got = raw[b][raw[b] >= 0]
+            np.testing.assert_array_equal(np.sort(got), expect, err_msg=f"trial {trial} row {b}")
+            np.testing.assert_array_equal(np.sort(out[b][raw[b] >= 0]), np.sort(hw.transform(b, expect)))
+            assert np.all(out[b][raw[b] < 0] == -1)
+
+
+def pin_exhaustive(mutant=0, max_n=8):
+    alphabet = np.array([-1.0, -0.0, 0.0, 1.0, 2.0], dtype=np.float32)
+    for n in range(1, max_n + 1):
+        combos = np.array(list(itertools.product(range(len(alphabet)), repeat=n)), dtype=np.int64)
+        vals = alphabet[combos]                      # [R, n]
+        R = vals.shape[0]
+        scores = np.ascontiguousarray(vals.reshape(-1))
+        seq_lens = np.full(R, n, dtype=np.int32)
+        offs = np.zeros(R, dtype=np.int32)
+        for k in range(1, n + 1):
+            out, raw, _ = oracle.topk_transform(oracle.RAGGED, scores, n, None, seq_lens, k,
+                                                out_offsets=offs, mutant=mutant)
+            expect = brute_force_select(vals, k)
+            got = np.zeros((R, n), dtype=bool)
+            rows = np.repeat(np.arange(R), k)
+            sel = raw.reshape(-1)
+            valid = sel >= 0
+            got[rows[valid], sel[valid]] = True
+            bad = np.nonzero((got != expect).any(1))[0]
+            assert bad.size == 0, f"n={n} k={k}: first bad row {vals[bad[0]].tolist()}"
+
+
+def pin_partition(mutant=0, seed=3):
+    rng = np.random.default_rng(seed)
+    for L, k in [(100, 7), (1000, 100), (5000, 2048), (3000, 1)]:
+        # distinct magnitudes with random signs
+        x = np.stack([rng.permutation(np.arange(1, L + 1)) * rng.choice([-1.0, 1.0], size=L) / 64.0
+                      for _ in range(4)]).astype(np.float32)
+        # tie-free and no zeros: the special case where plain numeric order is the order
+        assert all(np.unique(r).size == L for r in x) and not np.any(x == 0)
+        out, raw, _ = oracle.topk_transform(oracle.RAGGED, x.reshape(-1), L, None,
+                                            np.full(4, L, np.int32), k,
+                                            out_offsets=np.zeros(4, np.int32), mutant=mutant)
+        for b in range(4):
+            kth = -np.partition(-x[b], k - 1)[k - 1]            # k-th largest, by library routine
+            expect = np.nonzero(x[b] >= kth)[0]
+            np.testing.assert_array_equal(np.sort(raw[b]), expect)
+
+
+def pin_paged_expansion(mutant=0, seed=4):
+    for ps in (1, 2, 64, 256):
+        w = wl.custom("paged", 37, [list(np.random.default_rng(seed + ps).standard_normal(700))
+                                   for _ in range(5)], page_size=ps, seed=ps)
+        out, raw, _ = oracle.run_workload(w, mutant=mutant)
+        pt = w["page_table"].numpy()
+        for b in range(5):
+            phys = expand_page_table(pt[b], ps, 700)
+            np.testing.assert_array_equal(out[b], phys[raw[b]])
+            # inverting the table maps every physical slot back to its position
+            inv = {int(s): p for p, s in enumerate(phys)}
+            assert [inv[int(s)] for s in out[b]] == raw[b].tolist()
+
+
+def pin_invariants(mutant=0):
+    cases = [
+        wl.ragged_tiny("cpu", sub_id=0),
+        wl.paged_decode("cpu", batch=8, seq_len=2048, k=256),
+        wl.ragged_extend("cpu", chunk=0, rows_per_chunk=16, n_req=2, prefix=1000, new=24, k=200),
+        wl.paged_long("cpu", batch=2, seq_len=8192, k=512),
+        wl.mixed("cpu", mode="ragged", k=64, batch=12, max_len=4000, min_len=16),
+        wl.mixed("cpu", mode="paged", k=64, batch=12, max_len=4000, min_len=16),
+    ]
+    for w in cases:
+        hw = HostWorkload(w)
+        before = hw.scores.copy()
+        out, raw, err = oracle.run_workload(w, mutant=mutant)
+        assert err == 0
+        for b in range(hw.batch):
+            check_row_invariants(hw, b, out[b], raw[b])
+        np.testing.assert_array_equal(hw.scores.view(np.uint32), before.view(np.uint32))
+
+
+PINS = [pin_golden, pin_bruteforce, pin_exhaustive, pin_partition, pin_paged_expansion, pin_invariants]
+
+
+# ------------------------------------------------------------------ tests
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin()
+
+
+def test_error_rows_are_empty_and_counted():
+    w = wl.custom("ragged", 2, [[1.0, 2.0, 3.0], [4.0, 5.0, 6.0], [7.0, 8.0, 9.0]],
+                  out_offsets=[0, 10, 20])
+    w["seq_lens"] = torch.tensor([3, -1, 3], dtype=torch.int32)
+    w["row_starts"] = torch.tensor([0, 0, -4], dtype=torch.int32)
+    out, raw, err = oracle.run_workload(w)
+    assert err == 2
+    assert out[1].tolist() == [-1, -1] and out[2].tolist() == [-1, -1]
+    assert sorted(out[0].tolist()) == [1, 2]
+
+
+def test_planted_mistakes_are_caught():
+    """Each planted mistake in the oracle fails at least one pin family."""
+    for mutant in range(1, 7):
+        caught = []
+        for pin in PINS:
+            try:
+                pin(mutant=mutant)
+            except AssertionError:
+                caught.append(pin.__name__)
+        assert caught, f"mutant {mutant} passed every pin"

@@ -1,0 +1,184 @@
+/*
+ * Sparse-attention indexer top-k with its fused output transform, for one
+ * NVIDIA GB300 GPU (sm_103a). C ABI.
+ *
+ * What it computes. Each row b owns the window of fp32 scores
+ *   scores[b * score_stride + row_starts[b] + p],  p = 0 .. seq_lens[b]-1
+ * and keeps the k <= 2048 largest of them (sglang PR #35175 page,
+ * "Implementation breakdown" item 2; "#26788 [JIT Kernel] DeepSeek-V4 DSA
+ * indexer: faster top-k + page-table transform (runtime k <= 2048)" page,
+ * "Executive summary"). Each kept position p is written transformed:
+ *   PAGED : page_table[b * page_table_stride + p / page_size] * page_size
+ *           + p % page_size   (PR #35175 page, "Key source snippets",
+ *                              TopKProblem::transform_output / page_to_indices)
+ *   RAGGED: p + out_offsets[b] (PR #35175 page, "Key source snippets",
+ *                               TopKProblem::emit with its bias field)
+ * When seq_lens[b] <= k every position is written and no score is read; the
+ * remaining slots of the row hold -1, never transformed (PR #35175 page,
+ * topk_ragged_kernel's trivial path and "Review highlights").
+ *
+ * Order. Scores compare by an order-preserving map of their fp32 bit pattern
+ * to uint32 (a total order: -0.0 < +0.0; NaNs sort beyond +/-inf). In default
+ * mode any maximal set is returned: the multiset of selected score bit
+ * patterns is unique, and two results may differ only by swapping positions of
+ * equal scores. With TOPK_DETERMINISTIC the lowest positions win among equal
+ * scores, so the set is unique. The order of the k slots within a row is
+ * unspecified.
+ *
+ * Memory. Every pointer argument is a DEVICE pointer unless stated otherwise.
+ * The library never allocates; the caller owns all buffers. Work is enqueued
+ * on `stream` (a cudaStream_t; NULL = the legacy default stream) and the calls
+ * return without waiting for it. Scores are read only and never written.
+ *
+ * Errors. Argument errors are found on the host before anything is enqueued
+ * and returned as a topk_status; the call then has no effect. A failed launch
+ * returns TOPK_ERR_CUDA and leaves the CUDA error for cudaGetLastError().
+ * Per-row data errors found on the device (seq_len < 0, row_start < 0) make
+ * that row empty (all -1) and are counted in the workspace; read the count
+ * with topk_read_device_errors().
+ */
+#ifndef SPARSE_ATTENTION_TOP_ROW_GB300_TOPK_H
+#define SPARSE_ATTENTION_TOP_ROW_GB300_TOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TOPK_API __attribute__((visibility("default")))
+
+/* The largest k (the pages' runtime bound, "runtime k <= 2048"). */
+#define TOPK_MAX_K 2048
+/* The largest supported page size (a power of two). */
+#define TOPK_MAX_PAGE_SIZE (1 << 19)
+
+typedef struct CUstream_st* topk_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    TOPK_OK = 0,
+    TOPK_ERR_ARG = 1,       /* a required pointer is null, batch < 0, a stride is negative or
+                               score_stride is not a multiple of 4 */
+    TOPK_ERR_ALIGN = 2,     /* scores is not 16-byte aligned */
+    TOPK_ERR_K = 3,         /* k outside [1, TOPK_MAX_K] */
+    TOPK_ERR_PAGE_SIZE = 4, /* page_size is not a power of two in [1, TOPK_MAX_PAGE_SIZE] */
+    TOPK_ERR_WORKSPACE = 5, /* workspace is null or smaller than topk_workspace_bytes(batch) */
+    TOPK_ERR_CUDA = 6       /* a CUDA call failed; cudaGetLastError() names the cause */
+} topk_status;
+
+/* flags bits */
+#define TOPK_DETERMINISTIC 1u /* equal scores: lowest positions win */
+
+/* bits of the device flags word read by topk_read_device_errors */
+#define TOPK_DEVICE_FLAG_PLAN_MISMATCH 1u /* a transform found no plan for its (batch, k) and
+                                             processed every row without one */
+#define TOPK_DEVICE_FLAG_INTERNAL 2u      /* an internal consistency check failed (a library
+                                             bug): an output slot index was out of range and
+                                             the write was dropped */
+
+/*
+ * Bytes of device workspace that topk_plan and the transforms need for
+ * `batch` rows (a small header plus two int32 lists of `batch` entries).
+ * Host only, pure. Returns 0 for batch < 0.
+ */
+TOPK_API size_t topk_workspace_bytes(int32_t batch);
+
+/*
+ * Plan: route every row by its length, once per set of seq_lens.
+ * Counterpart of plan_topk_v2 / TopKKernel::plan ("#26788 [JIT Kernel]"
+ * page, "Implementation breakdown": a plan kernel emits the metadata that the
+ * transform dispatches on; "Key source snippets", topk.py).
+ *
+ *   seq_lens   int32 [batch], device. Negative entries are data errors
+ *              (counted; those rows come out empty).
+ *   batch      rows, >= 0.
+ *   k          1 .. TOPK_MAX_K; must equal the k later given to the transform.
+ *   workspace  device buffer of at least topk_workspace_bytes(batch) bytes,
+ *              caller-owned; this call overwrites it. Any alignment of 16 B
+ *              or more.
+ *
+ * One small kernel on `stream`. The plan sorts rows into length bands
+ * (longest first) and, for small batches, hands rows longer than 32768 to a
+ * thread-block-cluster path that splits each such row over 8 SMs. A
+ * transform run after it on the same stream (or otherwise ordered after it)
+ * consumes the plan; one plan serves any number of transforms with the same
+ * seq_lens, batch and k (e.g. every layer of a decode step). A transform whose
+ * (batch, k) does not match the plan sets TOPK_DEVICE_FLAG_PLAN_MISMATCH and
+ * still computes the right result, without the cluster path.
+ */
+TOPK_API int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace,
+                       size_t workspace_bytes, topk_stream_t stream);
+
+/*
+ * PAGED top-k + page-table transform (decode).
+ * Counterpart of topk_transform_paged / topk_transform_512_v2 ("#26788 [JIT
+ * Kernel]" page, "Key source snippets", topk.py; renamed on the PR #35175
+ * page, "Implementation breakdown" item 3).
+ *
+ *   scores            fp32, device, 16-byte aligned. Row b starts at
+ *                     scores + b*score_stride; its window at + row_starts[b].
+ *                     For every row the 16-byte-aligned span covering the
+ *                     window, [floor4(start), ceil4(start + seq_len)), must lie
+ *                     inside the allocation.
+ *   score_stride      elements between rows; >= 0 and a multiple of 4
+ *                     (0: all rows share one buffer).
+ *   row_starts        int32 [batch] or NULL (NULL: every window starts at 0).
+ *                     The logical position p counts from the window start.
+ *   seq_lens          int32 [batch], the same values the plan saw.
+ *   page_table        int32, row b at page_table + b*page_table_stride; it must
+ *                     hold ceil(seq_len / page_size) valid entries, and
+ *                     page * page_size + page_size - 1 must fit int32.
+ *   page_table_stride elements between page-table rows, >= 0.
+ *   page_size         a power of two, 1 .. TOPK_MAX_PAGE_SIZE.
+ *   batch, k          as given to topk_plan.
+ *   workspace         the buffer topk_plan filled (the transform adds to its
+ *                     device error count); at least topk_workspace_bytes(batch).
+ *   out               int32 [batch, k], row-major; every slot is written.
+ *   out_raw           int32 [batch, k] or NULL: the untransformed positions p
+ *                     in the same slots as `out` (-1 in the padding).
+ *   flags             0 or TOPK_DETERMINISTIC.
+ */
+TOPK_API int topk_transform_paged(const float* scores, int64_t score_stride,
+                                  const int32_t* row_starts, const int32_t* seq_lens,
+                                  const int32_t* page_table, int64_t page_table_stride,
+                                  int32_t page_size, int32_t batch, int32_t k, void* workspace,
+                                  size_t workspace_bytes, int32_t* out, int32_t* out_raw,
+                                  uint32_t flags, topk_stream_t stream);
+
+/*
+ * RAGGED top-k + offset transform (prefill / extend).
+ * Counterpart of topk_transform_ragged_v2 / topk_ragged_kernel (PR #35175
+ * page, "Implementation breakdown" items 2-3 and "Key source snippets").
+ * Arguments as for topk_transform_paged, with
+ *   out_offsets  int32 [batch]: added to every selected position of row b.
+ *                out_offsets[b] + seq_len - 1 must fit int32. With
+ *                out_offsets == row_starts the outputs are absolute
+ *                positions in the flattened KV.
+ * Unlike the pages' kernel, the scores buffer is never written: window heads
+ * that are not 16-byte aligned are excluded by position, not masked in place.
+ */
+TOPK_API int topk_transform_ragged(const float* scores, int64_t score_stride,
+                                   const int32_t* row_starts, const int32_t* seq_lens,
+                                   const int32_t* out_offsets, int32_t batch, int32_t k,
+                                   void* workspace, size_t workspace_bytes, int32_t* out,
+                                   int32_t* out_raw, uint32_t flags, topk_stream_t stream);
+
+/*
+ * Reads the workspace's device error count (rows with seq_len < 0 seen by the
+ * plan, plus rows with row_start < 0 seen by each transform since the plan)
+ * and the device flags word into HOST memory. Synchronises `stream`.
+ *   host_error_rows  host int32*, required.
+ *   host_flags       host uint32*, or NULL.
+ */
+TOPK_API int topk_read_device_errors(const void* workspace, int32_t* host_error_rows,
+                                     uint32_t* host_flags, topk_stream_t stream);
+
+/* A static, human-readable name for a topk_status value. Host only. */
+TOPK_API const char* topk_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTENTION_TOP_ROW_GB300_TOPK_H */

@@ -1,0 +1,158 @@
+"""Sparse-attention indexer top-k + transform on GB300: Python binding.
+
+Thin ctypes marshalling over the C ABI of ``include/topk.h`` (the
+``_build/libtopk.so`` library): the functions take torch CUDA tensors, pass
+their device pointers and the current CUDA stream, and raise on a non-zero
+status. Every step of the computation runs in the library's CUDA kernels;
+there is no fallback of any kind, and calling without the built library
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import workloads  # noqa: F401  (seeded synthetic inputs)
+
+TOPK_MAX_K = 2048
+TOPK_DETERMINISTIC = 1
+TOPK_DEVICE_FLAG_PLAN_MISMATCH = 1
+TOPK_DEVICE_FLAG_INTERNAL = 2
+
+STATUS = {0: "TOPK_OK", 1: "TOPK_ERR_ARG", 2: "TOPK_ERR_ALIGN", 3: "TOPK_ERR_K",
+          4: "TOPK_ERR_PAGE_SIZE", 5: "TOPK_ERR_WORKSPACE", 6: "TOPK_ERR_CUDA"}
+
+_LIB = None
+_LOCK = threading.Lock()
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
+
+EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_ragged",
+            "topk_read_device_errors", "topk_status_string")
+
+
+class TopKError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads the built library (``build()`` in ``__graft_entry__`` or
+    ``python -m sparse_attention_top_row_gb300.build`` makes it)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing")
+        import torch  # noqa: F401  (loads the shared CUDA runtime first)
+        lib = ctypes.CDLL(path)
+        c_i32, c_i64, c_u32, c_sz, c_p = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                          ctypes.c_size_t, ctypes.c_void_p)
+        lib.topk_workspace_bytes.restype = c_sz
+        lib.topk_workspace_bytes.argtypes = [c_i32]
+        lib.topk_plan.restype = ctypes.c_int
+        lib.topk_plan.argtypes = [c_p, c_i32, c_i32, c_p, c_sz, c_p]
+        lib.topk_transform_paged.restype = ctypes.c_int
+        lib.topk_transform_paged.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_i32,
+                                             c_p, c_sz, c_p, c_p, c_u32, c_p]
+        lib.topk_transform_ragged.restype = ctypes.c_int
+        lib.topk_transform_ragged.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32,
+                                              c_p, c_sz, c_p, c_p, c_u32, c_p]
+        lib.topk_read_device_errors.restype = ctypes.c_int
+        lib.topk_read_device_errors.argtypes = [c_p, ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_p]
+        lib.topk_status_string.restype = ctypes.c_char_p
+        lib.topk_status_string.argtypes = [ctypes.c_int]
+        _LIB = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise TopKError(fn, status)
+
+
+def topk_workspace_bytes(batch: int) -> int:
+    return int(load().topk_workspace_bytes(int(batch)))
+
+
+def new_workspace(batch: int, device="cuda"):
+    """A workspace tensor of topk_workspace_bytes(batch) bytes (torch owns it)."""
+    import torch
+    return torch.empty(topk_workspace_bytes(batch), dtype=torch.uint8, device=device)
+
+
+def topk_plan(seq_lens, k: int, workspace, stream=None):
+    lib = load()
+    batch = int(seq_lens.numel())
+    _check("topk_plan", lib.topk_plan(_ptr(seq_lens), batch, int(k), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def topk_transform_paged(scores, score_stride: int, row_starts, seq_lens, page_table,
+                         page_table_stride: int, page_size: int, k: int, workspace, out,
+                         out_raw=None, flags: int = 0, stream=None):
+    lib = load()
+    batch = int(seq_lens.numel())
+    _check("topk_transform_paged", lib.topk_transform_paged(
+        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(page_table),
+        int(page_table_stride), int(page_size), batch, int(k), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_raw), int(flags),
+        _stream(stream)))
+
+
+def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int,
+                          workspace, out, out_raw=None, flags: int = 0, stream=None):
+    lib = load()
+    batch = int(seq_lens.numel())
+    _check("topk_transform_ragged", lib.topk_transform_ragged(
+        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(out_offsets),
+        batch, int(k), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(out_raw), int(flags), _stream(stream)))
+
+
+def topk_read_device_errors(workspace, stream=None):
+    """Returns (error_rows, flags); synchronises the stream."""
+    lib = load()
+    n = ctypes.c_int32(0)
+    f = ctypes.c_uint32(0)
+    _check("topk_read_device_errors",
+           lib.topk_read_device_errors(_ptr(workspace), ctypes.byref(n), ctypes.byref(f), _stream(stream)))
+    return int(n.value), int(f.value)
+
+
+def run_workload(w, out=None, out_raw=None, workspace=None, flags: int = 0, plan: bool = True,
+                 stream=None):
+    """Plan + transform on a workload dict whose tensors are on the GPU.
+    Returns (out, out_raw, workspace)."""
+    import torch
+    dev = w["scores"].device
+    B, k = int(w["batch"]), int(w["k"])
+    if out is None:
+        out = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(B, dev)
+    if plan:
+        topk_plan(w["seq_lens"], k, workspace, stream=stream)
+    if w["mode"] == "paged":
+        topk_transform_paged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                             w["page_table"], w["page_table_stride"], w["page_size"], k, workspace,
+                             out, out_raw, flags, stream=stream)
+    else:
+        topk_transform_ragged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                              w["out_offsets"], k, workspace, out, out_raw, flags, stream=stream)
+    return out, out_raw, workspace

@@ -1,0 +1,1032 @@
+// Sparse-attention indexer top-k + output transform for GB300 (sm_103a).
+//
+// The kernels here select, for every row, the k <= 2048 largest fp32 scores of
+// a window and write each selected position through the PAGED page-table map
+// or the RAGGED offset (sglang PR #35175 page, "Implementation breakdown" and
+// "Key source snippets"; "#26788 [JIT Kernel] DeepSeek-V4 DSA indexer: faster
+// top-k + page-table transform (runtime k <= 2048)" page). The public C ABI is
+// declared in include/topk.h.
+//
+// Design (own design for sm_103a; the pages' CUDA/HIP kernels are prior art):
+//
+//  * Keys. A score's fp32 bits map to an order-preserving uint32 key. Every
+//    selection step works on keys, so no score is compared as a float.
+//  * Radix select on a 64-bit composite (key << 32 | ~position). Levels take
+//    12, 12 and 8 bits of the key from the top (a 4096-bin shared-memory
+//    histogram per level; the 12-bit first level is the one the PR #36684
+//    page, "Feature and motivation", describes), then, only when equal scores
+//    straddle the threshold and TOPK_DETERMINISTIC is set, 12/12/8 bits of
+//    ~position, so the lowest positions win. A level stops the descent as soon
+//    as its threshold bin holds exactly the count still needed.
+//  * Threshold bin search: every thread owns a run of bins, a warp-shuffle
+//    suffix scan plus one cross-warp pass finds the bin where the count from
+//    the top first reaches the target (cf. warp_inclusive_sum on the PR #36684
+//    page, "Key source snippets").
+//  * Compaction and slot allocation use ballot/popc with one shared-memory
+//    atomic per warp (cf. warp_sum_bool, same page).
+//  * Routes, chosen per row by length (the plan kernel orders rows longest
+//    first and hands long rows of small batches to the cluster path):
+//      trivial   L <= k: positions 0..L-1 then -1, scores never read;
+//      register  L <= 8192: the window lives in registers (16-byte loads),
+//                every level re-reads registers;
+//      streaming longer rows: one pass over HBM builds the level-1 histogram
+//                while collecting into shared memory every element whose top
+//                12 key bits clear a lower bound estimated from the first tile
+//                of the row; the later levels run on that candidate buffer. If
+//                the estimate was too high, or the buffer overflowed, the row
+//                is re-read from global memory (always exact, only slower);
+//      cluster   for few long rows: the same streaming pass split over a
+//                thread-block cluster of 8 CTAs, histograms merged through
+//                distributed shared memory (reduce-scatter + all-gather) and
+//                output slots allocated with atomics on the leader CTA's
+//                shared memory (cf. TopKCluster on the PR #36684 page).
+//  * Unaligned window heads: 16-byte loads start at the aligned address below
+//    the window and the up-to-3 leading / trailing lanes are excluded by
+//    position. Scores are never written (the pages' kernel masks them in place).
+//  * No wait here spins: all waits are __syncthreads or hardware cluster
+//    barriers.
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "topk.h"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kThreads = 512;                 // threads per CTA, all routes
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
+constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
+constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
+constexpr int kRegVecs = 4;                   // register route: 4 vectors per thread (L <= 8192)
+constexpr int kClusterSize = 8;               // CTAs per long row on the cluster path
+constexpr int kPlanThreads = 1024;
+constexpr int32_t kClusterFloor = 32768;      // rows longer than this may use the cluster path
+constexpr int32_t kClusterMaxBatch = 64;      // ... when the batch is at most this
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+constexpr int kBandTrivial = 32;              // plan bands: 0..31 by length, then these two
+constexpr int kBandCluster = 33;
+constexpr int kBands = 34;
+
+struct alignas(64) PlanHeader {
+    uint32_t magic;
+    int32_t batch;
+    int32_t k;
+    int32_t n_order;      // rows listed in order[] (all rows not on the cluster path)
+    int32_t n_cluster;    // rows listed in cluster_rows[]
+    uint32_t error_rows;  // device-side data errors
+    uint32_t flags;       // TOPK_DEVICE_FLAG_*
+    int32_t reserved[9];
+};
+static_assert(sizeof(PlanHeader) == 64, "header layout");
+constexpr uint32_t kPlanMagic = 0x6E616C50u;
+
+size_t workspace_bytes_for(int32_t batch) {
+    if (batch < 0) return 0;
+    size_t bytes = sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(batch);
+    return (bytes + 255) / 256 * 256;
+}
+
+// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each, the
+// candidate buffer is (key, position) pairs, then small scratch.
+struct Shared {
+    uint32_t* hist;      // local histogram
+    uint32_t* mhist;     // merged histogram (== hist on a single CTA)
+    uint32_t* cand_key;
+    int32_t* cand_pos;
+    uint32_t* red;       // kWarps words for scans
+    uint32_t* res;       // threshold search results
+    uint32_t* cnt;       // [0] candidates, [1] definite slots, [2] threshold-group slots
+};
+
+constexpr size_t kScratchWords = 64;
+constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kScratchWords) * 4;
+constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kScratchWords) * 4;
+
+__device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
+    Shared s;
+    uint32_t* w = reinterpret_cast<uint32_t*>(base);
+    s.hist = w;
+    w += kBins;
+    if (merged_separate) {
+        s.mhist = w;
+        w += kBins;
+    } else {
+        s.mhist = s.hist;
+    }
+    s.cand_key = w;
+    w += kCandCap;
+    s.cand_pos = reinterpret_cast<int32_t*>(w);
+    w += kCandCap;
+    s.red = w;
+    s.res = w + 32;
+    s.cnt = w + 48;
+    return s;
+}
+
+struct Params {
+    const float* scores;
+    int64_t score_stride;
+    const int32_t* row_starts;
+    const int32_t* seq_lens;
+    const int32_t* out_offsets;
+    const int32_t* page_table;
+    int64_t page_table_stride;
+    int32_t page_bits;
+    int32_t batch;
+    int32_t k;
+    uint32_t flags;
+    int32_t* out;
+    int32_t* out_raw;
+    PlanHeader* hdr;
+    const int32_t* order;
+    const int32_t* cluster_rows;
+};
+
+// ----------------------------------------------------------------------------
+// small device helpers
+// ----------------------------------------------------------------------------
+
+// Order-preserving fp32 -> uint32: flip all bits of negatives, set the sign bit
+// of non-negatives.
+__device__ __forceinline__ uint32_t score_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ float4 load_stream(const float4* p) {
+    float4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, v, off);
+        if (lane_id() >= static_cast<uint32_t>(off)) v += y;
+    }
+    return v;
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int32_t pos) {
+    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~pos);
+}
+
+// Radix levels over the 64-bit composite: 12/12/8 bits of the key, then
+// 12/12/8 bits of ~position (deterministic tie-break only).
+__device__ __forceinline__ int level_shift(int lvl) {
+    return lvl == 0 ? 52 : lvl == 1 ? 40 : lvl == 2 ? 32 : lvl == 3 ? 20 : lvl == 4 ? 8 : 0;
+}
+__device__ __forceinline__ int level_bins(int lvl) { return (lvl == 2 || lvl == 5) ? 256 : kBins; }
+
+// Finds the largest bin d of h[0..nb) with sum_{c >= d} h[c] >= target and
+// returns it with above = sum_{c > d} h[c] and count = h[d]. target must be
+// in [1, sum(h)]. All threads of the CTA call it; it synchronises twice.
+struct Threshold {
+    uint32_t bin, above, count;
+};
+
+__device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, const Shared& sh) {
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int bpt = (nb + kThreads - 1) / kThreads;
+    const int lo = tid * bpt;
+    uint32_t s = 0;
+    for (int i = 0; i < bpt; ++i) {
+        const int c = lo + i;
+        if (c < nb) s += h[c];
+    }
+    // suffix sum over lanes >= this lane
+    uint32_t x = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, x, off);
+        if (lane_id() + off < 32) x += y;
+    }
+    if (lane_id() == 0) sh.red[warp] = x;
+    __syncthreads();
+    uint32_t above_warps = 0;
+    for (int w = warp + 1; w < kWarps; ++w) above_warps += sh.red[w];
+    const uint32_t incl = x + above_warps;
+    const uint32_t excl = incl - s;
+    if (excl < target && incl >= target) {
+        uint32_t run = excl;
+        for (int i = bpt - 1; i >= 0; --i) {
+            const int c = lo + i;
+            if (c >= nb) continue;
+            const uint32_t hc = h[c];
+            if (run + hc >= target) {
+                sh.res[0] = static_cast<uint32_t>(c);
+                sh.res[1] = run;
+                sh.res[2] = hc;
+                break;
+            }
+            run += hc;
+        }
+    }
+    __syncthreads();
+    return Threshold{sh.res[0], sh.res[1], sh.res[2]};
+}
+
+__device__ __forceinline__ void clear_hist(uint32_t* h, int nb) {
+    for (int i = threadIdx.x; i < nb; i += kThreads) h[i] = 0u;
+}
+
+// Sum over the CTA of h[c] for c >= from (bins of the local histogram).
+__device__ uint32_t count_from(const uint32_t* h, int nb, uint32_t from, const Shared& sh) {
+    uint32_t s = 0;
+    for (int c = threadIdx.x; c < nb; c += kThreads)
+        if (static_cast<uint32_t>(c) >= from) s += h[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+    __syncthreads();
+    if (lane_id() == 0) sh.red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    uint32_t t = 0;
+    for (int w = 0; w < kWarps; ++w) t += sh.red[w];
+    __syncthreads();
+    return t;
+}
+
+// ----------------------------------------------------------------------------
+// merge policies: a single CTA, or a thread-block cluster over DSMEM
+// ----------------------------------------------------------------------------
+
+struct SoloMerge {
+    __device__ __forceinline__ const uint32_t* merge(const Shared& sh, int) const {
+        __syncthreads();
+        return sh.hist;
+    }
+    __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt[i]; }
+};
+
+struct ClusterMerge {
+    // hist (local) -> mhist (sum over the cluster), identical in every CTA.
+    __device__ const uint32_t* merge(const Shared& sh, int nb) const {
+        cg::cluster_group cluster = cg::this_cluster();
+        const unsigned rank = cluster.block_rank();
+        const int per = nb / kClusterSize;
+        cluster.sync();  // every local histogram is complete
+        for (int i = threadIdx.x; i < per; i += kThreads) {
+            const int bin = static_cast<int>(rank) * per + i;
+            uint32_t s = 0;
+#pragma unroll
+            for (int q = 0; q < kClusterSize; ++q) s += cluster.map_shared_rank(sh.hist, q)[bin];
+            sh.mhist[bin] = s;
+        }
+        cluster.sync();  // every slice of the sum is complete
+        for (int i = threadIdx.x; i < nb; i += kThreads) {
+            const int q = i / per;
+            if (q != static_cast<int>(rank)) sh.mhist[i] = cluster.map_shared_rank(sh.mhist, q)[i];
+        }
+        __syncthreads();
+        return sh.mhist;
+    }
+    __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const {
+        return cg::this_cluster().map_shared_rank(&sh.cnt[i], 0);
+    }
+};
+
+// ----------------------------------------------------------------------------
+// element sources: registers, the candidate buffer, global memory
+// ----------------------------------------------------------------------------
+
+// Register tile: v[u] holds vector j = u*kThreads + tid of the aligned window.
+template <int NV>
+struct RegSource {
+    const float4 (&v)[NV];
+    int rem, len;
+    template <class F>
+    __device__ __forceinline__ void visit(F&& f) const {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int j = u * kThreads + static_cast<int>(threadIdx.x);
+            const int p0 = 4 * j - rem;
+            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int p = p0 + c;
+                f(score_key(e[c]), p, static_cast<unsigned>(p) < static_cast<unsigned>(len));
+            }
+        }
+    }
+};
+
+struct CandSource {
+    const uint32_t* key;
+    const int32_t* pos;
+    uint32_t n;
+    template <class F>
+    __device__ __forceinline__ void visit(F&& f) const {
+        const uint32_t n_round = (n + kThreads - 1) / kThreads * kThreads;
+        for (uint32_t i = threadIdx.x; i < n_round; i += kThreads) {
+            const bool valid = i < n;
+            f(valid ? key[i] : 0u, valid ? pos[i] : 0, valid);
+        }
+    }
+};
+
+// Global memory: vectors [jb, je) of the aligned window, re-read.
+struct GlobalSource {
+    const float4* vbase;
+    int jb, je, rem, len;
+    template <class F>
+    __device__ __forceinline__ void visit(F&& f) const {
+        for (int j0 = jb; j0 < je; j0 += kTileVecs * kThreads) {
+            float4 v[kTileVecs];
+#pragma unroll
+            for (int u = 0; u < kTileVecs; ++u) {
+                const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+                v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kTileVecs; ++u) {
+                const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+                const int p0 = 4 * j - rem;
+                const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int p = p0 + c;
+                    f(score_key(e[c]), p, j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len));
+                }
+            }
+        }
+    }
+};
+
+// ----------------------------------------------------------------------------
+// selection state and the radix levels
+// ----------------------------------------------------------------------------
+
+// After the levels: an element whose composite, masked to the resolved high
+// bits, exceeds `prefix` is selected; one equal to `prefix` belongs to the
+// threshold group, of which `need` are selected (all of them when `exact`).
+struct SelState {
+    uint64_t prefix;
+    uint64_t mask;
+    uint32_t need;
+    bool exact;
+};
+
+__device__ __forceinline__ void apply_level(SelState& st, int lvl, const Threshold& t) {
+    const int shift = level_shift(lvl);
+    const uint64_t digit_mask = static_cast<uint64_t>(level_bins(lvl) - 1);
+    st.need -= t.above;
+    st.prefix |= static_cast<uint64_t>(t.bin) << shift;
+    st.mask |= digit_mask << shift;
+    st.exact = (t.count == st.need);
+}
+
+template <class Merge, class Src>
+__device__ void run_levels(SelState& st, int first, int last, const Src& src, const Shared& sh,
+                           const Merge& mg) {
+    for (int lvl = first; lvl <= last && !st.exact; ++lvl) {
+        const int nb = level_bins(lvl);
+        const int shift = level_shift(lvl);
+        clear_hist(sh.hist, nb);
+        __syncthreads();
+        const uint64_t prefix = st.prefix, mask = st.mask;
+        uint32_t* hist = sh.hist;
+        src.visit([&](uint32_t key, int32_t pos, bool valid) {
+            const uint64_t c = composite(key, pos);
+            if (valid && (c & mask) == prefix)
+                atomicAdd(&hist[static_cast<uint32_t>(c >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        });
+        const uint32_t* merged = mg.merge(sh, nb);
+        const Threshold t = find_threshold(merged, nb, st.need, sh);
+        apply_level(st, lvl, t);
+    }
+}
+
+// Output transform of one selected position.
+template <bool kPaged>
+struct Emitter {
+    int32_t* out;
+    int32_t* out_raw;
+    const int32_t* pt_row;
+    int32_t page_bits;
+    int32_t offset;
+    uint32_t k;
+    uint32_t* flags;  // device flags word of the workspace
+    __device__ __forceinline__ void write(uint32_t slot, int32_t pos) const {
+        if (slot >= k) {  // never taken when the selection is consistent
+            atomicOr(flags, TOPK_DEVICE_FLAG_INTERNAL);
+            return;
+        }
+        int32_t v;
+        if (kPaged) {
+            const int32_t page = __ldg(pt_row + (pos >> page_bits));
+            v = (page << page_bits) | (pos & ((1 << page_bits) - 1));
+        } else {
+            v = pos + offset;
+        }
+        out[slot] = v;
+        if (out_raw) out_raw[slot] = pos;
+    }
+};
+
+// Writes the k selected elements of `src` to their slots. Definite elements
+// take slots [0, k - need) from counter 1, the threshold group takes
+// [k - need, k) from counter 2 (the first `need` to arrive win, unless exact).
+template <bool kPaged, class Merge, class Src>
+__device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, const Shared& sh,
+                              const Merge& mg, const Emitter<kPaged>& em) {
+    uint32_t* ctr_def = mg.counter(sh, 1);
+    uint32_t* ctr_grp = mg.counter(sh, 2);
+    const uint64_t prefix = st.prefix, mask = st.mask;
+    const uint32_t need = st.need;
+    const bool exact = st.exact;
+    const uint32_t lt = lanemask_lt();
+    src.visit([&](uint32_t key, int32_t pos, bool valid) {
+        const uint64_t hi = composite(key, pos) & mask;
+        const bool def = valid && (hi > prefix || (exact && hi == prefix));
+        const bool grp = valid && !exact && hi == prefix;
+        const uint32_t md = __ballot_sync(kFull, def);
+        if (md) {
+            const int leader = __ffs(md) - 1;
+            uint32_t base = 0;
+            if (lane_id() == static_cast<uint32_t>(leader)) base = atomicAdd(ctr_def, __popc(md));
+            base = __shfl_sync(kFull, base, leader);
+            if (def) em.write(base + __popc(md & lt), pos);
+        }
+        const uint32_t mgp = __ballot_sync(kFull, grp);
+        if (mgp) {
+            const int leader = __ffs(mgp) - 1;
+            uint32_t base = 0;
+            if (lane_id() == static_cast<uint32_t>(leader)) base = atomicAdd(ctr_grp, __popc(mgp));
+            base = __shfl_sync(kFull, base, leader);
+            const uint32_t t = base + __popc(mgp & lt);
+            if (grp && t < need) em.write(k - need + t, pos);
+        }
+    });
+}
+
+// ----------------------------------------------------------------------------
+// routes
+// ----------------------------------------------------------------------------
+
+template <bool kPaged>
+__device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em) {
+    for (uint32_t t = threadIdx.x; t < k; t += kThreads) {
+        if (static_cast<int32_t>(t) < len) {
+            em.write(t, static_cast<int32_t>(t));
+        } else {
+            em.out[t] = -1;
+            if (em.out_raw) em.out_raw[t] = -1;
+        }
+    }
+}
+
+// Register route: the whole aligned window (nv vectors) fits NV vectors per thread.
+template <bool kPaged, int NV>
+__device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
+                             const Shared& sh, const Emitter<kPaged>& em) {
+    float4 v[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int j = u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < nv ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const RegSource<NV> src{v, rem, len};
+    SoloMerge mg;
+    SelState st{0ull, 0ull, k, false};
+    run_levels(st, 0, det ? 5 : 2, src, sh, mg);
+    emit_selected<kPaged>(st, k, src, sh, mg, em);
+}
+
+// Appends, warp-aggregated, the elements flagged in `pass` (bit e = element e
+// of this thread's tile) to the candidate buffer.
+__device__ __forceinline__ void collect_tile(const uint32_t (&key)[4 * kTileVecs], uint32_t pass,
+                                             int j0, int rem, const Shared& sh) {
+    const uint32_t c = __popc(pass);
+    const uint32_t incl = warp_inclusive_scan(c);
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    if (total == 0) return;
+    uint32_t base = 0;
+    if (lane_id() == 31) base = atomicAdd(&sh.cnt[0], total);
+    base = __shfl_sync(kFull, base, 31);
+    uint32_t idx = base + incl - c;
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e) {
+        if ((pass >> e) & 1u) {
+            if (idx < static_cast<uint32_t>(kCandCap)) {
+                const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
+                sh.cand_key[idx] = key[e];
+                sh.cand_pos[idx] = 4 * j - rem + (e % 4);
+            }
+            ++idx;
+        }
+    }
+}
+
+// Loads one tile (kTileVecs vectors per thread starting at vector j0), adds
+// every in-window element to the level-1 histogram and returns the keys.
+__device__ __forceinline__ void load_tile(const float4* vbase, int j0, int je, int rem, int len,
+                                          uint32_t (&key)[4 * kTileVecs], uint32_t& valid_bits,
+                                          const Shared& sh) {
+    float4 v[kTileVecs];
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    valid_bits = 0;
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        const int p0 = 4 * j - rem;
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int p = p0 + c;
+            const uint32_t kk = score_key(e[c]);
+            key[4 * u + c] = kk;
+            if (j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len)) {
+                valid_bits |= 1u << (4 * u + c);
+                atomicAdd(&sh.hist[kk >> 20], 1u);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pass_bits(const uint32_t (&key)[4 * kTileVecs], uint32_t valid_bits,
+                                              uint32_t bound_bin) {
+    uint32_t pass = 0;
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e)
+        if (((valid_bits >> e) & 1u) && (key[e] >> 20) >= bound_bin) pass |= 1u << e;
+    return pass;
+}
+
+// Streaming route over vectors [jb, je) of the aligned window (the whole row
+// on one CTA, or this CTA's slice of a cluster row).
+template <bool kPaged, class Merge>
+__device__ void streaming_row(const float4* vbase, int jb, int je, int rem, int len, uint32_t k,
+                              bool det, const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
+    // --- head tile: histogram only, then a lower bound for collection
+    uint32_t key[4 * kTileVecs];
+    uint32_t valid_bits;
+    load_tile(vbase, jb, je, rem, len, key, valid_bits, sh);
+    // elements of the head tile in the window
+    const int head_first = 4 * jb - rem, head_end = 4 * min(je, jb + kTileVecs * kThreads) - rem;
+    const int n_head = max(0, min(head_end, len) - max(head_first, 0));
+    __syncthreads();
+    uint32_t bound_bin = 0;
+    if (n_head > 0) {
+        // expected share of the row's top-k in the head tile, plus ~4 sigma
+        const float expect = static_cast<float>(k) * static_cast<float>(n_head) / static_cast<float>(len);
+        float tgt = expect + 4.0f * sqrtf(expect) + 16.0f;
+        uint32_t target = static_cast<uint32_t>(fminf(tgt, static_cast<float>(n_head)));
+        target = max(target, 1u);
+        bound_bin = find_threshold(sh.hist, kBins, target, sh).bin;
+    }
+    collect_tile(key, pass_bits(key, valid_bits, bound_bin), jb, rem, sh);
+
+    // --- main pass
+    for (int j0 = jb + kTileVecs * kThreads; j0 < je; j0 += kTileVecs * kThreads) {
+        load_tile(vbase, j0, je, rem, len, key, valid_bits, sh);
+        collect_tile(key, pass_bits(key, valid_bits, bound_bin), j0, rem, sh);
+    }
+
+    // --- level 1 over the merged histogram
+    const uint32_t* merged = mg.merge(sh, kBins);
+    SelState st{0ull, 0ull, k, false};
+    const Threshold t1 = find_threshold(merged, kBins, k, sh);
+    apply_level(st, 0, t1);
+
+    bool cands_ok = sh.cnt[0] <= static_cast<uint32_t>(kCandCap) && t1.bin >= bound_bin;
+    if (!cands_ok) {
+        // re-collect from global memory if this CTA's elements at or above the
+        // threshold bin fit the buffer
+        const uint32_t local = count_from(sh.hist, kBins, t1.bin, sh);
+        if (local <= static_cast<uint32_t>(kCandCap)) {
+            if (threadIdx.x == 0) sh.cnt[0] = 0;
+            __syncthreads();
+            for (int j0 = jb; j0 < je; j0 += kTileVecs * kThreads) {
+                float4 v[kTileVecs];
+#pragma unroll
+                for (int u = 0; u < kTileVecs; ++u) {
+                    const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+                    v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                uint32_t pass = 0;
+#pragma unroll
+                for (int u = 0; u < kTileVecs; ++u) {
+                    const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+                    const int p0 = 4 * j - rem;
+                    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t kk = score_key(e[c]);
+                        key[4 * u + c] = kk;
+                        const int p = p0 + c;
+                        if (j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len) &&
+                            (kk >> 20) >= t1.bin)
+                            pass |= 1u << (4 * u + c);
+                    }
+                }
+                collect_tile(key, pass, j0, rem, sh);
+            }
+            __syncthreads();
+            cands_ok = true;
+        }
+    }
+    const int last = det ? 5 : 2;
+    if (cands_ok) {
+        const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
+        run_levels(st, 1, last, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    } else {
+        const GlobalSource src{vbase, jb, je, rem, len};
+        run_levels(st, 1, last, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// kernels
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ bool plan_matches(const Params& p) {
+    const PlanHeader* h = p.hdr;
+    return h->magic == kPlanMagic && h->batch == p.batch && h->k == p.k;
+}
+
+template <bool kPaged>
+__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b) {
+    Emitter<kPaged> em;
+    em.out = p.out + static_cast<int64_t>(b) * p.k;
+    em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
+    em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(b) * p.page_table_stride : nullptr;
+    em.page_bits = p.page_bits;
+    em.offset = kPaged ? 0 : p.out_offsets[b];
+    em.k = static_cast<uint32_t>(p.k);
+    em.flags = &p.hdr->flags;
+    return em;
+}
+
+// One CTA per row; rows come from the plan's order (longest first), rows the
+// plan gave to the cluster path are skipped (their CTAs exit at once).
+template <bool kPaged>
+__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Shared sh = carve(smem, false);
+    if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
+    const bool planned = plan_matches(p);
+    int b = static_cast<int>(blockIdx.x);
+    if (planned) {
+        if (b >= p.hdr->n_order) return;
+        b = p.order[b];
+    } else if (blockIdx.x == 0 && threadIdx.x == 0) {
+        atomicOr(&p.hdr->flags, TOPK_DEVICE_FLAG_PLAN_MISMATCH);
+    }
+    int32_t len = p.seq_lens[b];
+    const int32_t start = p.row_starts ? p.row_starts[b] : 0;
+    if (len < 0 || start < 0) {
+        // seq_len < 0 was counted by the plan; count the rest here
+        if (threadIdx.x == 0 && (!planned || len >= 0)) atomicAdd(&p.hdr->error_rows, 1u);
+        len = 0;
+    }
+    const uint32_t k = static_cast<uint32_t>(p.k);
+    const Emitter<kPaged> em = make_emitter<kPaged>(p, b);
+    if (len <= p.k) {
+        trivial_row<kPaged>(len, k, em);
+        return;
+    }
+    if (threadIdx.x < 4) sh.cnt[threadIdx.x] = 0;
+    const int rem = start & 3;
+    const float4* vbase = reinterpret_cast<const float4*>(
+        p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
+    const int nv = (len + rem + 3) >> 2;
+    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
+    if (nv <= kRegVecs * kThreads) {
+        register_row<kPaged, kRegVecs>(vbase, nv, rem, len, k, det, sh, em);
+    } else {
+        clear_hist(sh.hist, kBins);
+        __syncthreads();
+        streaming_row<kPaged>(vbase, 0, nv, rem, len, k, det, sh, SoloMerge{}, em);
+    }
+}
+
+// One thread-block cluster per long row (looping over the plan's cluster list).
+template <bool kPaged>
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads, 2)
+    topk_cluster_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const Shared sh = carve(smem, true);
+    if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
+    if (!plan_matches(p)) return;  // uniform over the cluster: no barrier is skipped
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int n_slots = static_cast<int>(gridDim.x) / kClusterSize;
+    const int slot = static_cast<int>(blockIdx.x) / kClusterSize;
+    const int n_rows = p.hdr->n_cluster;
+    const ClusterMerge mg;
+    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
+    const uint32_t k = static_cast<uint32_t>(p.k);
+    for (int i = slot; i < n_rows; i += n_slots) {
+        const int b = p.cluster_rows[i];
+        int32_t len = p.seq_lens[b];
+        const int32_t start = p.row_starts ? p.row_starts[b] : 0;
+        if (len < 0 || start < 0) {
+            if (rank == 0 && threadIdx.x == 0 && start < 0) atomicAdd(&p.hdr->error_rows, 1u);
+            len = 0;
+        }
+        const Emitter<kPaged> em = make_emitter<kPaged>(p, b);
+        if (len <= p.k) {
+            if (rank == 0) trivial_row<kPaged>(len, k, em);
+            cluster.sync();
+            continue;
+        }
+        if (threadIdx.x < 4) sh.cnt[threadIdx.x] = 0;
+        clear_hist(sh.hist, kBins);
+        const int rem = start & 3;
+        const float4* vbase = reinterpret_cast<const float4*>(
+            p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
+        const int nv = (len + rem + 3) >> 2;
+        const int per = (nv + kClusterSize - 1) / kClusterSize;
+        const int jb = min(nv, rank * per);
+        const int je = min(nv, jb + per);
+        // counters of the leader CTA must be zero before any CTA emits: the
+        // merges below pass several cluster barriers first
+        __syncthreads();
+        streaming_row<kPaged>(vbase, jb, je, rem, len, k, det, sh, mg, em);
+        cluster.sync();  // all emits done before the leader's counters are reset
+    }
+}
+
+// Plan: bands rows by length (longest first), lists rows for the cluster path,
+// counts seq_len < 0.
+__device__ __forceinline__ int band_of(int32_t len, int32_t k, bool allow_cluster) {
+    if (len <= k) return kBandTrivial;
+    if (allow_cluster && len > kClusterFloor) return kBandCluster;
+    return __clz(len);  // 31 - floor(log2 len): longer rows get lower bands, go first
+}
+
+__global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* seq_lens, int32_t batch,
+                                                                 int32_t k, PlanHeader* hdr,
+                                                                 int32_t* order, int32_t* cluster_rows) {
+    __shared__ uint32_t count[kBands];
+    __shared__ uint32_t offset[kBands];
+    __shared__ uint32_t n_err;
+    const int tid = static_cast<int>(threadIdx.x);
+    if (tid < kBands) count[tid] = 0;
+    if (tid == 0) n_err = 0;
+    __syncthreads();
+    const bool allow_cluster = batch <= kClusterMaxBatch;
+    const int n_iter = (batch + kPlanThreads - 1) / kPlanThreads;
+    const uint32_t lt = lanemask_lt();
+    for (int it = 0; it < n_iter; ++it) {
+        const int i = it * kPlanThreads + tid;
+        const bool valid = i < batch;
+        const int32_t len = valid ? seq_lens[i] : 0;
+        const uint32_t merr = __ballot_sync(kFull, valid && len < 0);
+        if (lane_id() == 0 && merr) atomicAdd(&n_err, __popc(merr));
+        const int band = valid ? band_of(max(len, 0), k, allow_cluster) : kBands;
+        const uint32_t peers = __match_any_sync(kFull, band);
+        if (valid && (peers & lt) == 0) atomicAdd(&count[band], __popc(peers));
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t run = 0;
+        for (int bnd = 0; bnd <= kBandTrivial; ++bnd) {
+            offset[bnd] = run;
+            run += count[bnd];
+        }
+        offset[kBandCluster] = 0;
+        hdr->n_order = static_cast<int32_t>(run);
+        hdr->n_cluster = static_cast<int32_t>(count[kBandCluster]);
+        hdr->error_rows = n_err;
+        hdr->flags = 0;
+        hdr->batch = batch;
+        hdr->k = k;
+        hdr->magic = kPlanMagic;
+    }
+    __syncthreads();
+    for (int it = 0; it < n_iter; ++it) {
+        const int i = it * kPlanThreads + tid;
+        const bool valid = i < batch;
+        const int32_t len = valid ? seq_lens[i] : 0;
+        const int band = valid ? band_of(max(len, 0), k, allow_cluster) : kBands;
+        const uint32_t peers = __match_any_sync(kFull, band);
+        const int leader = __ffs(peers) - 1;
+        uint32_t base = 0;
+        if (valid && static_cast<int>(lane_id()) == leader) base = atomicAdd(&offset[band], __popc(peers));
+        base = __shfl_sync(kFull, base, leader);
+        if (valid) {
+            const uint32_t slot = base + __popc(peers & lt);
+            if (band == kBandCluster) cluster_rows[slot] = i;
+            else order[slot] = i;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+
+struct DeviceState {
+    bool ready = false;
+    cudaError_t err = cudaSuccess;
+    int max_clusters = 0;  // co-resident clusters of the cluster kernel
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+template <bool kPaged>
+cudaError_t prepare_kernels(int& max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemRows));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemCluster));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterSize, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemCluster;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterSize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kPaged>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();  // the query is advisory: fall back to one cluster per 8 SMs
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        n = sms > kClusterSize ? sms / kClusterSize : 1;
+    }
+    max_clusters = max_clusters == 0 ? n : min(max_clusters, n);
+    return cudaSuccess;
+}
+
+cudaError_t device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        int mc = 0;
+        e = prepare_kernels<true>(mc);
+        if (e == cudaSuccess) e = prepare_kernels<false>(mc);
+        if (e != cudaSuccess) return e;
+        st.max_clusters = mc > 0 ? mc : 1;
+        st.ready = true;
+    }
+    *out = &st;
+    return cudaSuccess;
+}
+
+bool valid_k(int32_t k) { return k >= 1 && k <= TOPK_MAX_K; }
+
+template <bool kPaged>
+int launch_transform(const Params& prm, cudaStream_t stream) {
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != cudaSuccess) return TOPK_ERR_CUDA;
+    topk_rows_kernel<kPaged><<<prm.batch, kThreads, kSmemRows, stream>>>(prm);
+    if (cudaPeekAtLastError() != cudaSuccess) return TOPK_ERR_CUDA;
+    if (prm.batch <= kClusterMaxBatch) {
+        const int slots = min(prm.batch, ds->max_clusters);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kClusterSize * slots, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemCluster;
+        cfg.stream = stream;
+        // the compile-time __cluster_dims__ fixes the cluster shape
+        if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kPaged>, prm) != cudaSuccess) return TOPK_ERR_CUDA;
+    }
+    return TOPK_OK;
+}
+
+int common_checks(const float* scores, int64_t score_stride, const int32_t* seq_lens, int32_t batch,
+                  int32_t k, void* workspace, size_t workspace_bytes, int32_t* out) {
+    if (!valid_k(k)) return TOPK_ERR_K;
+    if (batch < 0 || score_stride < 0 || (score_stride & 3) != 0) return TOPK_ERR_ARG;
+    if (batch > 0 && (scores == nullptr || seq_lens == nullptr || out == nullptr)) return TOPK_ERR_ARG;
+    if (batch > 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) != 0) return TOPK_ERR_ALIGN;
+    if (workspace == nullptr || workspace_bytes < workspace_bytes_for(batch)) return TOPK_ERR_WORKSPACE;
+    return TOPK_OK;
+}
+
+Params make_params(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                   const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace, int32_t* out,
+                   int32_t* out_raw, uint32_t flags) {
+    Params p = {};
+    p.scores = scores;
+    p.score_stride = score_stride;
+    p.row_starts = row_starts;
+    p.seq_lens = seq_lens;
+    p.batch = batch;
+    p.k = k;
+    p.flags = flags;
+    p.out = out;
+    p.out_raw = out_raw;
+    p.hdr = static_cast<PlanHeader*>(workspace);
+    p.order = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + sizeof(PlanHeader));
+    p.cluster_rows = p.order + batch;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t topk_workspace_bytes(int32_t batch) { return workspace_bytes_for(batch); }
+
+int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace, size_t workspace_bytes,
+              topk_stream_t stream) {
+    if (!valid_k(k)) return TOPK_ERR_K;
+    if (batch < 0 || (batch > 0 && seq_lens == nullptr)) return TOPK_ERR_ARG;
+    if (workspace == nullptr || workspace_bytes < workspace_bytes_for(batch)) return TOPK_ERR_WORKSPACE;
+    PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + sizeof(PlanHeader));
+    topk_plan_kernel<<<1, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        seq_lens, batch, k, hdr, order, order + batch);
+    return cudaPeekAtLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+int topk_transform_paged(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                         const int32_t* seq_lens, const int32_t* page_table, int64_t page_table_stride,
+                         int32_t page_size, int32_t batch, int32_t k, void* workspace,
+                         size_t workspace_bytes, int32_t* out, int32_t* out_raw, uint32_t flags,
+                         topk_stream_t stream) {
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out);
+    if (st != TOPK_OK) return st;
+    if (page_size < 1 || page_size > TOPK_MAX_PAGE_SIZE || (page_size & (page_size - 1)) != 0)
+        return TOPK_ERR_PAGE_SIZE;
+    if (page_table_stride < 0 || (batch > 0 && page_table == nullptr)) return TOPK_ERR_ARG;
+    if (batch == 0) return TOPK_OK;
+    Params p = make_params(scores, score_stride, row_starts, seq_lens, batch, k, workspace, out, out_raw, flags);
+    p.page_table = page_table;
+    p.page_table_stride = page_table_stride;
+    int bits = 0;
+    while ((1 << bits) < page_size) ++bits;
+    p.page_bits = bits;
+    return launch_transform<true>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topk_transform_ragged(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                          const int32_t* seq_lens, const int32_t* out_offsets, int32_t batch, int32_t k,
+                          void* workspace, size_t workspace_bytes, int32_t* out, int32_t* out_raw,
+                          uint32_t flags, topk_stream_t stream) {
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out);
+    if (st != TOPK_OK) return st;
+    if (batch > 0 && out_offsets == nullptr) return TOPK_ERR_ARG;
+    if (batch == 0) return TOPK_OK;
+    Params p = make_params(scores, score_stride, row_starts, seq_lens, batch, k, workspace, out, out_raw, flags);
+    p.out_offsets = out_offsets;
+    return launch_transform<false>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topk_read_device_errors(const void* workspace, int32_t* host_error_rows, uint32_t* host_flags,
+                            topk_stream_t stream) {
+    if (workspace == nullptr || host_error_rows == nullptr) return TOPK_ERR_ARG;
+    PlanHeader h;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TOPK_ERR_CUDA;
+    *host_error_rows = static_cast<int32_t>(h.error_rows);
+    if (host_flags) *host_flags = h.flags;
+    return TOPK_OK;
+}
+
+const char* topk_status_string(int status) {
+    switch (status) {
+        case TOPK_OK: return "ok";
+        case TOPK_ERR_ARG: return "invalid argument";
+        case TOPK_ERR_ALIGN: return "scores not 16-byte aligned";
+        case TOPK_ERR_K: return "k outside [1, 2048]";
+        case TOPK_ERR_PAGE_SIZE: return "page_size not a power of two in [1, 2^19]";
+        case TOPK_ERR_WORKSPACE: return "workspace missing or too small";
+        case TOPK_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

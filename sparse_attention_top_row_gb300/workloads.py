@@ -80,7 +80,7 @@ def paged_decode(device="cpu", sub_id=0, batch=128, seq_len=8192, k=2048, page_s
     physical pages."""
     g = _gen(device, seed_for(2, sub_id))
     scores = torch.randn(batch, seq_len, generator=g, device=device)
-    pages = seq_len // page_size
+    pages = (seq_len + page_size - 1) // page_size
     table = torch.randperm(batch * pages, generator=g, device=device).view(batch, pages)
     seq_lens = torch.full((batch,), seq_len, dtype=torch.int32, device=device)
     return dict(name=f"paged decode B={batch} L={seq_len} k={k} ps={page_size}", mode="paged",
@@ -129,7 +129,7 @@ def paged_long(device="cpu", sub_id=0, batch=1, seq_len=131072, k=2048, page_siz
     g = _gen(device, seed_for(4, sub_id))
     scores = (scale * torch.randn(batch, seq_len, generator=g, device=device))
     scores = scores.to(torch.bfloat16).to(torch.float32)
-    pages = seq_len // page_size
+    pages = (seq_len + page_size - 1) // page_size
     table = torch.randperm(batch * pages, generator=g, device=device).view(batch, pages)
     seq_lens = torch.full((batch,), seq_len, dtype=torch.int32, device=device)
     return dict(name=f"paged long B={batch} L={seq_len} k={k} bf16 ties", mode="paged", k=k,

@@ -1,0 +1,328 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Small cases are compared element by element on every row; the full-size
+workloads, in the launch configuration the benchmark times, are compared on
+sampled rows. Deterministic mode must match the oracle bit-exactly (rows
+sorted); default mode must select the bit-identical score multiset and pass
+every invariant. No floating-point tolerance applies: selection does no
+arithmetic on scores.
+"""
+
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_attention_top_row_gb300 import workloads as wl
+from topk_checks import HostWorkload, check_row_invariants, compare_with_oracle
+
+pytestmark = pytest.mark.gpu
+
+DET = 1
+CANARY = 0x7EADBEEF
+
+
+def assert_windows_in_bounds(w):
+    """The library's contract: every row's 16-byte-aligned window span lies
+    inside the score buffer (checked here so no test input reads past it)."""
+    hw = HostWorkload(w)
+    n = hw.scores.size
+    for b in range(hw.batch):
+        L = int(hw.seq_lens[b])
+        s = hw.start(b)
+        if L <= 0 or s < 0:
+            continue
+        rem = s % 4
+        lo = b * hw.stride + s - rem
+        hi = lo + 4 * ((L + rem + 3) // 4)
+        assert 0 <= lo and hi <= n, f"row {b}: window [{lo}, {hi}) outside the {n}-element buffer"
+        if hw.mode == "paged":
+            need = (L + hw.page_size - 1) // hw.page_size
+            assert b * hw.pt_stride + need <= hw.page_table.size, f"row {b}: page table too short"
+
+
+def run_gpu(topk, w, flags, raw=True):
+    assert_windows_in_bounds(w)
+    w = wl.to_device(w, "cuda")
+    B, k = int(w["batch"]), int(w["k"])
+    out = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+    out_raw = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda") if raw else None
+    before = w["scores"].clone()
+    _, _, ws = topk.run_workload(w, out=out, out_raw=out_raw, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int32), w["scores"].view(torch.int32)), "scores were written"
+    o = out.cpu().numpy()
+    r = out_raw.cpu().numpy() if raw else None
+    assert not np.any(o == CANARY), "an output slot was not written"
+    if raw:
+        assert not np.any(r == CANARY), "an out_raw slot was not written"
+    return o, r, ws
+
+
+def check_full(topk, w, flags_list=(DET, 0)):
+    hw = HostWorkload(w)
+    ref_out, ref_raw, ref_err = oracle.run_workload(w)
+    for flags in flags_list:
+        o, r, ws = run_gpu(topk, w, flags)
+        compare_with_oracle(hw, o, r, ref_out, ref_raw, deterministic=bool(flags & DET))
+        errs, dflags = topk.topk_read_device_errors(ws)
+        assert errs == ref_err
+        assert dflags == 0
+
+
+# ---------------------------------------------------------------- golden examples
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
+
+
+def test_golden_examples(cuda_lib):
+    from test_oracle_pins import _golden_workload
+    for case in json.load(open(GOLDEN))["cases"]:
+        w = _golden_workload(case)
+        for flags in (DET, 0):
+            o, r, _ = run_gpu(cuda_lib, w, flags)
+            got = np.sort(o, axis=1).tolist()
+            if flags & DET:
+                assert got == case["det"], case["name"]
+                assert np.sort(r, axis=1).tolist() == case["det_raw"], case["name"]
+            else:
+                assert got == case["det"] or got in case["also_valid"], case["name"]
+
+
+# ---------------------------------------------------------------- small workloads, every row
+
+SMALL = {
+    "ragged_tiny": lambda: wl.ragged_tiny("cpu", sub_id=0),
+    "ragged_tiny_s1": lambda: wl.ragged_tiny("cpu", sub_id=1),
+    "paged_decode_small": lambda: wl.paged_decode("cpu", batch=16, seq_len=8192, k=2048),
+    "paged_decode_k512": lambda: wl.paged_decode("cpu", batch=24, seq_len=4096, k=512, page_size=16),
+    "ragged_extend_small": lambda: wl.ragged_extend("cpu", chunk=1, rows_per_chunk=40, n_req=2,
+                                                    prefix=20000, new=40, k=2048),
+    "paged_long_small": lambda: wl.paged_long("cpu", batch=2, seq_len=40000, k=2048),
+    "paged_long_rows70": lambda: wl.paged_long("cpu", sub_id=3, batch=70, seq_len=20000, k=1024),
+    "mixed_paged": lambda: wl.mixed("cpu", mode="paged", k=1024, batch=31, max_len=70000),
+    "mixed_ragged": lambda: wl.mixed("cpu", mode="ragged", k=512, batch=31, max_len=70000),
+    "mixed_ragged_b129": lambda: wl.mixed("cpu", mode="ragged", k=2048, batch=129, max_len=20000,
+                                          sub_id=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workload_every_row(cuda_lib, name):
+    check_full(cuda_lib, SMALL[name]())
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _rows(rng, lens, kind="normal"):
+    rows = []
+    for L in lens:
+        if kind == "normal":
+            rows.append(rng.standard_normal(L).astype(np.float32).tolist())
+        elif kind == "ties":
+            rows.append(rng.choice([-1.0, 0.0, 0.5, 1.0], size=L).astype(np.float32).tolist())
+        elif kind == "equal":
+            rows.append([0.25] * L)
+        elif kind == "ascending":
+            rows.append(np.linspace(-3, 3, L, dtype=np.float32).tolist())
+        elif kind == "descending":
+            rows.append(np.linspace(3, -3, L, dtype=np.float32).tolist())
+        elif kind == "special":
+            v = rng.standard_normal(L).astype(np.float32)
+            idx = rng.integers(0, L, size=max(1, L // 50))
+            v[idx] = rng.choice(np.array([np.inf, -np.inf, -0.0, 0.0, np.finfo(np.float32).max,
+                                          -np.finfo(np.float32).max], dtype=np.float32), size=idx.size)
+            rows.append(v.tolist())
+    return rows
+
+
+@pytest.mark.parametrize("k", [1, 7, 512, 1000, 2048])
+@pytest.mark.parametrize("mode", ["ragged", "paged"])
+def test_boundary_lengths(cuda_lib, k, mode):
+    rng = np.random.default_rng(k)
+    lens = [0, 1, k - 1, k, k + 1, 8189, 8192, 8193, 16384, 16385, 40000]
+    lens = [L for L in lens if L >= 0]
+    starts = [int(x) for x in rng.integers(0, 4, size=len(lens))]
+    w = wl.custom(mode, k, _rows(rng, lens), row_starts=starts,
+                  out_offsets=[int(x) for x in rng.integers(0, 1 << 20, size=len(lens))],
+                  page_size=64, seed=k)
+    check_full(cuda_lib, w)
+
+
+@pytest.mark.parametrize("kind", ["ties", "equal", "ascending", "descending", "special"])
+@pytest.mark.parametrize("L", [3000, 12000, 50000])
+def test_adversarial_values(cuda_lib, kind, L):
+    """Heavy ties, one value everywhere, sorted rows (the first-tile estimate is
+    then wrong or the candidate buffer overflows: the exact fallbacks run),
+    infinities, signed zeros and the largest finite values."""
+    rng = np.random.default_rng(L)
+    w = wl.custom("ragged", 2048, _rows(rng, [L, L // 2 + 1], kind), row_starts=[1, 2],
+                  out_offsets=[0, 5])
+    check_full(cuda_lib, w)
+
+
+def test_cluster_path_with_adversarial_rows(cuda_lib):
+    """Few long rows (cluster path): sorted, equal and tied values."""
+    rng = np.random.default_rng(7)
+    rows = _rows(rng, [70000], "ascending") + _rows(rng, [70001], "descending") + \
+        _rows(rng, [65537], "equal") + _rows(rng, [100000], "ties")
+    w = wl.custom("paged", 2048, rows, page_size=64, seed=7)
+    check_full(cuda_lib, w)
+
+
+def test_nan_scores_order_deterministically(cuda_lib):
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal(20000).astype(np.float32)
+    v[rng.integers(0, 20000, 30)] = np.nan
+    v[rng.integers(0, 20000, 30)] = -np.nan
+    w = wl.custom("ragged", 100, [v.tolist()], out_offsets=[0])
+    hw = HostWorkload(w)
+    ref_out, ref_raw, _ = oracle.run_workload(w)
+    o, r, _ = run_gpu(cuda_lib, w, DET)
+    np.testing.assert_array_equal(np.sort(r), np.sort(ref_raw))
+
+
+def test_no_row_starts_and_no_out_raw(cuda_lib):
+    w = wl.paged_decode("cpu", batch=4, seq_len=10000, k=300, page_size=8)
+    hw = HostWorkload(w)
+    ref_out, _, _ = oracle.run_workload(w)
+    o, r, _ = run_gpu(cuda_lib, w, DET, raw=False)
+    np.testing.assert_array_equal(np.sort(o, axis=1), np.sort(ref_out, axis=1))
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 4096, 1 << 19])
+def test_page_sizes(cuda_lib, page_size):
+    rng = np.random.default_rng(page_size)
+    L = 9000
+    pages = (L + page_size - 1) // page_size
+    table = rng.permutation(3 * pages).reshape(3, pages) if page_size < 4096 else \
+        rng.integers(0, 1 << 31 >> 19, size=(3, pages))
+    w = wl.custom("paged", 777, _rows(rng, [L, L, 5000]), page_size=page_size,
+                  page_table=table.astype(np.int32))
+    check_full(cuda_lib, w)
+
+
+def test_shared_buffer_stride_zero(cuda_lib):
+    w = wl.ragged_tiny("cpu", sub_id=5, batch=40, k=100, max_len=20000)
+    check_full(cuda_lib, w)
+
+
+def test_data_errors_are_counted(cuda_lib):
+    rng = np.random.default_rng(3)
+    w = wl.custom("ragged", 16, _rows(rng, [100, 100, 100, 100]), out_offsets=[0, 0, 0, 0])
+    w["seq_lens"] = torch.tensor([100, -5, 100, 100], dtype=torch.int32)
+    w["row_starts"] = torch.tensor([0, 0, -8, 0], dtype=torch.int32)
+    ref_out, ref_raw, ref_err = oracle.run_workload(w)
+    assert ref_err == 2
+    o, r, ws = run_gpu(cuda_lib, w, DET)
+    np.testing.assert_array_equal(np.sort(o, axis=1), np.sort(ref_out, axis=1))
+    errs, flags = cuda_lib.topk_read_device_errors(ws)
+    assert errs == 2 and flags == 0
+
+
+def test_plan_mismatch_still_exact(cuda_lib):
+    """A transform whose (batch, k) differs from the plan's flags it and still
+    computes every row exactly (without the cluster path)."""
+    w = wl.to_device(wl.paged_long("cpu", batch=3, seq_len=70000, k=512), "cuda")
+    ref_out, ref_raw, _ = oracle.run_workload(w)
+    ws = cuda_lib.new_workspace(3)
+    cuda_lib.topk_plan(w["seq_lens"], 256, ws)  # planned for another k
+    out = torch.full((3, 512), CANARY, dtype=torch.int32, device="cuda")
+    raw = torch.full((3, 512), CANARY, dtype=torch.int32, device="cuda")
+    cuda_lib.topk_transform_paged(w["scores"], w["score_stride"], None, w["seq_lens"], w["page_table"],
+                                  w["page_table_stride"], 64, 512, ws, out, raw, DET)
+    np.testing.assert_array_equal(np.sort(raw.cpu().numpy(), 1), np.sort(ref_raw, 1))
+    errs, flags = cuda_lib.topk_read_device_errors(ws)
+    assert flags & cuda_lib.TOPK_DEVICE_FLAG_PLAN_MISMATCH
+
+
+def test_one_plan_serves_many_transforms(cuda_lib):
+    w = wl.to_device(wl.mixed("cpu", mode="ragged", k=512, batch=20, max_len=50000, sub_id=9), "cuda")
+    ref_out, ref_raw, _ = oracle.run_workload(w)
+    ws = cuda_lib.new_workspace(20)
+    cuda_lib.topk_plan(w["seq_lens"], 512, ws)
+    for _ in range(3):
+        out, _, _ = cuda_lib.run_workload(w, workspace=ws, flags=DET, plan=False)
+        np.testing.assert_array_equal(np.sort(out.cpu().numpy(), 1), np.sort(ref_out, 1))
+
+
+def test_deterministic_mode_is_repeatable(cuda_lib):
+    w = wl.to_device(wl.paged_long("cpu", batch=31, seq_len=50000, k=2048, sub_id=1), "cuda")
+    outs = [np.sort(cuda_lib.run_workload(w, flags=DET)[0].cpu().numpy(), 1) for _ in range(3)]
+    assert all(np.array_equal(outs[0], x) for x in outs[1:])
+
+
+def test_non_default_stream(cuda_lib):
+    w = wl.to_device(wl.paged_decode("cpu", batch=8, seq_len=8192, k=2048), "cuda")
+    ref_out, _, _ = oracle.run_workload(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, _, _ = cuda_lib.run_workload(w, flags=DET, stream=s)
+    s.synchronize()
+    np.testing.assert_array_equal(np.sort(out.cpu().numpy(), 1), np.sort(ref_out, 1))
+
+
+# ---------------------------------------------------------------- full sizes, sampled rows
+
+def _sample_and_check(topk, w, rows, flags=(DET, 0)):
+    assert_windows_in_bounds(w)
+    hw_rows = wl.select_rows(w, rows)
+    ref_out, ref_raw, _ = oracle.run_workload(hw_rows)
+    hw = HostWorkload(hw_rows)
+    for f in flags:
+        B, k = int(w["batch"]), int(w["k"])
+        out = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+        raw = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+        topk.run_workload(w, out=out, out_raw=raw, flags=f)
+        idx = torch.tensor(rows, device="cuda")
+        o = out[idx].cpu().numpy()
+        r = raw[idx].cpu().numpy()
+        compare_with_oracle(hw, o, r, ref_out, ref_raw, deterministic=bool(f & DET))
+        # every row: count and padding invariants on the device copy
+        valid = (raw >= 0).sum(1)
+        lens = w["seq_lens"].clamp(min=0).clamp(max=k)
+        assert torch.equal(valid.to(torch.int32), lens.to(torch.int32))
+        assert not bool((out == CANARY).any())
+
+
+@pytest.mark.slow
+def test_full_paged_decode(cuda_lib):
+    w = wl.paged_decode("cuda")
+    _sample_and_check(cuda_lib, w, [0, 1, 63, 127])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("chunk", [0, 7, 15])
+def test_full_ragged_extend_chunk(cuda_lib, chunk):
+    w = wl.ragged_extend("cuda", chunk=chunk)
+    _sample_and_check(cuda_lib, w, [0, 1, 511, 1023])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("batch", [1, 30, 31])
+def test_full_paged_long(cuda_lib, batch):
+    w = wl.paged_long("cuda", batch=batch, sub_id=batch)
+    _sample_and_check(cuda_lib, w, sorted({0, batch // 2, batch - 1}))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["paged", "ragged"])
+@pytest.mark.parametrize("k", [512, 1024, 2048])
+@pytest.mark.parametrize("batch", [1, 31, 129, 1024])
+def test_full_mixed_sweep(cuda_lib, mode, k, batch):
+    w = wl.mixed("cuda", mode=mode, k=k, batch=batch, sub_id=batch)
+    rows = sorted(set(range(min(batch, 9))) | {batch // 2, batch - 1})
+    _sample_and_check(cuda_lib, w, rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bi", range(9))
+def test_full_mixed_boundary_single_rows(cuda_lib, bi):
+    for mode in ("paged", "ragged"):
+        w = wl.mixed("cuda", mode=mode, k=2048, batch=1, boundary_index=bi, sub_id=50 + bi)
+        _sample_and_check(cuda_lib, w, [0])

@@ -174,6 +174,35 @@ TOPK_API int topk_transform_ragged(const float* scores, int64_t score_stride,
 TOPK_API int topk_read_device_errors(const void* workspace, int32_t* host_error_rows,
                                      uint32_t* host_flags, topk_stream_t stream);
 
+/*
+ * Allocation-free plan + RAGGED transform. The pages have no counterpart; this
+ * entry point exists for callers that cannot allocate device memory, for
+ * example a plugin host that hands a library only its input and output
+ * buffers, or a serving process that reserves all GPU memory up front (for its
+ * KV cache) and forbids allocations afterwards. It computes exactly what
+ * topk_plan followed by topk_transform_ragged computes, with the plan's
+ * workspace taken from an array built into the library instead of from the
+ * caller.
+ *
+ *   Arguments as for topk_transform_ragged, without the workspace.
+ *   batch must be at most TOPK_NOALLOC_MAX_BATCH; a larger batch returns
+ *   TOPK_ERR_WORKSPACE and enqueues nothing.
+ *
+ * The built-in workspace is about 128 KB, held by every GPU that loads the
+ * library until the process exits. The first call on a device looks up its
+ * address (no allocation); make that first call before any stream capture.
+ * Every call on a device shares the one array and rewrites it: calls whose
+ * GPU work may overlap (different streams, or different host threads without
+ * ordering) race and must be serialised by the caller. Device data-error
+ * counts of this entry point are not reported.
+ */
+#define TOPK_NOALLOC_MAX_BATCH 16384
+TOPK_API int topk_transform_ragged_noalloc(const float* scores, int64_t score_stride,
+                                           const int32_t* row_starts, const int32_t* seq_lens,
+                                           const int32_t* out_offsets, int32_t batch, int32_t k,
+                                           int32_t* out, int32_t* out_raw, uint32_t flags,
+                                           topk_stream_t stream);
+
 /* A static, human-readable name for a topk_status value. Host only. */
 TOPK_API const char* topk_status_string(int status);
 

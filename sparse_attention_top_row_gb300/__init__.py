@@ -30,7 +30,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
 
 EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_ragged",
-            "topk_read_device_errors", "topk_status_string")
+            "topk_read_device_errors", "topk_status_string", "topk_transform_ragged_noalloc")
+TOPK_NOALLOC_MAX_BATCH = 16384
 
 
 class TopKError(RuntimeError):
@@ -65,6 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                               c_p, c_sz, c_p, c_p, c_u32, c_p]
         lib.topk_read_device_errors.restype = ctypes.c_int
         lib.topk_read_device_errors.argtypes = [c_p, ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_p]
+        lib.topk_transform_ragged_noalloc.restype = ctypes.c_int
+        lib.topk_transform_ragged_noalloc.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_p, c_p, c_u32, c_p]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_status_string.argtypes = [ctypes.c_int]
         _LIB = lib
@@ -123,6 +126,17 @@ def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_o
         _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(out_offsets),
         batch, int(k), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _ptr(out_raw), int(flags), _stream(stream)))
+
+
+def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int, out,
+                                  out_raw=None, flags: int = 0, stream=None):
+    """Plan + RAGGED transform without a caller workspace (the library's
+    built-in one; batch <= TOPK_NOALLOC_MAX_BATCH). See include/topk.h."""
+    lib = load()
+    batch = int(seq_lens.numel())
+    _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(
+        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(out_offsets), batch, int(k),
+        _ptr(out), _ptr(out_raw), int(flags), _stream(stream)))
 
 
 def topk_read_device_errors(workspace, stream=None):

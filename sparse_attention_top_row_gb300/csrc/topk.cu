@@ -1030,3 +1030,72 @@ const char* topk_status_string(int status) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Allocation-free entry point (plan + RAGGED transform on a built-in workspace)
+// ----------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kNoAllocWorkspaceBytes =
+    (sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(TOPK_NOALLOC_MAX_BATCH) + 255) / 256 * 256;
+
+}  // namespace
+
+// The plan workspace used by topk_transform_ragged_noalloc: one per GPU that
+// loads the library, kept until the process exits. Host code must not pass
+// this name to a kernel (on the host it is only a stand-in symbol); it uses the
+// device address looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
+namespace {
+
+struct NoAllocState {
+    bool ready = false;
+    void* ptr = nullptr;  // device address of g_noalloc_workspace on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Looks up the device address of the built-in workspace, once per device,
+// with that device current.
+cudaError_t noalloc_workspace(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocState& st = g_noalloc[dev];
+    if (!st.ready) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_workspace);
+        if (e != cudaSuccess || ptr == nullptr) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+        st.ptr = ptr;
+        st.ready = true;
+    }
+    *out = st.ptr;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int topk_transform_ragged_noalloc(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                                             const int32_t* seq_lens, const int32_t* out_offsets, int32_t batch,
+                                             int32_t k, int32_t* out, int32_t* out_raw, uint32_t flags,
+                                             topk_stream_t stream) {
+    if (batch > TOPK_NOALLOC_MAX_BATCH) return TOPK_ERR_WORKSPACE;
+    // validate everything before anything is enqueued (a stand-in non-null
+    // workspace pointer: the real one is looked up below)
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, g_noalloc, kNoAllocWorkspaceBytes, out);
+    if (st != TOPK_OK) return st;
+    if (batch > 0 && out_offsets == nullptr) return TOPK_ERR_ARG;
+    if (batch == 0) return TOPK_OK;
+    void* ws = nullptr;
+    if (noalloc_workspace(&ws) != cudaSuccess) return TOPK_ERR_CUDA;
+    // the plan rewrites the whole header and both row lists, so nothing left
+    // by an earlier call is read
+    const int ps = topk_plan(seq_lens, batch, k, ws, kNoAllocWorkspaceBytes, stream);
+    if (ps != TOPK_OK) return ps;
+    return topk_transform_ragged(scores, score_stride, row_starts, seq_lens, out_offsets, batch, k, ws,
+                                 kNoAllocWorkspaceBytes, out, out_raw, flags, stream);
+}

@@ -169,6 +169,21 @@ __device__ __forceinline__ float4 load_stream(const float4* p) {
     return r;
 }
 
+// The same 16 bytes as raw integer bits (keys and key compares are integer
+// work; the bits never pass through a float register).
+__device__ __forceinline__ int4 load_stream_bits(const float4* p) {
+    int4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Order-preserving key of raw fp32 bits (same map as score_key).
+__device__ __forceinline__ uint32_t bits_key(uint32_t b) {
+    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -190,60 +205,82 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, int32_t pos) {
     return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~pos);
 }
 
-// Radix levels over the 64-bit composite: 12/12/8 bits of the key, then
-// 12/12/8 bits of ~position (deterministic tie-break only).
+// Radix levels over the 64-bit composite: 12/8/8/4 bits of the key, then
+// 8/8/8/8 bits of ~position (deterministic tie-break only).
+constexpr int kKeyLevels = 4;
+constexpr int kAllLevels = 8;
 __device__ __forceinline__ int level_shift(int lvl) {
-    return lvl == 0 ? 52 : lvl == 1 ? 40 : lvl == 2 ? 32 : lvl == 3 ? 20 : lvl == 4 ? 8 : 0;
+    return lvl == 0 ? 52 : lvl == 1 ? 44 : lvl == 2 ? 36 : lvl == 3 ? 32 : 8 * (7 - lvl);
 }
-__device__ __forceinline__ int level_bins(int lvl) { return (lvl == 2 || lvl == 5) ? 256 : kBins; }
+__device__ __forceinline__ int level_bins(int lvl) { return lvl == 0 ? kBins : lvl == 3 ? 16 : 256; }
 
 // Finds the largest bin d of h[0..nb) with sum_{c >= d} h[c] >= target and
-// returns it with above = sum_{c > d} h[c] and count = h[d]. target must be
-// in [1, sum(h)]. All threads of the CTA call it; it synchronises twice.
+// returns it with above = sum_{c > d} h[c] and count = h[d]; `found` is false
+// (with above = the total) when target exceeds the total. nb is 4096, 256 or
+// 16 (h 16-byte aligned). Warp 0 scans from the top in blocks of 256 bins
+// (lane l holds bins 8l..8l+7 of a block, a warp-shuffle suffix sum orders
+// them) and stops at the block holding the answer; the other warps wait at
+// the barrier. All threads call it; it synchronises once.
 struct Threshold {
     uint32_t bin, above, count;
+    bool found;
 };
 
 __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, const Shared& sh) {
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int bpt = (nb + kThreads - 1) / kThreads;
-    const int lo = tid * bpt;
-    uint32_t s = 0;
-    for (int i = 0; i < bpt; ++i) {
-        const int c = lo + i;
-        if (c < nb) s += h[c];
-    }
-    // suffix sum over lanes >= this lane
-    uint32_t x = s;
+    if (threadIdx.x < 32) {
+        const uint32_t lane = lane_id();
+        uint32_t run = 0;  // count in the bins above the current block
+        bool found = false;
+        for (int top = nb; top > 0 && !found; top -= 256) {
+            const int lo = max(top - 256, 0) + 8 * static_cast<int>(lane);
+            uint32_t b[8];
+            if (lo < top) {
+                const uint4 u = reinterpret_cast<const uint4*>(h + lo)[0];
+                const uint4 v = reinterpret_cast<const uint4*>(h + lo)[1];
+                b[0] = u.x, b[1] = u.y, b[2] = u.z, b[3] = u.w, b[4] = v.x, b[5] = v.y, b[6] = v.z, b[7] = v.w;
+            } else {
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_down_sync(kFull, x, off);
-        if (lane_id() + off < 32) x += y;
-    }
-    if (lane_id() == 0) sh.red[warp] = x;
-    __syncthreads();
-    uint32_t above_warps = 0;
-    for (int w = warp + 1; w < kWarps; ++w) above_warps += sh.red[w];
-    const uint32_t incl = x + above_warps;
-    const uint32_t excl = incl - s;
-    if (excl < target && incl >= target) {
-        uint32_t run = excl;
-        for (int i = bpt - 1; i >= 0; --i) {
-            const int c = lo + i;
-            if (c >= nb) continue;
-            const uint32_t hc = h[c];
-            if (run + hc >= target) {
-                sh.res[0] = static_cast<uint32_t>(c);
-                sh.res[1] = run;
-                sh.res[2] = hc;
-                break;
+                for (int i = 0; i < 8; ++i) b[i] = 0;
             }
-            run += hc;
+            const uint32_t s8 = b[0] + b[1] + b[2] + b[3] + b[4] + b[5] + b[6] + b[7];
+            uint32_t x = s8;  // sum over lanes >= this lane
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t y = __shfl_down_sync(kFull, x, off);
+                if (lane + off < 32) x += y;
+            }
+            const uint32_t block = __shfl_sync(kFull, x, 0);
+            if (run + block >= target) {  // warp-uniform
+                found = true;
+                const uint32_t incl = run + x, excl = incl - s8;
+                if (excl < target && incl >= target) {
+                    uint32_t r = excl;
+#pragma unroll
+                    for (int i = 7; i >= 0; --i) {
+                        if (r + b[i] >= target) {
+                            sh.res[0] = static_cast<uint32_t>(lo + i);
+                            sh.res[1] = r;
+                            sh.res[2] = b[i];
+                            break;
+                        }
+                        r += b[i];
+                    }
+                }
+            } else {
+                run += block;
+            }
+        }
+        if (lane == 0) {
+            if (!found) {
+                sh.res[0] = 0;
+                sh.res[1] = run;
+                sh.res[2] = 0;
+            }
+            sh.res[3] = found ? 1u : 0u;
         }
     }
     __syncthreads();
-    return Threshold{sh.res[0], sh.res[1], sh.res[2]};
+    return Threshold{sh.res[0], sh.res[1], sh.res[2], sh.res[3] != 0};
 }
 
 __device__ __forceinline__ void clear_hist(uint32_t* h, int nb) {
@@ -276,32 +313,52 @@ struct SoloMerge {
         return sh.hist;
     }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt[i]; }
+    // true if `flag` is set on any thread
+    __device__ __forceinline__ bool any(const Shared&, bool flag) const { return __syncthreads_or(flag) != 0; }
 };
 
 struct ClusterMerge {
     // hist (local) -> mhist (sum over the cluster), identical in every CTA.
+    // CTA r sums the 16-byte words w = r, r + 8, ... over all CTAs
+    // (reduce-scatter); then every CTA gathers the words it does not own.
     __device__ const uint32_t* merge(const Shared& sh, int nb) const {
         cg::cluster_group cluster = cg::this_cluster();
-        const unsigned rank = cluster.block_rank();
-        const int per = nb / kClusterSize;
+        const int rank = static_cast<int>(cluster.block_rank());
+        const int words = nb / 4;
         cluster.sync();  // every local histogram is complete
-        for (int i = threadIdx.x; i < per; i += kThreads) {
-            const int bin = static_cast<int>(rank) * per + i;
-            uint32_t s = 0;
+        for (int w = rank + kClusterSize * static_cast<int>(threadIdx.x); w < words; w += kClusterSize * kThreads) {
+            uint4 t = make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int q = 0; q < kClusterSize; ++q) s += cluster.map_shared_rank(sh.hist, q)[bin];
-            sh.mhist[bin] = s;
+            for (int q = 0; q < kClusterSize; ++q) {
+                const uint4 r = reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.hist, q))[w];
+                t.x += r.x, t.y += r.y, t.z += r.z, t.w += r.w;
+            }
+            reinterpret_cast<uint4*>(sh.mhist)[w] = t;
         }
-        cluster.sync();  // every slice of the sum is complete
-        for (int i = threadIdx.x; i < nb; i += kThreads) {
-            const int q = i / per;
-            if (q != static_cast<int>(rank)) sh.mhist[i] = cluster.map_shared_rank(sh.mhist, q)[i];
+        cluster.sync();  // every owned word of the sum is complete
+        for (int w = threadIdx.x; w < words; w += kThreads) {
+            const int q = w % kClusterSize;
+            if (q != rank)
+                reinterpret_cast<uint4*>(sh.mhist)[w] =
+                    reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.mhist, q))[w];
         }
         __syncthreads();
         return sh.mhist;
     }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const {
         return cg::this_cluster().map_shared_rank(&sh.cnt[i], 0);
+    }
+    // true if `flag` is set on any thread of any CTA of the cluster
+    __device__ bool any(const Shared& sh, bool flag) const {
+        cg::cluster_group cluster = cg::this_cluster();
+        const bool local = __syncthreads_or(flag) != 0;
+        if (threadIdx.x == 0) sh.cnt[4] = local ? 1u : 0u;
+        cluster.sync();
+        uint32_t v = 0;
+        if (threadIdx.x < kClusterSize) v = *cluster.map_shared_rank(&sh.cnt[4], threadIdx.x);
+        const bool r = __syncthreads_or(v != 0) != 0;
+        cluster.sync();  // no CTA rewrites its flag before every CTA has read it
+        return r;
     }
 };
 
@@ -403,13 +460,21 @@ __device__ void run_levels(SelState& st, int first, int last, const Src& src, co
         const int shift = level_shift(lvl);
         clear_hist(sh.hist, nb);
         __syncthreads();
-        const uint64_t prefix = st.prefix, mask = st.mask;
         uint32_t* hist = sh.hist;
-        src.visit([&](uint32_t key, int32_t pos, bool valid) {
-            const uint64_t c = composite(key, pos);
-            if (valid && (c & mask) == prefix)
-                atomicAdd(&hist[static_cast<uint32_t>(c >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-        });
+        const uint32_t digit = static_cast<uint32_t>(nb - 1);
+        if (lvl < kKeyLevels) {  // key digits: a 32-bit filter on the resolved key bits
+            const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32), msk = static_cast<uint32_t>(st.mask >> 32);
+            const int sh32 = shift - 32;
+            src.visit([&](uint32_t key, int32_t, bool valid) {
+                if (valid && (key & msk) == pfx) atomicAdd(&hist[(key >> sh32) & digit], 1u);
+            });
+        } else {  // position digits of the elements tied at the threshold
+            const uint64_t prefix = st.prefix, mask = st.mask;
+            src.visit([&](uint32_t key, int32_t pos, bool valid) {
+                const uint64_t c = composite(key, pos);
+                if (valid && (c & mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(c >> shift) & digit], 1u);
+            });
+        }
         const uint32_t* merged = mg.merge(sh, nb);
         const Threshold t = find_threshold(merged, nb, st.need, sh);
         apply_level(st, lvl, t);
@@ -451,14 +516,10 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
                               const Merge& mg, const Emitter<kPaged>& em) {
     uint32_t* ctr_def = mg.counter(sh, 1);
     uint32_t* ctr_grp = mg.counter(sh, 2);
-    const uint64_t prefix = st.prefix, mask = st.mask;
     const uint32_t need = st.need;
     const bool exact = st.exact;
     const uint32_t lt = lanemask_lt();
-    src.visit([&](uint32_t key, int32_t pos, bool valid) {
-        const uint64_t hi = composite(key, pos) & mask;
-        const bool def = valid && (hi > prefix || (exact && hi == prefix));
-        const bool grp = valid && !exact && hi == prefix;
+    auto place = [&](bool def, bool grp, int32_t pos) {
         const uint32_t md = __ballot_sync(kFull, def);
         if (md) {
             const int leader = __ffs(md) - 1;
@@ -476,7 +537,21 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
             const uint32_t t = base + __popc(mgp & lt);
             if (grp && t < need) em.write(k - need + t, pos);
         }
-    });
+    };
+    if (static_cast<uint32_t>(st.mask) == 0) {
+        // only key levels ran: the mask is top-aligned, so "masked key above
+        // the prefix" is a plain compare against the prefix (exact) or tau
+        const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32);
+        src.visit([&](uint32_t key, int32_t pos, bool valid) {
+            place(valid && (exact ? key >= pfx : key > pfx), valid && !exact && key == pfx, pos);
+        });
+    } else {
+        const uint64_t prefix = st.prefix, mask = st.mask;
+        src.visit([&](uint32_t key, int32_t pos, bool valid) {
+            const uint64_t hi = composite(key, pos) & mask;
+            place(valid && (hi > prefix || (exact && hi == prefix)), valid && !exact && hi == prefix, pos);
+        });
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -508,7 +583,7 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
     const RegSource<NV> src{v, rem, len};
     SoloMerge mg;
     SelState st{0ull, 0ull, k, false};
-    run_levels(st, 0, det ? 5 : 2, src, sh, mg);
+    run_levels(st, 0, (det ? kAllLevels : kKeyLevels) - 1, src, sh, mg);
     emit_selected<kPaged>(st, k, src, sh, mg, em);
 }
 
@@ -576,80 +651,132 @@ __device__ __forceinline__ uint32_t pass_bits(const uint32_t (&key)[4 * kTileVec
     return pass;
 }
 
-// Streaming route over vectors [jb, je) of the aligned window (the whole row
-// on one CTA, or this CTA's slice of a cluster row).
+// Loads one tile (kTileVecs vectors per thread from vector j0) and returns the
+// bit mask of its in-window elements whose key is at least bound_key, with
+// their keys. For a non-negative bound (the usual case) the test is one
+// signed compare of the raw bits: key >= bound_key <=> bits >= bound_key ^ 2^31.
+__device__ __forceinline__ uint32_t load_pass(const float4* vbase, int j0, int je, int rem, int len,
+                                              uint32_t bound_key, uint32_t (&key)[4 * kTileVecs]) {
+    int4 v[kTileVecs];
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < je ? load_stream_bits(vbase + j) : make_int4(0, 0, 0, 0);
+    }
+    const int first = 4 * j0 - rem;
+    const bool interior =
+        first >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
+    uint32_t pass = 0;
+    if (interior && bound_key >= 0x80000000u) {
+        const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
+#pragma unroll
+        for (int u = 0; u < kTileVecs; ++u) {
+            const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                key[4 * u + c] = static_cast<uint32_t>(e[c]) | 0x80000000u;  // the key when it passes
+                pass |= static_cast<uint32_t>(e[c] >= bb) << (4 * u + c);
+            }
+        }
+        return pass;
+    }
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        const int p0 = 4 * j - rem;
+        const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t kk = bits_key(static_cast<uint32_t>(e[c]));
+            key[4 * u + c] = kk;
+            if (j < je && static_cast<unsigned>(p0 + c) < static_cast<unsigned>(len) && kk >= bound_key)
+                pass |= 1u << (4 * u + c);
+        }
+    }
+    return pass;
+}
+
+// Number of window positions p in [4*ja - rem, 4*jb - rem) (vectors [ja, jb)).
+__device__ __forceinline__ int window_count(int ja, int jb, int rem, int len) {
+    const int lo = max(4 * ja - rem, 0), hi = min(4 * jb - rem, len);
+    return max(hi - lo, 0);
+}
+
+// Level-1 histogram of the candidate buffer.
+__device__ __forceinline__ void hist_cands(const Shared& sh, uint32_t n) {
+    for (uint32_t i = threadIdx.x; i < n; i += kThreads) atomicAdd(&sh.hist[sh.cand_key[i] >> 20], 1u);
+}
+
+// Streaming route over vectors [jb, je) of the aligned window: the whole row
+// on one CTA, or this CTA's slice of a cluster row of nv vectors cut into
+// `parts` slices of `per` vectors.
+//  1. The head tile of every slice gets a full level-1 histogram; the merged
+//     head histogram sets a lower bound on the threshold bin, aiming about
+//     4 sigma above the row's expected share of the top-k in the heads.
+//  2. One pass over the rest collects every element at or above the bound.
+//  3. Level 1 comes from the candidates' histogram. It is exact when they
+//     number at least k (they then hold every element of every bin at or
+//     above the threshold bin); otherwise, or if a buffer overflowed, a full
+//     histogram pass and a re-collection run (always exact, only slower).
 template <bool kPaged, class Merge>
-__device__ void streaming_row(const float4* vbase, int jb, int je, int rem, int len, uint32_t k,
-                              bool det, const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
-    // --- head tile: histogram only, then a lower bound for collection
+__device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int per, int parts, int rem, int len,
+                              uint32_t k, bool det, const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
     uint32_t key[4 * kTileVecs];
     uint32_t valid_bits;
-    load_tile(vbase, jb, je, rem, len, key, valid_bits, sh);
-    // elements of the head tile in the window
-    const int head_first = 4 * jb - rem, head_end = 4 * min(je, jb + kTileVecs * kThreads) - rem;
-    const int n_head = max(0, min(head_end, len) - max(head_first, 0));
-    __syncthreads();
+    load_tile(vbase, jb, je, rem, len, key, valid_bits, sh);  // full histogram of the head tile
+    const uint32_t* head = mg.merge(sh, kBins);
+    int n_head = 0;
+    for (int r = 0; r < parts; ++r) {
+        const int a = min(nv, r * per), b = min(nv, a + per);
+        n_head += window_count(a, min(b, a + kTileVecs * kThreads), rem, len);
+    }
     uint32_t bound_bin = 0;
     if (n_head > 0) {
-        // expected share of the row's top-k in the head tile, plus ~4 sigma
         const float expect = static_cast<float>(k) * static_cast<float>(n_head) / static_cast<float>(len);
-        float tgt = expect + 4.0f * sqrtf(expect) + 16.0f;
-        uint32_t target = static_cast<uint32_t>(fminf(tgt, static_cast<float>(n_head)));
-        target = max(target, 1u);
-        bound_bin = find_threshold(sh.hist, kBins, target, sh).bin;
+        const float tgt = fminf(expect + 4.0f * sqrtf(expect) + 16.0f, static_cast<float>(n_head));
+        bound_bin = find_threshold(head, kBins, max(static_cast<uint32_t>(tgt), 1u), sh).bin;
     }
+    const uint32_t bound_key = bound_bin << 20;
     collect_tile(key, pass_bits(key, valid_bits, bound_bin), jb, rem, sh);
-
-    // --- main pass
     for (int j0 = jb + kTileVecs * kThreads; j0 < je; j0 += kTileVecs * kThreads) {
-        load_tile(vbase, j0, je, rem, len, key, valid_bits, sh);
-        collect_tile(key, pass_bits(key, valid_bits, bound_bin), j0, rem, sh);
+        const uint32_t pass = load_pass(vbase, j0, je, rem, len, bound_key, key);
+        collect_tile(key, pass, j0, rem, sh);
     }
-
-    // --- level 1 over the merged histogram
+    __syncthreads();
+    const uint32_t n_cand = sh.cnt[0];
+    const bool overflow = n_cand > static_cast<uint32_t>(kCandCap);
+    clear_hist(sh.hist, kBins);
+    __syncthreads();
+    if (!overflow) hist_cands(sh, n_cand);
     const uint32_t* merged = mg.merge(sh, kBins);
-    SelState st{0ull, 0ull, k, false};
-    const Threshold t1 = find_threshold(merged, kBins, k, sh);
-    apply_level(st, 0, t1);
-
-    bool cands_ok = sh.cnt[0] <= static_cast<uint32_t>(kCandCap) && t1.bin >= bound_bin;
-    if (!cands_ok) {
-        // re-collect from global memory if this CTA's elements at or above the
-        // threshold bin fit the buffer
-        const uint32_t local = count_from(sh.hist, kBins, t1.bin, sh);
-        if (local <= static_cast<uint32_t>(kCandCap)) {
+    Threshold t1 = find_threshold(merged, kBins, k, sh);
+    bool cands_ok = true;
+    if (mg.any(sh, overflow) || !t1.found) {  // uniform over a cluster
+        // full level-1 histogram of this CTA's elements, then re-collect
+        clear_hist(sh.hist, kBins);
+        __syncthreads();
+        uint32_t* hist = sh.hist;
+        const GlobalSource all{vbase, jb, je, rem, len};
+        all.visit([&](uint32_t kk, int32_t, bool valid) {
+            if (valid) atomicAdd(&hist[kk >> 20], 1u);
+        });
+        merged = mg.merge(sh, kBins);
+        t1 = find_threshold(merged, kBins, k, sh);
+        cands_ok = false;
+        if (count_from(sh.hist, kBins, t1.bin, sh) <= static_cast<uint32_t>(kCandCap)) {
             if (threadIdx.x == 0) sh.cnt[0] = 0;
             __syncthreads();
             for (int j0 = jb; j0 < je; j0 += kTileVecs * kThreads) {
-                float4 v[kTileVecs];
-#pragma unroll
-                for (int u = 0; u < kTileVecs; ++u) {
-                    const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-                    v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                uint32_t pass = 0;
-#pragma unroll
-                for (int u = 0; u < kTileVecs; ++u) {
-                    const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-                    const int p0 = 4 * j - rem;
-                    const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t kk = score_key(e[c]);
-                        key[4 * u + c] = kk;
-                        const int p = p0 + c;
-                        if (j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len) &&
-                            (kk >> 20) >= t1.bin)
-                            pass |= 1u << (4 * u + c);
-                    }
-                }
+                const uint32_t pass = load_pass(vbase, j0, je, rem, len, t1.bin << 20, key);
                 collect_tile(key, pass, j0, rem, sh);
             }
             __syncthreads();
             cands_ok = true;
         }
     }
-    const int last = det ? 5 : 2;
+    SelState st{0ull, 0ull, k, false};
+    apply_level(st, 0, t1);
+    const int last = (det ? kAllLevels : kKeyLevels) - 1;
     if (cands_ok) {
         const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
         run_levels(st, 1, last, src, sh, mg);
@@ -711,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
         trivial_row<kPaged>(len, k, em);
         return;
     }
-    if (threadIdx.x < 4) sh.cnt[threadIdx.x] = 0;
+    if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
     const int rem = start & 3;
     const float4* vbase = reinterpret_cast<const float4*>(
         p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
@@ -722,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
     } else {
         clear_hist(sh.hist, kBins);
         __syncthreads();
-        streaming_row<kPaged>(vbase, 0, nv, rem, len, k, det, sh, SoloMerge{}, em);
+        streaming_row<kPaged>(vbase, 0, nv, nv, nv, 1, rem, len, k, det, sh, SoloMerge{}, em);
     }
 }
 
@@ -756,7 +883,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
             cluster.sync();
             continue;
         }
-        if (threadIdx.x < 4) sh.cnt[threadIdx.x] = 0;
+        if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
         clear_hist(sh.hist, kBins);
         const int rem = start & 3;
         const float4* vbase = reinterpret_cast<const float4*>(
@@ -768,7 +895,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         // counters of the leader CTA must be zero before any CTA emits: the
         // merges below pass several cluster barriers first
         __syncthreads();
-        streaming_row<kPaged>(vbase, jb, je, rem, len, k, det, sh, mg, em);
+        streaming_row<kPaged>(vbase, jb, je, nv, per, kClusterSize, rem, len, k, det, sh, mg, em);
         cluster.sync();  // all emits done before the leader's counters are reset
     }
 }

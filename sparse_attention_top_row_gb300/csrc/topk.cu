@@ -64,8 +64,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
 constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
 constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
-constexpr int kRegVecs = 4;                   // register route: 4 vectors per thread (L <= 8192)
-constexpr int kClusterSize = 8;               // CTAs per long row on the cluster path
+constexpr int kClusterSize = 4;               // CTAs per long row on the cluster path
 constexpr int kPlanThreads = 1024;
 constexpr int32_t kClusterFloor = 32768;      // rows longer than this may use the cluster path
 constexpr int32_t kClusterMaxBatch = 64;      // ... when the batch is at most this
@@ -284,7 +283,7 @@ __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, 
 }
 
 __device__ __forceinline__ void clear_hist(uint32_t* h, int nb) {
-    for (int i = threadIdx.x; i < nb; i += kThreads) h[i] = 0u;
+    for (int i = threadIdx.x; i < nb / 4; i += kThreads) reinterpret_cast<uint4*>(h)[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Sum over the CTA of h[c] for c >= from (bins of the local histogram).
@@ -308,6 +307,7 @@ __device__ uint32_t count_from(const uint32_t* h, int nb, uint32_t from, const S
 // ----------------------------------------------------------------------------
 
 struct SoloMerge {
+    static constexpr bool kSolo = true;
     __device__ __forceinline__ const uint32_t* merge(const Shared& sh, int) const {
         __syncthreads();
         return sh.hist;
@@ -318,6 +318,7 @@ struct SoloMerge {
 };
 
 struct ClusterMerge {
+    static constexpr bool kSolo = false;
     // hist (local) -> mhist (sum over the cluster), identical in every CTA.
     // CTA r sums the 16-byte words w = r, r + 8, ... over all CTAs
     // (reduce-scatter); then every CTA gathers the words it does not own.
@@ -508,50 +509,75 @@ struct Emitter {
     }
 };
 
-// Writes the k selected elements of `src` to their slots. Definite elements
-// take slots [0, k - need) from counter 1, the threshold group takes
-// [k - need, k) from counter 2 (the first `need` to arrive win, unless exact).
+// Writes the k selected elements of `src`: definite elements to slots
+// [0, k - need), the first `need` members of the threshold group (all of it
+// when exact) to [k - need, k). Two visits with the same thread-to-element
+// assignment: the first counts each thread's elements of both kinds, a
+// block-wide exclusive scan (plus, on a cluster, one atomic per CTA on the
+// leader's counters) gives every thread its first slots, the second writes.
 template <bool kPaged, class Merge, class Src>
 __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, const Shared& sh,
                               const Merge& mg, const Emitter<kPaged>& em) {
-    uint32_t* ctr_def = mg.counter(sh, 1);
-    uint32_t* ctr_grp = mg.counter(sh, 2);
     const uint32_t need = st.need;
     const bool exact = st.exact;
-    const uint32_t lt = lanemask_lt();
-    auto place = [&](bool def, bool grp, int32_t pos) {
-        const uint32_t md = __ballot_sync(kFull, def);
-        if (md) {
-            const int leader = __ffs(md) - 1;
-            uint32_t base = 0;
-            if (lane_id() == static_cast<uint32_t>(leader)) base = atomicAdd(ctr_def, __popc(md));
-            base = __shfl_sync(kFull, base, leader);
-            if (def) em.write(base + __popc(md & lt), pos);
-        }
-        const uint32_t mgp = __ballot_sync(kFull, grp);
-        if (mgp) {
-            const int leader = __ffs(mgp) - 1;
-            uint32_t base = 0;
-            if (lane_id() == static_cast<uint32_t>(leader)) base = atomicAdd(ctr_grp, __popc(mgp));
-            base = __shfl_sync(kFull, base, leader);
-            const uint32_t t = base + __popc(mgp & lt);
-            if (grp && t < need) em.write(k - need + t, pos);
+    const bool key_only = static_cast<uint32_t>(st.mask) == 0;  // only key levels ran
+    const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32);
+    const uint64_t prefix = st.prefix, mask = st.mask;
+    // with a top-aligned mask, "masked key above the prefix" is a plain
+    // compare against the prefix (exact) or tau
+    auto classify = [&](uint32_t key, int32_t pos, bool valid, bool& def, bool& grp) {
+        if (key_only) {
+            def = valid && (exact ? key >= pfx : key > pfx);
+            grp = valid && !exact && key == pfx;
+        } else {
+            const uint64_t hi = composite(key, pos) & mask;
+            def = valid && (hi > prefix || (exact && hi == prefix));
+            grp = valid && !exact && hi == prefix;
         }
     };
-    if (static_cast<uint32_t>(st.mask) == 0) {
-        // only key levels ran: the mask is top-aligned, so "masked key above
-        // the prefix" is a plain compare against the prefix (exact) or tau
-        const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32);
-        src.visit([&](uint32_t key, int32_t pos, bool valid) {
-            place(valid && (exact ? key >= pfx : key > pfx), valid && !exact && key == pfx, pos);
-        });
-    } else {
-        const uint64_t prefix = st.prefix, mask = st.mask;
-        src.visit([&](uint32_t key, int32_t pos, bool valid) {
-            const uint64_t hi = composite(key, pos) & mask;
-            place(valid && (hi > prefix || (exact && hi == prefix)), valid && !exact && hi == prefix, pos);
-        });
+    uint32_t nd = 0, ng = 0;
+    src.visit([&](uint32_t key, int32_t pos, bool valid) {
+        bool d, g;
+        classify(key, pos, valid, d, g);
+        nd += d;
+        ng += g;
+    });
+    const uint32_t xd = warp_inclusive_scan(nd), xg = warp_inclusive_scan(ng);
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    if (lane_id() == 31) {
+        sh.red[warp] = xd;
+        sh.red[kWarps + warp] = xg;
     }
+    __syncthreads();
+    uint32_t bd = xd - nd, bg = xg - ng, td = 0, tg = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t rd = sh.red[w], rg = sh.red[kWarps + w];
+        bd += w < warp ? rd : 0u;
+        bg += w < warp ? rg : 0u;
+        td += rd;
+        tg += rg;
+    }
+    if (!Merge::kSolo) {  // this CTA's share of the cluster-wide slot ranges
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            sh.red[0] = td ? atomicAdd(mg.counter(sh, 1), td) : 0u;
+            sh.red[1] = tg ? atomicAdd(mg.counter(sh, 2), tg) : 0u;
+        }
+        __syncthreads();
+        bd += sh.red[0];
+        bg += sh.red[1];
+    }
+    src.visit([&](uint32_t key, int32_t pos, bool valid) {
+        bool d, g;
+        classify(key, pos, valid, d, g);
+        if (d) em.write(bd++, pos);
+        if (g) {
+            if (bg < need) em.write(k - need + bg, pos);
+            ++bg;
+        }
+    });
+    __syncthreads();  // red is free again
 }
 
 // ----------------------------------------------------------------------------
@@ -570,27 +596,61 @@ __device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em) 
     }
 }
 
-// Register route: the whole aligned window (nv vectors) fits NV vectors per thread.
-template <bool kPaged, int NV>
-__device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
-                             const Shared& sh, const Emitter<kPaged>& em) {
-    float4 v[NV];
+
+
+
+
+// Raw bits of one tile: kTileVecs vectors per thread from vector j0 (vectors
+// at or past je read as zero bits and are never in the window).
+__device__ __forceinline__ void load_bits(int4 (&v)[kTileVecs], const float4* vbase, int j0, int je) {
 #pragma unroll
-    for (int u = 0; u < NV; ++u) {
-        const int j = u * kThreads + static_cast<int>(threadIdx.x);
-        v[u] = j < nv ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < je ? load_stream_bits(vbase + j) : make_int4(0, 0, 0, 0);
     }
-    const RegSource<NV> src{v, rem, len};
-    SoloMerge mg;
-    SelState st{0ull, 0ull, k, false};
-    run_levels(st, 0, (det ? kAllLevels : kKeyLevels) - 1, src, sh, mg);
-    emit_selected<kPaged>(st, k, src, sh, mg, em);
 }
 
-// Appends, warp-aggregated, the elements flagged in `pass` (bit e = element e
-// of this thread's tile) to the candidate buffer.
-__device__ __forceinline__ void collect_tile(const uint32_t (&key)[4 * kTileVecs], uint32_t pass,
-                                             int j0, int rem, const Shared& sh) {
+__device__ __forceinline__ int tile_elem(const int4 (&v)[kTileVecs], int e) {
+    const int4 q = v[e / 4];
+    return (e % 4) == 0 ? q.x : (e % 4) == 1 ? q.y : (e % 4) == 2 ? q.z : q.w;
+}
+
+// Bit e set: element e of this thread's tile at vector j0 lies in the window.
+__device__ __forceinline__ uint32_t tile_valid(int j0, int je, int rem, int len) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e) {
+        const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
+        if (j < je && static_cast<unsigned>(4 * j - rem + (e % 4)) < static_cast<unsigned>(len)) m |= 1u << e;
+    }
+    return m;
+}
+
+// Bit mask of the tile's in-window elements whose key is at least bound_key.
+// For an interior tile and a non-negative bound (the usual case) the test is
+// one signed compare of the raw bits: key >= bound_key <=> bits >= bound_key ^ 2^31.
+__device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0, int je, int rem, int len,
+                                              uint32_t bound_key) {
+    const bool interior =
+        4 * j0 - rem >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
+    uint32_t pass = 0;
+    if (interior && bound_key >= 0x80000000u) {
+        const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
+#pragma unroll
+        for (int e = 0; e < 4 * kTileVecs; ++e) pass |= static_cast<uint32_t>(tile_elem(v, e) >= bb) << e;
+        return pass;
+    }
+    const uint32_t valid = tile_valid(j0, je, rem, len);
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e)
+        pass |= static_cast<uint32_t>(bits_key(static_cast<uint32_t>(tile_elem(v, e))) >= bound_key) << e;
+    return pass & valid;
+}
+
+// Appends the tile elements flagged in `pass` to the candidate buffer: one
+// warp scan and one shared atomic per warp.
+__device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_t pass, int j0, int rem,
+                                             const Shared& sh, bool count_hist = false) {
     const uint32_t c = __popc(pass);
     const uint32_t incl = warp_inclusive_scan(c);
     const uint32_t total = __shfl_sync(kFull, incl, 31);
@@ -602,9 +662,11 @@ __device__ __forceinline__ void collect_tile(const uint32_t (&key)[4 * kTileVecs
 #pragma unroll
     for (int e = 0; e < 4 * kTileVecs; ++e) {
         if ((pass >> e) & 1u) {
+            const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
+            if (count_hist) atomicAdd(&sh.hist[kk >> 20], 1u);
             if (idx < static_cast<uint32_t>(kCandCap)) {
                 const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
-                sh.cand_key[idx] = key[e];
+                sh.cand_key[idx] = kk;
                 sh.cand_pos[idx] = 4 * j - rem + (e % 4);
             }
             ++idx;
@@ -612,88 +674,44 @@ __device__ __forceinline__ void collect_tile(const uint32_t (&key)[4 * kTileVecs
     }
 }
 
-// Loads one tile (kTileVecs vectors per thread starting at vector j0), adds
-// every in-window element to the level-1 histogram and returns the keys.
-__device__ __forceinline__ void load_tile(const float4* vbase, int j0, int je, int rem, int len,
-                                          uint32_t (&key)[4 * kTileVecs], uint32_t& valid_bits,
-                                          const Shared& sh) {
-    float4 v[kTileVecs];
-#pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    valid_bits = 0;
-#pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        const int p0 = 4 * j - rem;
-        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int p = p0 + c;
-            const uint32_t kk = score_key(e[c]);
-            key[4 * u + c] = kk;
-            if (j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len)) {
-                valid_bits |= 1u << (4 * u + c);
-                atomicAdd(&sh.hist[kk >> 20], 1u);
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t pass_bits(const uint32_t (&key)[4 * kTileVecs], uint32_t valid_bits,
-                                              uint32_t bound_bin) {
-    uint32_t pass = 0;
+// Register route: the whole aligned window (nv <= kTileVecs * kThreads
+// vectors) is one register tile. Level 1 is a full histogram; every element
+// at or above its threshold bin is then compacted into the candidate buffer,
+// and the later levels and the emit loop over that buffer (a fallback keeps
+// them on the registers when the threshold bin is too full to copy).
+template <bool kPaged>
+__device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
+                             const Shared& sh, const Emitter<kPaged>& em) {
+    int4 v[kTileVecs];
+    load_bits(v, vbase, 0, nv);  // in flight while the histogram is cleared
+    clear_hist(sh.hist, kBins);
+    __syncthreads();
+    const uint32_t valid = tile_valid(0, nv, rem, len);
 #pragma unroll
     for (int e = 0; e < 4 * kTileVecs; ++e)
-        if (((valid_bits >> e) & 1u) && (key[e] >> 20) >= bound_bin) pass |= 1u << e;
-    return pass;
-}
-
-// Loads one tile (kTileVecs vectors per thread from vector j0) and returns the
-// bit mask of its in-window elements whose key is at least bound_key, with
-// their keys. For a non-negative bound (the usual case) the test is one
-// signed compare of the raw bits: key >= bound_key <=> bits >= bound_key ^ 2^31.
-__device__ __forceinline__ uint32_t load_pass(const float4* vbase, int j0, int je, int rem, int len,
-                                              uint32_t bound_key, uint32_t (&key)[4 * kTileVecs]) {
-    int4 v[kTileVecs];
+        if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> 20], 1u);
+    __syncthreads();
+    const Threshold t1 = find_threshold(sh.hist, kBins, k, sh);
+    SoloMerge mg;
+    SelState st{0ull, 0ull, k, false};
+    apply_level(st, 0, t1);
+    const int last = (det ? kAllLevels : kKeyLevels) - 1;
+    if (t1.above + t1.count <= static_cast<uint32_t>(kCandCap)) {
+        collect_bits(v, tile_pass(v, 0, nv, rem, len, t1.bin << 20), 0, rem, sh);
+        __syncthreads();
+        const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
+        run_levels(st, 1, last, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    } else {
+        float4 f[kTileVecs];
 #pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        v[u] = j < je ? load_stream_bits(vbase + j) : make_int4(0, 0, 0, 0);
+        for (int u = 0; u < kTileVecs; ++u)
+            f[u] = make_float4(__int_as_float(v[u].x), __int_as_float(v[u].y), __int_as_float(v[u].z),
+                               __int_as_float(v[u].w));
+        const RegSource<kTileVecs> src{f, rem, len};
+        run_levels(st, 1, last, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
     }
-    const int first = 4 * j0 - rem;
-    const bool interior =
-        first >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
-    uint32_t pass = 0;
-    if (interior && bound_key >= 0x80000000u) {
-        const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
-#pragma unroll
-        for (int u = 0; u < kTileVecs; ++u) {
-            const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                key[4 * u + c] = static_cast<uint32_t>(e[c]) | 0x80000000u;  // the key when it passes
-                pass |= static_cast<uint32_t>(e[c] >= bb) << (4 * u + c);
-            }
-        }
-        return pass;
-    }
-#pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        const int p0 = 4 * j - rem;
-        const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t kk = bits_key(static_cast<uint32_t>(e[c]));
-            key[4 * u + c] = kk;
-            if (j < je && static_cast<unsigned>(p0 + c) < static_cast<unsigned>(len) && kk >= bound_key)
-                pass |= 1u << (4 * u + c);
-        }
-    }
-    return pass;
 }
 
 // Number of window positions p in [4*ja - rem, 4*jb - rem) (vectors [ja, jb)).
@@ -702,10 +720,6 @@ __device__ __forceinline__ int window_count(int ja, int jb, int rem, int len) {
     return max(hi - lo, 0);
 }
 
-// Level-1 histogram of the candidate buffer.
-__device__ __forceinline__ void hist_cands(const Shared& sh, uint32_t n) {
-    for (uint32_t i = threadIdx.x; i < n; i += kThreads) atomicAdd(&sh.hist[sh.cand_key[i] >> 20], 1u);
-}
 
 // Streaming route over vectors [jb, je) of the aligned window: the whole row
 // on one CTA, or this CTA's slice of a cluster row of nv vectors cut into
@@ -721,14 +735,21 @@ __device__ __forceinline__ void hist_cands(const Shared& sh, uint32_t n) {
 template <bool kPaged, class Merge>
 __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int per, int parts, int rem, int len,
                               uint32_t k, bool det, const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
-    uint32_t key[4 * kTileVecs];
-    uint32_t valid_bits;
-    load_tile(vbase, jb, je, rem, len, key, valid_bits, sh);  // full histogram of the head tile
+    constexpr int T = kTileVecs * kThreads;
+    int4 cur[kTileVecs], nxt[kTileVecs];
+    load_bits(cur, vbase, jb, je);                   // the head tile
+    if (jb + T < je) load_bits(nxt, vbase, jb + T, je);  // the next tile is in flight meanwhile
+    {
+        const uint32_t valid = tile_valid(jb, je, rem, len);
+#pragma unroll
+        for (int e = 0; e < 4 * kTileVecs; ++e)
+            if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(cur, e))) >> 20], 1u);
+    }
     const uint32_t* head = mg.merge(sh, kBins);
     int n_head = 0;
     for (int r = 0; r < parts; ++r) {
         const int a = min(nv, r * per), b = min(nv, a + per);
-        n_head += window_count(a, min(b, a + kTileVecs * kThreads), rem, len);
+        n_head += window_count(a, min(b, a + T), rem, len);
     }
     uint32_t bound_bin = 0;
     if (n_head > 0) {
@@ -737,21 +758,22 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
         bound_bin = find_threshold(head, kBins, max(static_cast<uint32_t>(tgt), 1u), sh).bin;
     }
     const uint32_t bound_key = bound_bin << 20;
-    collect_tile(key, pass_bits(key, valid_bits, bound_bin), jb, rem, sh);
-    for (int j0 = jb + kTileVecs * kThreads; j0 < je; j0 += kTileVecs * kThreads) {
-        const uint32_t pass = load_pass(vbase, j0, je, rem, len, bound_key, key);
-        collect_tile(key, pass, j0, rem, sh);
+    collect_bits(cur, tile_pass(cur, jb, je, rem, len, bound_key), jb, rem, sh);
+    for (int j0 = jb + T; j0 < je; j0 += T) {
+#pragma unroll
+        for (int u = 0; u < kTileVecs; ++u) cur[u] = nxt[u];
+        if (j0 + T < je) load_bits(nxt, vbase, j0 + T, je);  // prefetch
+        collect_bits(cur, tile_pass(cur, j0, je, rem, len, bound_key), j0, rem, sh, true);
     }
     __syncthreads();
-    const uint32_t n_cand = sh.cnt[0];
-    const bool overflow = n_cand > static_cast<uint32_t>(kCandCap);
-    clear_hist(sh.hist, kBins);
-    __syncthreads();
-    if (!overflow) hist_cands(sh, n_cand);
+    const bool overflow = sh.cnt[0] > static_cast<uint32_t>(kCandCap);
+    // The histogram holds every head-tile element and every candidate after
+    // it, so its counts are exact for every bin at or above the bound: level
+    // 1 is exact when its threshold bin is one of them.
     const uint32_t* merged = mg.merge(sh, kBins);
     Threshold t1 = find_threshold(merged, kBins, k, sh);
     bool cands_ok = true;
-    if (mg.any(sh, overflow) || !t1.found) {  // uniform over a cluster
+    if (mg.any(sh, overflow) || !t1.found || t1.bin < bound_bin) {  // uniform over a cluster
         // full level-1 histogram of this CTA's elements, then re-collect
         clear_hist(sh.hist, kBins);
         __syncthreads();
@@ -766,9 +788,9 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
         if (count_from(sh.hist, kBins, t1.bin, sh) <= static_cast<uint32_t>(kCandCap)) {
             if (threadIdx.x == 0) sh.cnt[0] = 0;
             __syncthreads();
-            for (int j0 = jb; j0 < je; j0 += kTileVecs * kThreads) {
-                const uint32_t pass = load_pass(vbase, j0, je, rem, len, t1.bin << 20, key);
-                collect_tile(key, pass, j0, rem, sh);
+            for (int j0 = jb; j0 < je; j0 += T) {
+                load_bits(cur, vbase, j0, je);
+                collect_bits(cur, tile_pass(cur, j0, je, rem, len, t1.bin << 20), j0, rem, sh);
             }
             __syncthreads();
             cands_ok = true;
@@ -844,8 +866,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
         p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
     const int nv = (len + rem + 3) >> 2;
     const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
-    if (nv <= kRegVecs * kThreads) {
-        register_row<kPaged, kRegVecs>(vbase, nv, rem, len, k, det, sh, em);
+    if (nv <= kTileVecs * kThreads) {
+        register_row<kPaged>(vbase, nv, rem, len, k, det, sh, em);
     } else {
         clear_hist(sh.hist, kBins);
         __syncthreads();

@@ -12,23 +12,25 @@
 //  * Keys. A score's fp32 bits map to an order-preserving uint32 key. Every
 //    selection step works on keys, so no score is compared as a float.
 //  * Radix select on a 64-bit composite (key << 32 | ~position). Levels take
-//    12, 12 and 8 bits of the key from the top (a 4096-bin shared-memory
-//    histogram per level; the 12-bit first level is the one the PR #36684
-//    page, "Feature and motivation", describes), then, only when equal scores
-//    straddle the threshold and TOPK_DETERMINISTIC is set, 12/12/8 bits of
-//    ~position, so the lowest positions win. A level stops the descent as soon
-//    as its threshold bin holds exactly the count still needed.
-//  * Threshold bin search: every thread owns a run of bins, a warp-shuffle
-//    suffix scan plus one cross-warp pass finds the bin where the count from
-//    the top first reaches the target (cf. warp_inclusive_sum on the PR #36684
-//    page, "Key source snippets").
-//  * Compaction and slot allocation use ballot/popc with one shared-memory
-//    atomic per warp (cf. warp_sum_bool, same page).
+//    12, 8, 8 and 4 bits of the key from the top (the 12-bit first level is
+//    the one the PR #36684 page, "Feature and motivation", describes), then,
+//    only when equal scores straddle the threshold and TOPK_DETERMINISTIC is
+//    set, 8/8/8/8 bits of ~position, so the lowest positions win. A level
+//    stops the descent as soon as its threshold bin holds exactly the count
+//    still needed.
+//  * Threshold bin search: for the 4096-bin level every thread owns a run of
+//    bins and a warp-shuffle suffix sum plus one pass over the warp totals
+//    finds the bin where the count from the top first reaches the target
+//    (cf. warp_inclusive_sum on the PR #36684 page, "Key source snippets");
+//    the small levels use one warp.
 //  * Routes, chosen per row by length (the plan kernel orders rows longest
 //    first and hands long rows of small batches to the cluster path):
 //      trivial   L <= k: positions 0..L-1 then -1, scores never read;
-//      register  L <= 8192: the window lives in registers (16-byte loads),
-//                every level re-reads registers;
+//      register  L <= 8192: the window lives in registers (16-byte loads);
+//                levels 1 and 2 are histogrammed from the registers, the
+//                elements above the 20-bit threshold prefix are written
+//                straight to their slots and the few equal to it are ranked
+//                against each other (every remaining digit at once);
 //      streaming longer rows: one pass over HBM builds the level-1 histogram
 //                while collecting into shared memory every element whose top
 //                12 key bits clear a lower bound estimated from the first tile
@@ -36,15 +38,22 @@
 //                the estimate was too high, or the buffer overflowed, the row
 //                is re-read from global memory (always exact, only slower);
 //      cluster   for few long rows: the same streaming pass split over a
-//                thread-block cluster of 8 CTAs, histograms merged through
+//                thread-block cluster of 4 CTAs, histograms merged through
 //                distributed shared memory (reduce-scatter + all-gather) and
 //                output slots allocated with atomics on the leader CTA's
 //                shared memory (cf. TopKCluster on the PR #36684 page).
+//  * Compaction uses a warp scan and one shared-memory atomic per warp; the
+//    emit gives slots by a block-wide scan (cf. warp_sum_bool, same page).
+//  * PAGED rows copy their page-table entries into shared memory with
+//    cp.async while the scores load, so the emit's lookups stay on chip.
 //  * Unaligned window heads: 16-byte loads start at the aligned address below
 //    the window and the up-to-3 leading / trailing lanes are excluded by
 //    position. Scores are never written (the pages' kernel masks them in place).
-//  * No wait here spins: all waits are __syncthreads or hardware cluster
-//    barriers.
+//  * Every kernel is launched with programmatic dependent launch and waits
+//    (griddepcontrol.wait) before touching global memory, so it is scheduled
+//    while the previous kernel on the stream drains without breaking stream
+//    order. No wait here spins: all waits are __syncthreads, hardware cluster
+//    barriers or that grid dependency.
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -63,6 +72,7 @@ constexpr int kThreads = 512;                 // threads per CTA, all routes
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
 constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
+constexpr int kPageCache = 4096;              // page-table entries of a row held in shared memory
 constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
 constexpr int kClusterSize = 4;               // CTAs per long row on the cluster path
 constexpr int kPlanThreads = 1024;
@@ -94,20 +104,22 @@ size_t workspace_bytes_for(int32_t batch) {
 }
 
 // Shared memory carve-up (dynamic). hist/mhist are 4096 counters each, the
-// candidate buffer is (key, position) pairs, then small scratch.
+// candidate buffer is (key, position) pairs, then the row's page-table
+// entries (PAGED) and small scratch.
 struct Shared {
     uint32_t* hist;      // local histogram
     uint32_t* mhist;     // merged histogram (== hist on a single CTA)
     uint32_t* cand_key;
     int32_t* cand_pos;
-    uint32_t* red;       // kWarps words for scans
+    int32_t* pages;      // kPageCache page-table entries
+    uint32_t* red;       // 2 * kWarps words for scans
     uint32_t* res;       // threshold search results
     uint32_t* cnt;       // [0] candidates, [1] definite slots, [2] threshold-group slots
 };
 
-constexpr size_t kScratchWords = 64;
-constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kScratchWords) * 4;
-constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kScratchWords) * 4;
+constexpr size_t kScratchWords = 2 * kWarps + 32;  // red: 2 words per warp; res: 16; cnt: 16
+constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
 
 __device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
     Shared s;
@@ -124,9 +136,11 @@ __device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
     w += kCandCap;
     s.cand_pos = reinterpret_cast<int32_t*>(w);
     w += kCandCap;
+    s.pages = reinterpret_cast<int32_t*>(w);
+    w += kPageCache;
     s.red = w;
-    s.res = w + 32;
-    s.cnt = w + 48;
+    s.res = w + 2 * kWarps;
+    s.cnt = w + 2 * kWarps + 16;
     return s;
 }
 
@@ -216,16 +230,69 @@ __device__ __forceinline__ int level_bins(int lvl) { return lvl == 0 ? kBins : l
 // Finds the largest bin d of h[0..nb) with sum_{c >= d} h[c] >= target and
 // returns it with above = sum_{c > d} h[c] and count = h[d]; `found` is false
 // (with above = the total) when target exceeds the total. nb is 4096, 256 or
-// 16 (h 16-byte aligned). Warp 0 scans from the top in blocks of 256 bins
-// (lane l holds bins 8l..8l+7 of a block, a warp-shuffle suffix sum orders
-// them) and stops at the block holding the answer; the other warps wait at
-// the barrier. All threads call it; it synchronises once.
+// 16 (h 16-byte aligned); target >= 1. All threads call it.
+//  * nb = 4096 (find_threshold_wide): thread t holds bins Rt..Rt+R-1
+//    (R = 4096 / threads); a warp-shuffle suffix sum plus the warp totals in
+//    shared memory give
+//    every thread the count above its run, and the one thread whose run
+//    crosses the target resolves the bin. Two barriers.
+//  * nb <= 256: warp 0 holds the bins (lane l: 8l..8l+7), one warp-shuffle
+//    suffix sum; the other warps wait at the single barrier.
 struct Threshold {
     uint32_t bin, above, count;
     bool found;
 };
 
+__device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, const Shared& sh) {
+    constexpr int R = kBins / kThreads;  // bins per thread
+    static_assert(R % 4 == 0 && R * kThreads == kBins, "whole 16-byte runs of bins per thread");
+    const uint32_t lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    uint32_t b[R];
+#pragma unroll
+    for (int q = 0; q < R / 4; ++q) {
+        const uint4 u = reinterpret_cast<const uint4*>(h)[(R / 4) * threadIdx.x + q];
+        b[4 * q] = u.x, b[4 * q + 1] = u.y, b[4 * q + 2] = u.z, b[4 * q + 3] = u.w;
+    }
+    uint32_t s8 = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) s8 += b[i];
+    uint32_t x = s8;  // sum over the lanes >= this lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, x, off);
+        if (lane + off < 32) x += y;
+    }
+    if (lane == 0) sh.red[warp] = x;
+    __syncthreads();
+    uint32_t above = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t r = sh.red[w];
+        total += r;
+        above += w > warp ? r : 0u;
+    }
+    const uint32_t incl = above + x, excl = incl - s8;
+    if (excl < target && incl >= target) {
+        uint32_t r = excl;
+#pragma unroll
+        for (int i = R - 1; i >= 0; --i) {
+            if (r + b[i] >= target) {
+                sh.res[0] = R * threadIdx.x + static_cast<uint32_t>(i);
+                sh.res[1] = r;
+                sh.res[2] = b[i];
+                break;
+            }
+            r += b[i];
+        }
+    }
+    __syncthreads();
+    if (total < target) return Threshold{0u, total, 0u, false};
+    return Threshold{sh.res[0], sh.res[1], sh.res[2], true};
+}
+
 __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, const Shared& sh) {
+    if (nb == kBins) return find_threshold_wide(h, target, sh);
     if (threadIdx.x < 32) {
         const uint32_t lane = lane_id();
         uint32_t run = 0;  // count in the bins above the current block
@@ -453,16 +520,17 @@ __device__ __forceinline__ void apply_level(SelState& st, int lvl, const Thresho
     st.exact = (t.count == st.need);
 }
 
+// Levels first..last of the radix descent, stopping once exact.
 template <class Merge, class Src>
 __device__ void run_levels(SelState& st, int first, int last, const Src& src, const Shared& sh,
                            const Merge& mg) {
     for (int lvl = first; lvl <= last && !st.exact; ++lvl) {
         const int nb = level_bins(lvl);
         const int shift = level_shift(lvl);
-        clear_hist(sh.hist, nb);
-        __syncthreads();
         uint32_t* hist = sh.hist;
         const uint32_t digit = static_cast<uint32_t>(nb - 1);
+        clear_hist(sh.hist, nb);
+        __syncthreads();
         if (lvl < kKeyLevels) {  // key digits: a 32-bit filter on the resolved key bits
             const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32), msk = static_cast<uint32_t>(st.mask >> 32);
             const int sh32 = shift - 32;
@@ -488,6 +556,7 @@ struct Emitter {
     int32_t* out;
     int32_t* out_raw;
     const int32_t* pt_row;
+    const int32_t* pt_cached;  // the row's page-table entries in shared memory, or null
     int32_t page_bits;
     int32_t offset;
     uint32_t k;
@@ -499,13 +568,32 @@ struct Emitter {
         }
         int32_t v;
         if (kPaged) {
-            const int32_t page = __ldg(pt_row + (pos >> page_bits));
+            const int32_t page = pt_cached ? pt_cached[pos >> page_bits] : __ldg(pt_row + (pos >> page_bits));
             v = (page << page_bits) | (pos & ((1 << page_bits) - 1));
         } else {
             v = pos + offset;
         }
         out[slot] = v;
         if (out_raw) out_raw[slot] = pos;
+    }
+    // Straight-line form for unrolled loops: writes when `w` (and the slot is
+    // in range); every load it makes is in bounds whether or not it writes.
+    // The caller reports out-of-range slots (see flag_if).
+    __device__ __forceinline__ void write_if(bool w, uint32_t slot, int32_t pos) const {
+        const bool ok = w && slot < k;
+        int32_t v;
+        if (kPaged) {
+            const int32_t q = ok ? (pos >> page_bits) : 0;  // entry 0 exists: the row is not empty
+            const int32_t page = pt_cached ? pt_cached[q] : __ldg(pt_row + q);
+            v = (page << page_bits) | (pos & ((1 << page_bits) - 1));
+        } else {
+            v = pos + offset;
+        }
+        if (ok) out[slot] = v;
+        if (ok && out_raw) out_raw[slot] = pos;
+    }
+    __device__ __forceinline__ void flag_if(bool bad) const {
+        if (bad) atomicOr(flags, TOPK_DEVICE_FLAG_INTERNAL);
     }
 };
 
@@ -518,6 +606,9 @@ struct Emitter {
 template <bool kPaged, class Merge, class Src>
 __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, const Shared& sh,
                               const Merge& mg, const Emitter<kPaged>& em) {
+    // this thread's page-table copies have landed; the barrier after the
+    // counting pass publishes them to the CTA
+    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");
     const uint32_t need = st.need;
     const bool exact = st.exact;
     const bool key_only = static_cast<uint32_t>(st.mask) == 0;  // only key levels ran
@@ -648,9 +739,12 @@ __device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0
 }
 
 // Appends the tile elements flagged in `pass` to the candidate buffer: one
-// warp scan and one shared atomic per warp.
+// warp scan and one shared atomic per warp. With kCountLevel1 each appended
+// element is also counted in the level-1 histogram.
+constexpr int kCountNone = 0, kCountLevel1 = 1;
+template <int kCount = kCountNone>
 __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_t pass, int j0, int rem,
-                                             const Shared& sh, bool count_hist = false) {
+                                             const Shared& sh) {
     const uint32_t c = __popc(pass);
     const uint32_t incl = warp_inclusive_scan(c);
     const uint32_t total = __shfl_sync(kFull, incl, 31);
@@ -663,7 +757,7 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
     for (int e = 0; e < 4 * kTileVecs; ++e) {
         if ((pass >> e) & 1u) {
             const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
-            if (count_hist) atomicAdd(&sh.hist[kk >> 20], 1u);
+            if (kCount == kCountLevel1) atomicAdd(&sh.hist[kk >> 20], 1u);
             if (idx < static_cast<uint32_t>(kCandCap)) {
                 const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
                 sh.cand_key[idx] = kk;
@@ -674,11 +768,64 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
     }
 }
 
+// Ranks the threshold bin's elements, held in the candidate buffer
+// (n <= kThreads of them): the rank of an element is the number of bin
+// members whose composite (key, ~position) is larger, and the ones ranked
+// below `need` take slots k - need + rank. This settles every remaining key
+// and position digit at once (ties go to the lowest position). The buffer is
+// padded to a multiple of 4 with entries that rank below everything; each
+// element is compared by kThreads / m threads (m = n rounded up to a power of
+// two), each over one segment of the buffer, and the partial ranks meet in
+// shared-memory counters (the level-1 histogram's bins, no longer needed).
+template <bool kPaged>
+__device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, const Shared& sh,
+                                   const Emitter<kPaged>& em) {
+    uint32_t* rank = sh.hist;
+    const uint32_t n4 = (n + 3u) & ~3u;
+    if (threadIdx.x < n4 - n) {
+        sh.cand_key[n + threadIdx.x] = 0u;
+        sh.cand_pos[n + threadIdx.x] = INT32_MAX;
+    }
+    if (threadIdx.x < n) rank[threadIdx.x] = 0u;
+    __syncthreads();
+    uint32_t m = 32;
+    while (m < n) m <<= 1;
+    const uint32_t segs = static_cast<uint32_t>(kThreads) / m;
+    const uint32_t i = threadIdx.x & (m - 1u), seg = threadIdx.x / m;
+    const uint32_t per = (n4 / 4u + segs - 1u) / segs * 4u;
+    const uint32_t j0 = seg * per, j1 = min(n4, j0 + per);
+    if (i < n && j0 < j1) {
+        const uint32_t ki = sh.cand_key[i];
+        const int32_t pi = sh.cand_pos[i];
+        uint32_t r = 0;
+        for (uint32_t j = j0; j < j1; j += 4) {
+            const uint4 kj = *reinterpret_cast<const uint4*>(sh.cand_key + j);
+            const int4 pj = *reinterpret_cast<const int4*>(sh.cand_pos + j);
+            r += static_cast<uint32_t>(kj.x > ki || (kj.x == ki && pj.x < pi));
+            r += static_cast<uint32_t>(kj.y > ki || (kj.y == ki && pj.y < pi));
+            r += static_cast<uint32_t>(kj.z > ki || (kj.z == ki && pj.z < pi));
+            r += static_cast<uint32_t>(kj.w > ki || (kj.w == ki && pj.w < pi));
+        }
+        atomicAdd(&rank[i], r);
+    }
+    __syncthreads();
+    if (seg == 0 && i < n) {
+        const uint32_t r = rank[i];
+        if (r < need) em.write(k - need + r, sh.cand_pos[i]);
+    }
+}
+
 // Register route: the whole aligned window (nv <= kTileVecs * kThreads
-// vectors) is one register tile. Level 1 is a full histogram; every element
-// at or above its threshold bin is then compacted into the candidate buffer,
-// and the later levels and the emit loop over that buffer (a fallback keeps
-// them on the registers when the threshold bin is too full to copy).
+// vectors) is one register tile, and level 1 is a full histogram of it.
+// Unless level 1 is exact, level 2 (the next 8 key bits) is histogrammed
+// from the registers over the level-1 threshold bin.
+//  * Level-2 threshold bin of at most kThreads elements (the usual case): one
+//    more look at the tile writes every element above the 20-bit threshold
+//    prefix straight to its output slot and copies the elements equal to it
+//    to the candidate buffer (one block scan of both counts orders the
+//    slots), where rank_threshold_bin finishes the row.
+//  * Otherwise (many equal scores) the radix levels continue on the candidate
+//    buffer, or on the registers when the bins do not fit it.
 template <bool kPaged>
 __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
                              const Shared& sh, const Emitter<kPaged>& em) {
@@ -696,11 +843,77 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
     SelState st{0ull, 0ull, k, false};
     apply_level(st, 0, t1);
     const int last = (det ? kAllLevels : kKeyLevels) - 1;
+    // Level 2 inside the threshold bin, histogrammed from the registers (the
+    // level-1 bins have been read: their storage is free).
+    int shift = 20;           // the selection prefix is key >> shift ...
+    uint32_t tau = t1.bin;    // ... compared with tau
+    uint32_t n_tie = 0;
+    if (!st.exact) {
+        clear_hist(sh.hist, level_bins(1));
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4 * kTileVecs; ++e) {
+            const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
+            if (((valid >> e) & 1u) && (kk >> 20) == t1.bin) atomicAdd(&sh.hist[(kk >> 12) & 0xFFu], 1u);
+        }
+        __syncthreads();
+        const Threshold t2 = find_threshold(sh.hist, level_bins(1), st.need, sh);
+        apply_level(st, 1, t2);
+        shift = 12;
+        tau = (t1.bin << 8) | t2.bin;
+        n_tie = t2.count;
+    }
+    if (st.exact || n_tie <= static_cast<uint32_t>(kThreads)) {
+        if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
+        const bool exact = st.exact;
+        uint32_t def = 0, tie = 0;
+#pragma unroll
+        for (int e = 0; e < 4 * kTileVecs; ++e) {
+            const uint32_t pf = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> shift;
+            def |= static_cast<uint32_t>(exact ? pf >= tau : pf > tau) << e;
+            tie |= static_cast<uint32_t>(pf == tau) << e;
+        }
+        def &= valid;
+        tie = exact ? 0u : (tie & valid);
+        // both counts in one scan: selected in the low half, ties in the high
+        // half (a CTA holds at most 8192 elements)
+        const uint32_t c = static_cast<uint32_t>(__popc(def)) | (static_cast<uint32_t>(__popc(tie)) << 16);
+        const uint32_t incl = warp_inclusive_scan(c);
+        const int warp = static_cast<int>(threadIdx.x >> 5);
+        if (lane_id() == 31) sh.red[warp] = incl;
+        __syncthreads();
+        uint32_t base = incl - c;
+        for (int w = 0; w < warp; ++w) base += sh.red[w];
+        uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
+#pragma unroll
+        for (int e = 0; e < 4 * kTileVecs; ++e) {
+            const int32_t pos = 4 * ((e / 4) * kThreads + static_cast<int>(threadIdx.x)) - rem + (e % 4);
+            const bool w = (def >> e) & 1u;
+            const bool t = (tie >> e) & 1u;
+            em.write_if(w, slot, pos);
+            if (t) {
+                sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
+                sh.cand_pos[tslot] = pos;
+            }
+            slot += w;
+            tslot += t;
+        }
+        em.flag_if(slot > k - (exact ? 0u : st.need));
+        if (!exact) {
+            __syncthreads();
+            rank_threshold_bin<kPaged>(n_tie, st.need, k, sh, em);
+        }
+        return;
+    }
+    // A threshold bin too full to rank (many equal scores): the radix levels
+    // continue from level 3 on the candidate buffer, or on the registers when
+    // the bins at or above the level-1 threshold do not fit it.
     if (t1.above + t1.count <= static_cast<uint32_t>(kCandCap)) {
+        __syncthreads();
         collect_bits(v, tile_pass(v, 0, nv, rem, len, t1.bin << 20), 0, rem, sh);
         __syncthreads();
         const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
-        run_levels(st, 1, last, src, sh, mg);
+        run_levels(st, 2, last, src, sh, mg);
         emit_selected<kPaged>(st, k, src, sh, mg, em);
     } else {
         float4 f[kTileVecs];
@@ -709,7 +922,7 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
             f[u] = make_float4(__int_as_float(v[u].x), __int_as_float(v[u].y), __int_as_float(v[u].z),
                                __int_as_float(v[u].w));
         const RegSource<kTileVecs> src{f, rem, len};
-        run_levels(st, 1, last, src, sh, mg);
+        run_levels(st, 2, last, src, sh, mg);
         emit_selected<kPaged>(st, k, src, sh, mg, em);
     }
 }
@@ -763,7 +976,7 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
 #pragma unroll
         for (int u = 0; u < kTileVecs; ++u) cur[u] = nxt[u];
         if (j0 + T < je) load_bits(nxt, vbase, j0 + T, je);  // prefetch
-        collect_bits(cur, tile_pass(cur, j0, je, rem, len, bound_key), j0, rem, sh, true);
+        collect_bits<kCountLevel1>(cur, tile_pass(cur, j0, je, rem, len, bound_key), j0, rem, sh);
     }
     __syncthreads();
     const bool overflow = sh.cnt[0] > static_cast<uint32_t>(kCandCap);
@@ -814,22 +1027,49 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
 // kernels
 // ----------------------------------------------------------------------------
 
+// Programmatic dependent launch. Every kernel here is launched so that it may
+// be scheduled while the previous kernel on the stream is still running, and
+// reads or writes no global memory before grid_dependency_wait(), which
+// returns once the previous kernels have completed and their writes are
+// visible: stream order is kept, only the launch latency is hidden.
+// allow_dependents() lets the next kernel on the stream be scheduled early
+// under the same rule (a kernel launched without the attribute is unaffected).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool plan_matches(const Params& p) {
     const PlanHeader* h = p.hdr;
     return h->magic == kPlanMagic && h->batch == p.batch && h->k == p.k;
 }
 
 template <bool kPaged>
-__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b) {
+__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, int32_t offset) {
     Emitter<kPaged> em;
     em.out = p.out + static_cast<int64_t>(b) * p.k;
     em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
     em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(b) * p.page_table_stride : nullptr;
+    em.pt_cached = nullptr;
     em.page_bits = p.page_bits;
-    em.offset = kPaged ? 0 : p.out_offsets[b];
+    em.offset = offset;
     em.k = static_cast<uint32_t>(p.k);
     em.flags = &p.hdr->flags;
     return em;
+}
+
+// PAGED, non-trivial row: starts asynchronous copies of the row's page-table
+// entries 0..ceil(len / page_size)-1 (each one a page some window position
+// maps to) into shared memory when they fit; emit_selected waits for them.
+template <bool kPaged>
+__device__ __forceinline__ void prefetch_pages(Emitter<kPaged>& em, int32_t len, const Shared& sh) {
+    if (!kPaged) return;
+    const int n = ((len - 1) >> em.page_bits) + 1;
+    if (n > kPageCache) return;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sh.pages + i));
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(em.pt_row + i) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    em.pt_cached = sh.pages;
 }
 
 // One CTA per row; rows come from the plan's order (longest first), rows the
@@ -838,28 +1078,45 @@ template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const Shared sh = carve(smem, false);
+    grid_dependency_wait();
+    allow_dependents();
+    // The header, this CTA's order entry and the row data of row blockIdx.x
+    // are read together: when the plan kept rows in place (a batch in one
+    // length band) the row is blockIdx.x and no second round trip is needed.
+    // (blockIdx.x < batch, so every read is in bounds.)
+    const int b0 = static_cast<int>(blockIdx.x);
+    const PlanHeader* hdr = p.hdr;
+    const uint32_t magic = hdr->magic;
+    const int32_t h_batch = hdr->batch, h_k = hdr->k, n_order = hdr->n_order;
+    const int32_t ord = p.order[b0];
+    const int32_t len0 = p.seq_lens[b0];
+    const int32_t start0 = p.row_starts ? p.row_starts[b0] : 0;
+    const int32_t off0 = kPaged ? 0 : p.out_offsets[b0];
+    const bool planned = magic == kPlanMagic && h_batch == p.batch && h_k == p.k;
     if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
-    const bool planned = plan_matches(p);
-    int b = static_cast<int>(blockIdx.x);
+    int b = b0;
     if (planned) {
-        if (b >= p.hdr->n_order) return;
-        b = p.order[b];
+        if (b0 >= n_order) return;
+        b = ord;
     } else if (blockIdx.x == 0 && threadIdx.x == 0) {
         atomicOr(&p.hdr->flags, TOPK_DEVICE_FLAG_PLAN_MISMATCH);
     }
-    int32_t len = p.seq_lens[b];
-    const int32_t start = p.row_starts ? p.row_starts[b] : 0;
+    const bool same = b == b0;
+    int32_t len = same ? len0 : p.seq_lens[b];
+    const int32_t start = same ? start0 : (p.row_starts ? p.row_starts[b] : 0);
+    const int32_t offset = kPaged ? 0 : (same ? off0 : p.out_offsets[b]);
     if (len < 0 || start < 0) {
         // seq_len < 0 was counted by the plan; count the rest here
         if (threadIdx.x == 0 && (!planned || len >= 0)) atomicAdd(&p.hdr->error_rows, 1u);
         len = 0;
     }
     const uint32_t k = static_cast<uint32_t>(p.k);
-    const Emitter<kPaged> em = make_emitter<kPaged>(p, b);
+    Emitter<kPaged> em = make_emitter<kPaged>(p, b, offset);
     if (len <= p.k) {
         trivial_row<kPaged>(len, k, em);
         return;
     }
+    prefetch_pages<kPaged>(em, len, sh);
     if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
     const int rem = start & 3;
     const float4* vbase = reinterpret_cast<const float4*>(
@@ -881,6 +1138,8 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
     topk_cluster_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const Shared sh = carve(smem, true);
+    grid_dependency_wait();
+    allow_dependents();
     if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
     if (!plan_matches(p)) return;  // uniform over the cluster: no barrier is skipped
     cg::cluster_group cluster = cg::this_cluster();
@@ -899,12 +1158,13 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
             if (rank == 0 && threadIdx.x == 0 && start < 0) atomicAdd(&p.hdr->error_rows, 1u);
             len = 0;
         }
-        const Emitter<kPaged> em = make_emitter<kPaged>(p, b);
+        Emitter<kPaged> em = make_emitter<kPaged>(p, b, kPaged ? 0 : p.out_offsets[b]);
         if (len <= p.k) {
             if (rank == 0) trivial_row<kPaged>(len, k, em);
             cluster.sync();
             continue;
         }
+        prefetch_pages<kPaged>(em, len, sh);
         if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
         clear_hist(sh.hist, kBins);
         const int rem = start & 3;
@@ -923,7 +1183,9 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
 }
 
 // Plan: bands rows by length (longest first), lists rows for the cluster path,
-// counts seq_len < 0.
+// counts seq_len < 0. A batch whose rows all fall in one band keeps its order
+// (order[i] = i), which lets the rows kernel read its row's data without
+// waiting for the order entry.
 __device__ __forceinline__ int band_of(int32_t len, int32_t k, bool allow_cluster) {
     if (len <= k) return kBandTrivial;
     if (allow_cluster && len > kClusterFloor) return kBandCluster;
@@ -936,6 +1198,9 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
     __shared__ uint32_t count[kBands];
     __shared__ uint32_t offset[kBands];
     __shared__ uint32_t n_err;
+    __shared__ bool in_place;
+    grid_dependency_wait();
+    allow_dependents();
     const int tid = static_cast<int>(threadIdx.x);
     if (tid < kBands) count[tid] = 0;
     if (tid == 0) n_err = 0;
@@ -961,6 +1226,9 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
             run += count[bnd];
         }
         offset[kBandCluster] = 0;
+        // one band holds every row: the rows keep their own order
+        in_place = false;
+        for (int bnd = 0; bnd <= kBandTrivial; ++bnd) in_place |= count[bnd] == static_cast<uint32_t>(batch);
         hdr->n_order = static_cast<int32_t>(run);
         hdr->n_cluster = static_cast<int32_t>(count[kBandCluster]);
         hdr->error_rows = n_err;
@@ -970,6 +1238,10 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
         hdr->magic = kPlanMagic;
     }
     __syncthreads();
+    if (in_place) {
+        for (int i = tid; i < batch; i += kPlanThreads) order[i] = i;
+        return;
+    }
     for (int it = 0; it < n_iter; ++it) {
         const int i = it * kPlanThreads + tid;
         const bool valid = i < batch;
@@ -1054,21 +1326,35 @@ cudaError_t device_state(DeviceState** out) {
 
 bool valid_k(int32_t k) { return k >= 1 && k <= TOPK_MAX_K; }
 
+// Launches with the programmatic-stream-serialization attribute (see
+// grid_dependency_wait); a cluster kernel's shape comes from __cluster_dims__.
+template <class... Args, class... Vals>
+cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem, cudaStream_t stream,
+                       Vals... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <bool kPaged>
 int launch_transform(const Params& prm, cudaStream_t stream) {
     DeviceState* ds = nullptr;
     if (device_state(&ds) != cudaSuccess) return TOPK_ERR_CUDA;
-    topk_rows_kernel<kPaged><<<prm.batch, kThreads, kSmemRows, stream>>>(prm);
-    if (cudaPeekAtLastError() != cudaSuccess) return TOPK_ERR_CUDA;
+    if (launch_pdl(topk_rows_kernel<kPaged>, prm.batch, kThreads, kSmemRows, stream, prm) != cudaSuccess)
+        return TOPK_ERR_CUDA;
     if (prm.batch <= kClusterMaxBatch) {
         const int slots = min(prm.batch, ds->max_clusters);
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kClusterSize * slots, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemCluster;
-        cfg.stream = stream;
-        // the compile-time __cluster_dims__ fixes the cluster shape
-        if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel<kPaged>, prm) != cudaSuccess) return TOPK_ERR_CUDA;
+        if (launch_pdl(topk_cluster_kernel<kPaged>, kClusterSize * slots, kThreads, kSmemCluster, stream, prm) !=
+            cudaSuccess)
+            return TOPK_ERR_CUDA;
     }
     return TOPK_OK;
 }
@@ -1115,9 +1401,9 @@ int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace
     if (workspace == nullptr || workspace_bytes < workspace_bytes_for(batch)) return TOPK_ERR_WORKSPACE;
     PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + sizeof(PlanHeader));
-    topk_plan_kernel<<<1, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        seq_lens, batch, k, hdr, order, order + batch);
-    return cudaPeekAtLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+    const cudaError_t e = launch_pdl(topk_plan_kernel, 1, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream),
+                                     seq_lens, batch, k, hdr, order, order + batch);
+    return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }
 
 int topk_transform_paged(const float* scores, int64_t score_stride, const int32_t* row_starts,

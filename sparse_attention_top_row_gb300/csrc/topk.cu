@@ -706,41 +706,63 @@ __device__ __forceinline__ int tile_elem(const int4 (&v)[kTileVecs], int e) {
     return (e % 4) == 0 ? q.x : (e % 4) == 1 ? q.y : (e % 4) == 2 ? q.z : q.w;
 }
 
-// Bit e set: element e of this thread's tile at vector j0 lies in the window.
+// Bit e set: element e of this thread's tile at vector j0 lies in the window
+// (vector u of the tile holds positions 4j - rem .. 4j - rem + 3 for
+// j = j0 + u * kThreads + tid; vectors at or past je are not in it).
 __device__ __forceinline__ uint32_t tile_valid(int j0, int je, int rem, int len) {
     uint32_t m = 0;
 #pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e) {
-        const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
-        if (j < je && static_cast<unsigned>(4 * j - rem + (e % 4)) < static_cast<unsigned>(len)) m |= 1u << e;
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        const int lo = 4 * j - rem;
+        const int a = max(-lo, 0), b = min(len - lo, 4);  // lanes [a, b) are in the window
+        const uint32_t vm = (j < je && a < b) ? (1u << b) - (1u << a) : 0u;
+        m |= vm << (4 * u);
     }
     return m;
 }
 
-// Bit mask of the tile's in-window elements whose key is at least bound_key.
-// For an interior tile and a non-negative bound (the usual case) the test is
-// one signed compare of the raw bits: key >= bound_key <=> bits >= bound_key ^ 2^31.
+// Bit mask of the tile's in-window elements whose key is at least bound_key,
+// by one compare of the raw bits per element: for bound_key >= 2^31 (a
+// non-negative bound) key >= bound_key <=> bits >= bound_key ^ 2^31 as signed
+// integers; below it, key >= bound_key <=> bits <= ~bound_key as unsigned
+// ones. Only a tile that reaches past either end of the window is masked.
 __device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0, int je, int rem, int len,
                                               uint32_t bound_key) {
-    const bool interior =
-        4 * j0 - rem >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
     uint32_t pass = 0;
-    if (interior && bound_key >= 0x80000000u) {
+    if (bound_key >= 0x80000000u) {
         const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
 #pragma unroll
         for (int e = 0; e < 4 * kTileVecs; ++e) pass |= static_cast<uint32_t>(tile_elem(v, e) >= bb) << e;
-        return pass;
-    }
-    const uint32_t valid = tile_valid(j0, je, rem, len);
+    } else {
+        const uint32_t ub = ~bound_key;
 #pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e)
-        pass |= static_cast<uint32_t>(bits_key(static_cast<uint32_t>(tile_elem(v, e))) >= bound_key) << e;
-    return pass & valid;
+        for (int e = 0; e < 4 * kTileVecs; ++e)
+            pass |= static_cast<uint32_t>(static_cast<uint32_t>(tile_elem(v, e)) <= ub) << e;
+    }
+    const bool interior =
+        4 * j0 - rem >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
+    return interior ? pass : pass & tile_valid(j0, je, rem, len);
+}
+
+// Element e of the tile with e known only at run time: a select tree over the
+// registers (no local-memory copy of the tile).
+__device__ __forceinline__ int tile_elem_at(const int4 (&v)[kTileVecs], int e) {
+    static_assert(kTileVecs == 4, "select tree for four vectors");
+    const int c = e & 3;
+    const bool hi = (e & 8) != 0, odd = (e & 4) != 0;
+    const int4 a = hi ? v[2] : v[0], b = hi ? v[3] : v[1];
+    const int4 q = odd ? b : a;
+    const int lo2 = (c & 1) ? q.y : q.x, hi2 = (c & 1) ? q.w : q.z;
+    return (c & 2) ? hi2 : lo2;
 }
 
 // Appends the tile elements flagged in `pass` to the candidate buffer: one
-// warp scan and one shared atomic per warp. With kCountLevel1 each appended
-// element is also counted in the level-1 histogram.
+// warp scan and one shared atomic per warp reserve the slots, then each
+// thread walks the set bits of its own mask (so a warp's loop runs as many
+// times as its busiest lane has candidates, not once per tile element). With
+// kCountLevel1 each appended element is also counted in the level-1
+// histogram.
 constexpr int kCountNone = 0, kCountLevel1 = 1;
 template <int kCount = kCountNone>
 __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_t pass, int j0, int rem,
@@ -753,18 +775,16 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
     if (lane_id() == 31) base = atomicAdd(&sh.cnt[0], total);
     base = __shfl_sync(kFull, base, 31);
     uint32_t idx = base + incl - c;
-#pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e) {
-        if ((pass >> e) & 1u) {
-            const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
-            if (kCount == kCountLevel1) atomicAdd(&sh.hist[kk >> 20], 1u);
-            if (idx < static_cast<uint32_t>(kCandCap)) {
-                const int j = j0 + (e / 4) * kThreads + static_cast<int>(threadIdx.x);
-                sh.cand_key[idx] = kk;
-                sh.cand_pos[idx] = 4 * j - rem + (e % 4);
-            }
-            ++idx;
+    const int p0 = 4 * (j0 + static_cast<int>(threadIdx.x)) - rem;  // element 0's position
+    for (uint32_t rest = pass; rest != 0; rest &= rest - 1u) {
+        const int e = __ffs(static_cast<int>(rest)) - 1;
+        const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem_at(v, e)));
+        if (kCount == kCountLevel1) atomicAdd(&sh.hist[kk >> 20], 1u);
+        if (idx < static_cast<uint32_t>(kCandCap)) {
+            sh.cand_key[idx] = kk;
+            sh.cand_pos[idx] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
         }
+        ++idx;
     }
 }
 
@@ -972,11 +992,15 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
     }
     const uint32_t bound_key = bound_bin << 20;
     collect_bits(cur, tile_pass(cur, jb, je, rem, len, bound_key), jb, rem, sh);
-    for (int j0 = jb + T; j0 < je; j0 += T) {
-#pragma unroll
-        for (int u = 0; u < kTileVecs; ++u) cur[u] = nxt[u];
-        if (j0 + T < je) load_bits(nxt, vbase, j0 + T, je);  // prefetch
+    // two register tiles in turn: one is collected while the next loads
+    for (int j0 = jb + T; j0 < je;) {
+        if (j0 + T < je) load_bits(cur, vbase, j0 + T, je);
+        collect_bits<kCountLevel1>(nxt, tile_pass(nxt, j0, je, rem, len, bound_key), j0, rem, sh);
+        j0 += T;
+        if (j0 >= je) break;
+        if (j0 + T < je) load_bits(nxt, vbase, j0 + T, je);
         collect_bits<kCountLevel1>(cur, tile_pass(cur, j0, je, rem, len, bound_key), j0, rem, sh);
+        j0 += T;
     }
     __syncthreads();
     const bool overflow = sh.cnt[0] > static_cast<uint32_t>(kCandCap);

@@ -138,6 +138,8 @@ def _rows(rng, lens, kind="normal"):
             e = (code % 1600) // 8 - 100
             m = code % 8
             rows.append((sign * np.ldexp(1.0 + m / 8.0, e)).astype(np.float32).tolist())
+        elif kind == "negative":  # every score below zero: negative thresholds and bounds
+            rows.append((-1.0 - np.abs(rng.standard_normal(L))).astype(np.float32).tolist())
         elif kind == "bf16":  # N(0, 0.01) rounded to bf16: long runs of equal keys at the threshold
             v = (rng.standard_normal(L) * 0.1).astype(np.float32)
             rows.append((v.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).tolist())
@@ -163,15 +165,17 @@ def test_boundary_lengths(cuda_lib, k, mode):
     check_full(cuda_lib, w)
 
 
-@pytest.mark.parametrize("kind", ["ties", "equal", "ascending", "descending", "special", "spread", "bf16"])
+@pytest.mark.parametrize("kind", ["ties", "equal", "ascending", "descending", "special", "spread", "bf16",
+                                  "negative"])
 @pytest.mark.parametrize("L", [3000, 8000, 12000, 50000])
 def test_adversarial_values(cuda_lib, kind, L):
     """Heavy ties, one value everywhere, sorted rows (the first-tile estimate is
     then wrong or the candidate buffer overflows: the exact fallbacks run),
     infinities, signed zeros and the largest finite values; one value per
     level-1 bin (level 1 is exact); bf16-rounded values (equal keys beyond
-    the second level). L = 8000 puts a one-value row on the register route's
-    fallback that keeps the levels in registers."""
+    the second level); all-negative rows (negative thresholds and bounds).
+    L = 8000 puts a one-value row on the register route's fallback that
+    keeps the levels in registers."""
     rng = np.random.default_rng(L)
     w = wl.custom("ragged", 2048, _rows(rng, [L, L // 2 + 1], kind), row_starts=[1, 2],
                   out_offsets=[0, 5])

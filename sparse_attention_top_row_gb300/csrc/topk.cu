@@ -788,23 +788,22 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
     }
 }
 
-// Ranks the threshold bin's elements, held in the candidate buffer
-// (n <= kThreads of them): the rank of an element is the number of bin
-// members whose composite (key, ~position) is larger, and the ones ranked
-// below `need` take slots k - need + rank. This settles every remaining key
-// and position digit at once (ties go to the lowest position). The buffer is
-// padded to a multiple of 4 with entries that rank below everything; each
-// element is compared by kThreads / m threads (m = n rounded up to a power of
-// two), each over one segment of the buffer, and the partial ranks meet in
-// shared-memory counters (the level-1 histogram's bins, no longer needed).
+// Ranks the threshold bin's elements, n <= kThreads of them in tkey/tpos
+// (16-byte aligned, room for n rounded up to 4): the rank of an element is
+// the number of bin members whose composite (key, ~position) is larger, and
+// the ones ranked below `need` take slots k - need + rank. This settles every
+// remaining key and position digit at once (ties go to the lowest position).
+// The arrays are padded to a multiple of 4 with entries that rank below
+// everything; each element is compared by kThreads / m threads (m = n
+// rounded up to a power of two), each over one segment, and the partial
+// ranks meet in the shared-memory counters `rank` (n words).
 template <bool kPaged>
-__device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, const Shared& sh,
-                                   const Emitter<kPaged>& em) {
-    uint32_t* rank = sh.hist;
+__device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32_t* tkey, int32_t* tpos,
+                                   uint32_t* rank, const Emitter<kPaged>& em) {
     const uint32_t n4 = (n + 3u) & ~3u;
     if (threadIdx.x < n4 - n) {
-        sh.cand_key[n + threadIdx.x] = 0u;
-        sh.cand_pos[n + threadIdx.x] = INT32_MAX;
+        tkey[n + threadIdx.x] = 0u;
+        tpos[n + threadIdx.x] = INT32_MAX;
     }
     if (threadIdx.x < n) rank[threadIdx.x] = 0u;
     __syncthreads();
@@ -815,12 +814,12 @@ __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, const 
     const uint32_t per = (n4 / 4u + segs - 1u) / segs * 4u;
     const uint32_t j0 = seg * per, j1 = min(n4, j0 + per);
     if (i < n && j0 < j1) {
-        const uint32_t ki = sh.cand_key[i];
-        const int32_t pi = sh.cand_pos[i];
+        const uint32_t ki = tkey[i];
+        const int32_t pi = tpos[i];
         uint32_t r = 0;
         for (uint32_t j = j0; j < j1; j += 4) {
-            const uint4 kj = *reinterpret_cast<const uint4*>(sh.cand_key + j);
-            const int4 pj = *reinterpret_cast<const int4*>(sh.cand_pos + j);
+            const uint4 kj = *reinterpret_cast<const uint4*>(tkey + j);
+            const int4 pj = *reinterpret_cast<const int4*>(tpos + j);
             r += static_cast<uint32_t>(kj.x > ki || (kj.x == ki && pj.x < pi));
             r += static_cast<uint32_t>(kj.y > ki || (kj.y == ki && pj.y < pi));
             r += static_cast<uint32_t>(kj.z > ki || (kj.z == ki && pj.z < pi));
@@ -831,8 +830,76 @@ __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, const 
     __syncthreads();
     if (seg == 0 && i < n) {
         const uint32_t r = rank[i];
-        if (r < need) em.write(k - need + r, sh.cand_pos[i]);
+        if (r < need) em.write(k - need + r, tpos[i]);
     }
+}
+
+// The finish shared by the solo routes once level 1 is known and every
+// element at or above its threshold bin sits in the candidate buffer (n of
+// them): level 2 is histogrammed over the threshold bin's candidates (unless
+// level 1 is exact); then one counting pass and one writing pass over the
+// buffer send every element above the threshold prefix to its slot (a block
+// scan orders them) and copy the elements equal to it to a tie list (in the
+// histogram's storage), which rank_threshold_bin finishes. Returns false,
+// having written nothing, when the level-2 threshold bin is too full to rank
+// (many equal scores): the caller continues with the radix levels from
+// level 3 (st then holds levels 1 and 2).
+template <bool kPaged>
+__device__ bool finish_candidates(SelState& st, uint32_t bin1, uint32_t n, uint32_t k, const Shared& sh,
+                                  const Emitter<kPaged>& em) {
+    int shift = 20;
+    uint32_t tau = bin1, n_tie = 0;
+    if (!st.exact) {
+        clear_hist(sh.hist, level_bins(1));
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+            const uint32_t kk = sh.cand_key[i];
+            if ((kk >> 20) == bin1) atomicAdd(&sh.hist[(kk >> 12) & 0xFFu], 1u);
+        }
+        __syncthreads();
+        const Threshold t2 = find_threshold(sh.hist, level_bins(1), st.need, sh);
+        apply_level(st, 1, t2);
+        shift = 12;
+        tau = (bin1 << 8) | t2.bin;
+        n_tie = t2.count;
+        if (!st.exact && n_tie > static_cast<uint32_t>(kThreads)) return false;
+    }
+    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
+    const bool exact = st.exact;
+    uint32_t c = 0;  // selected in the low half, ties in the high half (n <= kCandCap < 2^16)
+    for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t pf = sh.cand_key[i] >> shift;
+        c += (exact ? pf >= tau : pf > tau) ? 1u : (!exact && pf == tau) ? 0x10000u : 0u;
+    }
+    const uint32_t incl = warp_inclusive_scan(c);
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    if (lane_id() == 31) sh.red[warp] = incl;
+    __syncthreads();
+    uint32_t base = incl - c;
+    for (int w = 0; w < warp; ++w) base += sh.red[w];
+    uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
+    uint32_t* tkey = sh.hist;                                  // tie list: kThreads + 4 entries each
+    int32_t* tpos = reinterpret_cast<int32_t*>(sh.hist + 2 * kThreads);
+    for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t kk = sh.cand_key[i];
+        const uint32_t pf = kk >> shift;
+        const bool w = exact ? pf >= tau : pf > tau;
+        const bool t = !exact && pf == tau;
+        const int32_t pos = sh.cand_pos[i];
+        em.write_if(w, slot, pos);
+        if (t) {
+            tkey[tslot] = kk;
+            tpos[tslot] = pos;
+        }
+        slot += w;
+        tslot += t;
+    }
+    em.flag_if(slot > k - (exact ? 0u : st.need));
+    if (!exact) {
+        __syncthreads();
+        rank_threshold_bin<kPaged>(n_tie, st.need, k, tkey, tpos, sh.cand_key, em);
+    }
+    return true;
 }
 
 // Register route: the whole aligned window (nv <= kTileVecs * kThreads
@@ -921,7 +988,7 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
         em.flag_if(slot > k - (exact ? 0u : st.need));
         if (!exact) {
             __syncthreads();
-            rank_threshold_bin<kPaged>(n_tie, st.need, k, sh, em);
+            rank_threshold_bin<kPaged>(n_tie, st.need, k, sh.cand_key, sh.cand_pos, sh.hist, em);
         }
         return;
     }
@@ -1038,7 +1105,12 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
     const int last = (det ? kAllLevels : kKeyLevels) - 1;
     if (cands_ok) {
         const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
-        run_levels(st, 1, last, src, sh, mg);
+        int first = 1;
+        if (Merge::kSolo) {
+            if (finish_candidates<kPaged>(st, t1.bin, src.n, k, sh, em)) return;
+            first = 2;
+        }
+        run_levels(st, first, last, src, sh, mg);
         emit_selected<kPaged>(st, k, src, sh, mg, em);
     } else {
         const GlobalSource src{vbase, jb, je, rem, len};

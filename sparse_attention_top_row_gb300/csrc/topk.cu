@@ -34,14 +34,19 @@
 //      streaming longer rows: one pass over HBM builds the level-1 histogram
 //                while collecting into shared memory every element whose top
 //                12 key bits clear a lower bound estimated from the first tile
-//                of the row; the later levels run on that candidate buffer. If
-//                the estimate was too high, or the buffer overflowed, the row
-//                is re-read from global memory (always exact, only slower);
+//                of the row; level 2 and the emit then run on that candidate
+//                buffer, and the few elements equal to the 20-bit threshold
+//                prefix are ranked. If the estimate was too high, or the
+//                buffer overflowed, the row is re-read from global memory
+//                (always exact, only slower);
 //      cluster   for few long rows: the same streaming pass split over a
-//                thread-block cluster of 4 CTAs, histograms merged through
+//                thread-block cluster of 4 CTAs (each slice bounds itself
+//                from its own head tile), histograms merged through
 //                distributed shared memory (reduce-scatter + all-gather) and
 //                output slots allocated with atomics on the leader CTA's
-//                shared memory (cf. TopKCluster on the PR #36684 page).
+//                shared memory (cf. TopKCluster on the PR #36684 page). A key
+//                level whose group has no bit set below its digit (scores
+//                rounded to bf16 or coarser) ends the key descent early.
 //  * Compaction uses a warp scan and one shared-memory atomic per warp; the
 //    emit gives slots by a block-wide scan (cf. warp_sum_bool, same page).
 //  * PAGED rows copy their page-table entries into shared memory with
@@ -71,10 +76,12 @@ namespace {
 constexpr int kThreads = 512;                 // threads per CTA, all routes
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
+constexpr int kHistExtra = 8;                 // words after the bins, merged (summed) with them
 constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
 constexpr int kPageCache = 4096;              // page-table entries of a row held in shared memory
 constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
 constexpr int kClusterSize = 4;               // CTAs per long row on the cluster path
+static_assert(kHistExtra == 2 * kClusterSize, "a bound word and an overflow word per part");
 constexpr int kPlanThreads = 1024;
 constexpr int32_t kClusterFloor = 32768;      // rows longer than this may use the cluster path
 constexpr int32_t kClusterMaxBatch = 64;      // ... when the batch is at most this
@@ -118,17 +125,17 @@ struct Shared {
 };
 
 constexpr size_t kScratchWords = 2 * kWarps + 32;  // red: 2 words per warp; res: 16; cnt: 16
-constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
-constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kSmemRows = (kBins + kHistExtra + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kSmemCluster = (2 * (kBins + kHistExtra) + 2 * kCandCap + kPageCache + kScratchWords) * 4;
 
 __device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
     Shared s;
     uint32_t* w = reinterpret_cast<uint32_t*>(base);
     s.hist = w;
-    w += kBins;
+    w += kBins + kHistExtra;
     if (merged_separate) {
         s.mhist = w;
-        w += kBins;
+        w += kBins + kHistExtra;
     } else {
         s.mhist = s.hist;
     }
@@ -380,8 +387,6 @@ struct SoloMerge {
         return sh.hist;
     }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt[i]; }
-    // true if `flag` is set on any thread
-    __device__ __forceinline__ bool any(const Shared&, bool flag) const { return __syncthreads_or(flag) != 0; }
 };
 
 struct ClusterMerge {
@@ -415,18 +420,6 @@ struct ClusterMerge {
     }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const {
         return cg::this_cluster().map_shared_rank(&sh.cnt[i], 0);
-    }
-    // true if `flag` is set on any thread of any CTA of the cluster
-    __device__ bool any(const Shared& sh, bool flag) const {
-        cg::cluster_group cluster = cg::this_cluster();
-        const bool local = __syncthreads_or(flag) != 0;
-        if (threadIdx.x == 0) sh.cnt[4] = local ? 1u : 0u;
-        cluster.sync();
-        uint32_t v = 0;
-        if (threadIdx.x < kClusterSize) v = *cluster.map_shared_rank(&sh.cnt[4], threadIdx.x);
-        const bool r = __syncthreads_or(v != 0) != 0;
-        cluster.sync();  // no CTA rewrites its flag before every CTA has read it
-        return r;
     }
 };
 
@@ -520,7 +513,11 @@ __device__ __forceinline__ void apply_level(SelState& st, int lvl, const Thresho
     st.exact = (t.count == st.need);
 }
 
-// Levels first..last of the radix descent, stopping once exact.
+// Levels first..last of the radix descent, stopping once exact. A key level
+// also counts, in the word after its bins, the elements of the current group
+// with any key bit below its digit set; when the merged count is 0 every such
+// bit is 0 throughout the group (scores rounded to bf16 or coarser), so the
+// key is settled and the remaining key levels are skipped.
 template <class Merge, class Src>
 __device__ void run_levels(SelState& st, int first, int last, const Src& src, const Shared& sh,
                            const Merge& mg) {
@@ -529,14 +526,24 @@ __device__ void run_levels(SelState& st, int first, int last, const Src& src, co
         const int shift = level_shift(lvl);
         uint32_t* hist = sh.hist;
         const uint32_t digit = static_cast<uint32_t>(nb - 1);
-        clear_hist(sh.hist, nb);
+        const bool key_level = lvl < kKeyLevels;
+        const int words = key_level ? nb + 4 : nb;
+        clear_hist(sh.hist, words);
         __syncthreads();
-        if (lvl < kKeyLevels) {  // key digits: a 32-bit filter on the resolved key bits
+        uint32_t below = 0;
+        if (key_level) {  // key digits: a 32-bit filter on the resolved key bits
             const uint32_t pfx = static_cast<uint32_t>(st.prefix >> 32), msk = static_cast<uint32_t>(st.mask >> 32);
             const int sh32 = shift - 32;
+            below = (1u << sh32) - 1u;
+            uint32_t nz = 0;
             src.visit([&](uint32_t key, int32_t, bool valid) {
-                if (valid && (key & msk) == pfx) atomicAdd(&hist[(key >> sh32) & digit], 1u);
+                if (valid && (key & msk) == pfx) {
+                    atomicAdd(&hist[(key >> sh32) & digit], 1u);
+                    nz += (key & below) != 0u;
+                }
             });
+            nz = __reduce_add_sync(kFull, nz);
+            if (lane_id() == 0 && nz != 0) atomicAdd(&hist[nb], nz);
         } else {  // position digits of the elements tied at the threshold
             const uint64_t prefix = st.prefix, mask = st.mask;
             src.visit([&](uint32_t key, int32_t pos, bool valid) {
@@ -544,9 +551,14 @@ __device__ void run_levels(SelState& st, int first, int last, const Src& src, co
                 if (valid && (c & mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(c >> shift) & digit], 1u);
             });
         }
-        const uint32_t* merged = mg.merge(sh, nb);
+        const uint32_t* merged = mg.merge(sh, words);
+        const bool settled = key_level && merged[nb] == 0u;  // read before find's barrier
         const Threshold t = find_threshold(merged, nb, st.need, sh);
         apply_level(st, lvl, t);
+        if (settled && lvl < kKeyLevels - 1) {
+            st.mask |= static_cast<uint64_t>(below) << 32;  // those bits are 0 in the prefix too
+            lvl = kKeyLevels - 1;
+        }
     }
 }
 
@@ -1022,19 +1034,21 @@ __device__ __forceinline__ int window_count(int ja, int jb, int rem, int len) {
 
 
 // Streaming route over vectors [jb, je) of the aligned window: the whole row
-// on one CTA, or this CTA's slice of a cluster row of nv vectors cut into
-// `parts` slices of `per` vectors.
-//  1. The head tile of every slice gets a full level-1 histogram; the merged
-//     head histogram sets a lower bound on the threshold bin, aiming about
-//     4 sigma above the row's expected share of the top-k in the heads.
+// on one CTA, or slice `part` of a row cut over a thread-block cluster.
+//  1. The slice's head tile gets a full level-1 histogram, which sets the
+//     slice's own lower bound on the threshold bin, aiming about 4 sigma
+//     above the slice head's expected share of the top-k (no cluster
+//     exchange).
 //  2. One pass over the rest collects every element at or above the bound.
-//  3. Level 1 comes from the candidates' histogram. It is exact when they
-//     number at least k (they then hold every element of every bin at or
-//     above the threshold bin); otherwise, or if a buffer overflowed, a full
+//  3. Level 1 comes from the merged histograms. It is exact when its
+//     threshold bin clears every slice's bound (each slice's counts are
+//     exact from its bound up); otherwise, or if a buffer overflowed, a full
 //     histogram pass and a re-collection run (always exact, only slower).
+//  4. Solo rows finish with finish_candidates; cluster rows run the radix
+//     levels and emit_selected over the slices' candidate buffers.
 template <bool kPaged, class Merge>
-__device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int per, int parts, int rem, int len,
-                              uint32_t k, bool det, const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
+__device__ void streaming_row(const float4* vbase, int jb, int je, int part, int rem, int len, uint32_t k, bool det,
+                              const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
     load_bits(cur, vbase, jb, je);                   // the head tile
@@ -1045,17 +1059,14 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
         for (int e = 0; e < 4 * kTileVecs; ++e)
             if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(cur, e))) >> 20], 1u);
     }
-    const uint32_t* head = mg.merge(sh, kBins);
-    int n_head = 0;
-    for (int r = 0; r < parts; ++r) {
-        const int a = min(nv, r * per), b = min(nv, a + per);
-        n_head += window_count(a, min(b, a + T), rem, len);
-    }
+    __syncthreads();  // the head histogram is complete
+    // this part's lower bound, from its own head tile
+    const int n_head = window_count(jb, min(je, jb + T), rem, len);
     uint32_t bound_bin = 0;
     if (n_head > 0) {
         const float expect = static_cast<float>(k) * static_cast<float>(n_head) / static_cast<float>(len);
         const float tgt = fminf(expect + 4.0f * sqrtf(expect) + 16.0f, static_cast<float>(n_head));
-        bound_bin = find_threshold(head, kBins, max(static_cast<uint32_t>(tgt), 1u), sh).bin;
+        bound_bin = find_threshold(sh.hist, kBins, max(static_cast<uint32_t>(tgt), 1u), sh).bin;
     }
     const uint32_t bound_key = bound_bin << 20;
     collect_bits(cur, tile_pass(cur, jb, je, rem, len, bound_key), jb, rem, sh);
@@ -1070,14 +1081,25 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int nv, int p
         j0 += T;
     }
     __syncthreads();
-    const bool overflow = sh.cnt[0] > static_cast<uint32_t>(kCandCap);
-    // The histogram holds every head-tile element and every candidate after
-    // it, so its counts are exact for every bin at or above the bound: level
-    // 1 is exact when its threshold bin is one of them.
-    const uint32_t* merged = mg.merge(sh, kBins);
+    // Each part's histogram holds every head-tile element and every candidate
+    // after it, so its counts are exact for every bin at or above its bound;
+    // the merged level 1 is exact when its threshold bin clears every part's
+    // bound. The words after the bins carry each part's bound and overflow
+    // flag through the same merge.
+    if (threadIdx.x == 0) {
+        sh.hist[kBins + part] = bound_bin;
+        sh.hist[kBins + kClusterSize + part] = sh.cnt[0] > static_cast<uint32_t>(kCandCap) ? 1u : 0u;
+    }
+    const uint32_t* merged = mg.merge(sh, kBins + kHistExtra);
+    uint32_t max_bound = 0, overflow = 0;
+#pragma unroll
+    for (int r = 0; r < kClusterSize; ++r) {
+        max_bound = max(max_bound, merged[kBins + r]);
+        overflow |= merged[kBins + kClusterSize + r];
+    }
     Threshold t1 = find_threshold(merged, kBins, k, sh);
     bool cands_ok = true;
-    if (mg.any(sh, overflow) || !t1.found || t1.bin < bound_bin) {  // uniform over a cluster
+    if (overflow != 0 || !t1.found || t1.bin < max_bound) {  // uniform over a cluster
         // full level-1 histogram of this CTA's elements, then re-collect
         clear_hist(sh.hist, kBins);
         __syncthreads();
@@ -1222,9 +1244,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
     if (nv <= kTileVecs * kThreads) {
         register_row<kPaged>(vbase, nv, rem, len, k, det, sh, em);
     } else {
-        clear_hist(sh.hist, kBins);
+        clear_hist(sh.hist, kBins + kHistExtra);
         __syncthreads();
-        streaming_row<kPaged>(vbase, 0, nv, nv, nv, 1, rem, len, k, det, sh, SoloMerge{}, em);
+        streaming_row<kPaged>(vbase, 0, nv, 0, rem, len, k, det, sh, SoloMerge{}, em);
     }
 }
 
@@ -1262,7 +1284,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         }
         prefetch_pages<kPaged>(em, len, sh);
         if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
-        clear_hist(sh.hist, kBins);
+        clear_hist(sh.hist, kBins + kHistExtra);
         const int rem = start & 3;
         const float4* vbase = reinterpret_cast<const float4*>(
             p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
@@ -1273,7 +1295,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         // counters of the leader CTA must be zero before any CTA emits: the
         // merges below pass several cluster barriers first
         __syncthreads();
-        streaming_row<kPaged>(vbase, jb, je, nv, per, kClusterSize, rem, len, k, det, sh, mg, em);
+        streaming_row<kPaged>(vbase, jb, je, rank, rem, len, k, det, sh, mg, em);
         cluster.sync();  // all emits done before the leader's counters are reset
     }
 }

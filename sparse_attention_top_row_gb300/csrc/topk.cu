@@ -250,7 +250,11 @@ struct Threshold {
     bool found;
 };
 
-__device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, const Shared& sh) {
+// First half of the 4096-bin search: every thread returns the histogram's
+// total and the thread whose run crosses the target writes the bin to
+// sh.res. One barrier (after it every bin has been read); the caller reads
+// the result with find_wide_result after a barrier of its own.
+__device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const Shared& sh) {
     constexpr int R = kBins / kThreads;  // bins per thread
     static_assert(R % 4 == 0 && R * kThreads == kBins, "whole 16-byte runs of bins per thread");
     const uint32_t lane = lane_id();
@@ -293,9 +297,18 @@ __device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, con
             r += b[i];
         }
     }
-    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ Threshold find_wide_result(uint32_t total, uint32_t target, const Shared& sh) {
     if (total < target) return Threshold{0u, total, 0u, false};
     return Threshold{sh.res[0], sh.res[1], sh.res[2], true};
+}
+
+__device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, const Shared& sh) {
+    const uint32_t total = find_wide_publish(h, target, sh);
+    __syncthreads();
+    return find_wide_result(total, target, sh);
 }
 
 __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, const Shared& sh) {
@@ -805,13 +818,30 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
 // the number of bin members whose composite (key, ~position) is larger, and
 // the ones ranked below `need` take slots k - need + rank. This settles every
 // remaining key and position digit at once (ties go to the lowest position).
-// The arrays are padded to a multiple of 4 with entries that rank below
-// everything; each element is compared by kThreads / m threads (m = n
-// rounded up to a power of two), each over one segment, and the partial
-// ranks meet in the shared-memory counters `rank` (n words).
+// Up to 32 members are ranked by one warp through shuffles. Longer lists are
+// padded to a multiple of 4 with entries that rank below everything; each
+// element is compared by kThreads / m threads (m = n rounded up to a power of
+// two), each over one segment, and the partial ranks meet in the
+// shared-memory counters `rank` (n words). A caller's barrier must make the
+// lists visible first; the function ends without one.
 template <bool kPaged>
 __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32_t* tkey, int32_t* tpos,
                                    uint32_t* rank, const Emitter<kPaged>& em) {
+    if (n <= 32u) {  // the usual case: warp 0 alone, the members passed round by shuffles
+        if (threadIdx.x < 32) {
+            const uint32_t lane = lane_id();
+            const uint32_t ki = lane < n ? tkey[lane] : 0u;
+            const int32_t pi = lane < n ? tpos[lane] : INT32_MAX;
+            uint32_t r = 0;
+            for (uint32_t j = 0; j < n; ++j) {
+                const uint32_t kj = __shfl_sync(kFull, ki, static_cast<int>(j));
+                const int32_t pj = __shfl_sync(kFull, pi, static_cast<int>(j));
+                r += static_cast<uint32_t>(kj > ki || (kj == ki && pj < pi));
+            }
+            if (lane < n && r < need) em.write(k - need + r, pi);
+        }
+        return;
+    }
     const uint32_t n4 = (n + 3u) & ~3u;
     if (threadIdx.x < n4 - n) {
         tkey[n + threadIdx.x] = 0u;
@@ -937,19 +967,21 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
     for (int e = 0; e < 4 * kTileVecs; ++e)
         if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> 20], 1u);
     __syncthreads();
-    const Threshold t1 = find_threshold(sh.hist, kBins, k, sh);
+    // Level 1; its bins are free once the search has read them, so the
+    // level-2 bins are cleared before the barrier that publishes the result.
+    const uint32_t total1 = find_wide_publish(sh.hist, k, sh);
+    clear_hist(sh.hist, level_bins(1));
+    __syncthreads();
+    const Threshold t1 = find_wide_result(total1, k, sh);
     SoloMerge mg;
     SelState st{0ull, 0ull, k, false};
     apply_level(st, 0, t1);
     const int last = (det ? kAllLevels : kKeyLevels) - 1;
-    // Level 2 inside the threshold bin, histogrammed from the registers (the
-    // level-1 bins have been read: their storage is free).
+    // Level 2 inside the threshold bin, histogrammed from the registers.
     int shift = 20;           // the selection prefix is key >> shift ...
     uint32_t tau = t1.bin;    // ... compared with tau
     uint32_t n_tie = 0;
     if (!st.exact) {
-        clear_hist(sh.hist, level_bins(1));
-        __syncthreads();
 #pragma unroll
         for (int e = 0; e < 4 * kTileVecs; ++e) {
             const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));

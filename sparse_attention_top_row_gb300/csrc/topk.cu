@@ -601,9 +601,9 @@ struct Emitter {
         out[slot] = v;
         if (out_raw) out_raw[slot] = pos;
     }
-    // Straight-line form for unrolled loops: writes when `w` (and the slot is
-    // in range); every load it makes is in bounds whether or not it writes.
-    // The caller reports out-of-range slots (see flag_if).
+    // Straight-line form for loops over candidates: writes when `w` (and the
+    // slot is in range); every load it makes is in bounds whether or not it
+    // writes. The caller reports out-of-range slots (see flag_if).
     __device__ __forceinline__ void write_if(bool w, uint32_t slot, int32_t pos) const {
         const bool ok = w && slot < k;
         int32_t v;
@@ -617,6 +617,7 @@ struct Emitter {
         if (ok) out[slot] = v;
         if (ok && out_raw) out_raw[slot] = pos;
     }
+    // Reports an out-of-range slot found by a caller that assigns slots itself.
     __device__ __forceinline__ void flag_if(bool bad) const {
         if (bad) atomicOr(flags, TOPK_DEVICE_FLAG_INTERNAL);
     }
@@ -816,7 +817,8 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
 // Ranks the threshold bin's elements, n <= kThreads of them in tkey/tpos
 // (16-byte aligned, room for n rounded up to 4): the rank of an element is
 // the number of bin members whose composite (key, ~position) is larger, and
-// the ones ranked below `need` take slots k - need + rank. This settles every
+// the ones ranked below `need` take slots k - need + rank: put(slot, pos)
+// stores each one. This settles every
 // remaining key and position digit at once (ties go to the lowest position).
 // Up to 32 members are ranked by one warp through shuffles. Longer lists are
 // padded to a multiple of 4 with entries that rank below everything; each
@@ -824,9 +826,9 @@ __device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_
 // two), each over one segment, and the partial ranks meet in the
 // shared-memory counters `rank` (n words). A caller's barrier must make the
 // lists visible first; the function ends without one.
-template <bool kPaged>
+template <class Put>
 __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32_t* tkey, int32_t* tpos,
-                                   uint32_t* rank, const Emitter<kPaged>& em) {
+                                   uint32_t* rank, const Put& put) {
     if (n <= 32u) {  // the usual case: warp 0 alone, the members passed round by shuffles
         if (threadIdx.x < 32) {
             const uint32_t lane = lane_id();
@@ -838,7 +840,7 @@ __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32
                 const int32_t pj = __shfl_sync(kFull, pi, static_cast<int>(j));
                 r += static_cast<uint32_t>(kj > ki || (kj == ki && pj < pi));
             }
-            if (lane < n && r < need) em.write(k - need + r, pi);
+            if (lane < n && r < need) put(k - need + r, pi);
         }
         return;
     }
@@ -872,17 +874,25 @@ __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32
     __syncthreads();
     if (seg == 0 && i < n) {
         const uint32_t r = rank[i];
-        if (r < need) em.write(k - need + r, tpos[i]);
+        if (r < need) put(k - need + r, tpos[i]);
     }
 }
 
-// The finish shared by the solo routes once level 1 is known and every
+// Writes the slot-ordered position list (k entries in shared memory) to the
+// output row: thread t takes slots t, t + kThreads, ..., so every warp store
+// covers 32 consecutive slots. Follows a barrier that completes the list.
+template <bool kPaged>
+__device__ __forceinline__ void write_slots(const int32_t* slots, uint32_t k, const Emitter<kPaged>& em) {
+    for (uint32_t s = threadIdx.x; s < k; s += kThreads) em.write(s, slots[s]);
+}
+
+// The finish of a solo streaming row once level 1 is known and every
 // element at or above its threshold bin sits in the candidate buffer (n of
 // them): level 2 is histogrammed over the threshold bin's candidates (unless
 // level 1 is exact); then one counting pass and one writing pass over the
 // buffer send every element above the threshold prefix to its slot (a block
 // scan orders them) and copy the elements equal to it to a tie list (in the
-// histogram's storage), which rank_threshold_bin finishes. Returns false,
+// histogram's storage), which rank_threshold_bin orders into the last slots. Returns false,
 // having written nothing, when the level-2 threshold bin is too full to rank
 // (many equal scores): the caller continues with the radix levels from
 // level 3 (st then holds levels 1 and 2).
@@ -939,7 +949,8 @@ __device__ bool finish_candidates(SelState& st, uint32_t bin1, uint32_t n, uint3
     em.flag_if(slot > k - (exact ? 0u : st.need));
     if (!exact) {
         __syncthreads();
-        rank_threshold_bin<kPaged>(n_tie, st.need, k, tkey, tpos, sh.cand_key, em);
+        rank_threshold_bin(n_tie, st.need, k, tkey, tpos, sh.cand_key,
+                           [&](uint32_t s, int32_t pos) { em.write(s, pos); });
     }
     return true;
 }
@@ -1016,12 +1027,13 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
         uint32_t base = incl - c;
         for (int w = 0; w < warp; ++w) base += sh.red[w];
         uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
+        int32_t* slots = reinterpret_cast<int32_t*>(sh.hist + kBins - TOPK_MAX_K);  // slot-ordered positions
 #pragma unroll
         for (int e = 0; e < 4 * kTileVecs; ++e) {
             const int32_t pos = 4 * ((e / 4) * kThreads + static_cast<int>(threadIdx.x)) - rem + (e % 4);
             const bool w = (def >> e) & 1u;
             const bool t = (tie >> e) & 1u;
-            em.write_if(w, slot, pos);
+            if (w && slot < k) slots[slot] = pos;
             if (t) {
                 sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
                 sh.cand_pos[tslot] = pos;
@@ -1030,10 +1042,13 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
             tslot += t;
         }
         em.flag_if(slot > k - (exact ? 0u : st.need));
+        __syncthreads();
         if (!exact) {
+            rank_threshold_bin(n_tie, st.need, k, sh.cand_key, sh.cand_pos, sh.hist,
+                               [&](uint32_t s, int32_t pos) { slots[s] = pos; });
             __syncthreads();
-            rank_threshold_bin<kPaged>(n_tie, st.need, k, sh.cand_key, sh.cand_pos, sh.hist, em);
         }
+        write_slots<kPaged>(slots, k, em);
         return;
     }
     // A threshold bin too full to rank (many equal scores): the radix levels

@@ -191,6 +191,36 @@ def test_cluster_path_with_adversarial_rows(cuda_lib):
     check_full(cuda_lib, w)
 
 
+@pytest.mark.parametrize("kind", ["bf16", "negative", "spread", "special"])
+def test_cluster_path_value_kinds(cuda_lib, kind):
+    """Cluster rows (B <= 64, L > 32768) on value kinds that steer the
+    radix descent: bf16-rounded scores end the key descent early, negative
+    scores give negative bounds, one value per level-1 bin makes level 1
+    exact, and infinities/signed zeros/extreme finite values."""
+    rng = np.random.default_rng(11)
+    rows = _rows(rng, [40000, 131072, 65537], kind)
+    w = wl.custom("ragged", 2048, rows, row_starts=[3, 1, 2], out_offsets=[0, 7, 1 << 20], seed=11)
+    check_full(cuda_lib, w)
+
+
+@pytest.mark.parametrize("k", [1, 33, 2048])
+def test_small_tie_lists(cuda_lib, k):
+    """Rows whose threshold value repeats a few times (up to 32 members: the
+    one-warp ranking) and many times (the segmented ranking), on the register
+    and streaming routes."""
+    rng = np.random.default_rng(k)
+    rows = []
+    for L, reps in ((5000, 5), (5000, 40), (20000, 20), (20000, 300)):
+        v = rng.standard_normal(L).astype(np.float32)
+        order = np.sort(v)[::-1]
+        thr = order[min(k, L) - 1]
+        idx = rng.choice(L, size=reps, replace=False)
+        v[idx] = thr  # the k-th largest value now occurs reps (+1) times
+        rows.append(v.tolist())
+    w = wl.custom("paged", k, rows, page_size=16, seed=k)
+    check_full(cuda_lib, w)
+
+
 def test_nan_scores_order_deterministically(cuda_lib):
     rng = np.random.default_rng(11)
     v = rng.standard_normal(20000).astype(np.float32)

@@ -29,6 +29,9 @@
  * The library never allocates; the caller owns all buffers. Work is enqueued
  * on `stream` (a cudaStream_t; NULL = the legacy default stream) and the calls
  * return without waiting for it. Scores are read only and never written.
+ * The kernels are launched with programmatic dependent launch: they may be
+ * scheduled while earlier work on the stream drains, but read and write no
+ * memory until that work has completed, so stream order holds as usual.
  *
  * Errors. Argument errors are found on the host before anything is enqueued
  * and returned as a topk_status; the call then has no effect. A failed launch
@@ -137,7 +140,7 @@ TOPK_API int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* 
  *   out               int32 [batch, k], row-major; every slot is written.
  *   out_raw           int32 [batch, k] or NULL: the untransformed positions p
  *                     in the same slots as `out` (-1 in the padding).
- *   flags             0 or TOPK_DETERMINISTIC.
+ *   flags             0 or TOPK_DETERMINISTIC (any other bit: TOPK_ERR_ARG).
  */
 TOPK_API int topk_transform_paged(const float* scores, int64_t score_stride,
                                   const int32_t* row_starts, const int32_t* seq_lens,

@@ -1525,8 +1525,9 @@ int launch_transform(const Params& prm, cudaStream_t stream) {
 }
 
 int common_checks(const float* scores, int64_t score_stride, const int32_t* seq_lens, int32_t batch,
-                  int32_t k, void* workspace, size_t workspace_bytes, int32_t* out) {
+                  int32_t k, void* workspace, size_t workspace_bytes, int32_t* out, uint32_t flags) {
     if (!valid_k(k)) return TOPK_ERR_K;
+    if ((flags & ~TOPK_DETERMINISTIC) != 0) return TOPK_ERR_ARG;
     if (batch < 0 || score_stride < 0 || (score_stride & 3) != 0) return TOPK_ERR_ARG;
     if (batch > 0 && (scores == nullptr || seq_lens == nullptr || out == nullptr)) return TOPK_ERR_ARG;
     if (batch > 0 && (reinterpret_cast<uintptr_t>(scores) & 15u) != 0) return TOPK_ERR_ALIGN;
@@ -1576,7 +1577,7 @@ int topk_transform_paged(const float* scores, int64_t score_stride, const int32_
                          int32_t page_size, int32_t batch, int32_t k, void* workspace,
                          size_t workspace_bytes, int32_t* out, int32_t* out_raw, uint32_t flags,
                          topk_stream_t stream) {
-    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out);
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out, flags);
     if (st != TOPK_OK) return st;
     if (page_size < 1 || page_size > TOPK_MAX_PAGE_SIZE || (page_size & (page_size - 1)) != 0)
         return TOPK_ERR_PAGE_SIZE;
@@ -1595,7 +1596,7 @@ int topk_transform_ragged(const float* scores, int64_t score_stride, const int32
                           const int32_t* seq_lens, const int32_t* out_offsets, int32_t batch, int32_t k,
                           void* workspace, size_t workspace_bytes, int32_t* out, int32_t* out_raw,
                           uint32_t flags, topk_stream_t stream) {
-    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out);
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out, flags);
     if (st != TOPK_OK) return st;
     if (batch > 0 && out_offsets == nullptr) return TOPK_ERR_ARG;
     if (batch == 0) return TOPK_OK;
@@ -1686,7 +1687,8 @@ extern "C" int topk_transform_ragged_noalloc(const float* scores, int64_t score_
     if (batch > TOPK_NOALLOC_MAX_BATCH) return TOPK_ERR_WORKSPACE;
     // validate everything before anything is enqueued (a stand-in non-null
     // workspace pointer: the real one is looked up below)
-    const int st = common_checks(scores, score_stride, seq_lens, batch, k, g_noalloc, kNoAllocWorkspaceBytes, out);
+    const int st =
+        common_checks(scores, score_stride, seq_lens, batch, k, g_noalloc, kNoAllocWorkspaceBytes, out, flags);
     if (st != TOPK_OK) return st;
     if (batch > 0 && out_offsets == nullptr) return TOPK_ERR_ARG;
     if (batch == 0) return TOPK_OK;

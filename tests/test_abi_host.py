@@ -78,10 +78,14 @@ def test_transform_validation(lib):
     assert paged(FAKE, 64, None, FAKE, FAKE, 4, 64, 8, 16, FAKE, ws, None, None, 0, None) == 1
     assert paged(FAKE, 64, None, FAKE, FAKE, 4, 64, 8, 16, FAKE, ws - 1, FAKE, None, 0, None) == 5
     assert paged(FAKE, 64, None, FAKE, FAKE, 4, 64, -2, 16, FAKE, ws, FAKE, None, 0, None) == 1
+    # flags: TOPK_DETERMINISTIC is the only bit
+    assert paged(FAKE, 64, None, FAKE, FAKE, 4, 64, 8, 16, FAKE, ws, FAKE, None, 2, None) == 1
+    assert paged(FAKE, 64, None, FAKE, FAKE, 4, 64, 8, 16, FAKE, ws, FAKE, None, 1 << 31, None) == 1
     # scores, stride, row_starts, seq_lens, out_offsets, batch, k, ws, ws_bytes, out, out_raw, flags, stream
     assert ragged(FAKE, 0, None, FAKE, None, 8, 16, FAKE, ws, FAKE, None, 0, None) == 1
     assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 4096, FAKE, ws, FAKE, None, 0, None) == 3
     assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 16, None, ws, FAKE, None, 0, None) == 5
+    assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, None, 3, None) == 1
     # an empty batch is a no-op that enqueues nothing
     assert ragged(None, 0, None, None, None, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, None, 0, None) == 0
     assert paged(None, 0, None, None, None, 0, 1, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, None, 0, None) == 0

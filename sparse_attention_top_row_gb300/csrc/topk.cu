@@ -77,6 +77,8 @@ constexpr int kThreads = 512;                 // threads per CTA, all routes
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
 constexpr int kHistExtra = 8;                 // words after the bins, merged (summed) with them
+constexpr int kFineShift = 18;                // register route: a 14-bit first digit ...
+constexpr int kFineWords = 8192;              // ... two 16-bit counters per word
 constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
 constexpr int kPageCache = 4096;              // page-table entries of a row held in shared memory
 constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
@@ -303,6 +305,67 @@ __device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const 
 __device__ __forceinline__ Threshold find_wide_result(uint32_t total, uint32_t target, const Shared& sh) {
     if (total < target) return Threshold{0u, total, 0u, false};
     return Threshold{sh.res[0], sh.res[1], sh.res[2], true};
+}
+
+// find_wide_publish for the register route's 16384 bins of 16-bit counters,
+// two per word (bin 2w in the low half of word w): thread t holds words
+// 16t..16t+15. Per-thread sums add whole words (each half stays below 2^16:
+// a row holds at most 8192 elements).
+__device__ uint32_t find_fine_publish(const uint32_t* h, uint32_t target, const Shared& sh) {
+    constexpr int W = kFineWords / kThreads;
+    static_assert(W % 4 == 0 && W * kThreads == kFineWords, "whole 16-byte runs of words per thread");
+    const uint32_t lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    uint32_t wd[W];
+#pragma unroll
+    for (int q = 0; q < W / 4; ++q) {
+        const uint4 u = reinterpret_cast<const uint4*>(h)[(W / 4) * threadIdx.x + q];
+        wd[4 * q] = u.x, wd[4 * q + 1] = u.y, wd[4 * q + 2] = u.z, wd[4 * q + 3] = u.w;
+    }
+    uint32_t pair = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) pair += wd[i];
+    const uint32_t s32 = (pair & 0xFFFFu) + (pair >> 16);
+    uint32_t x = s32;  // sum over the lanes >= this lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, x, off);
+        if (lane + off < 32) x += y;
+    }
+    if (lane == 0) sh.red[warp] = x;
+    __syncthreads();
+    uint32_t above = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t r = sh.red[w];
+        total += r;
+        above += w > warp ? r : 0u;
+    }
+    const uint32_t incl = above + x, excl = incl - s32;
+    if (excl < target && incl >= target) {
+        // the word first (both halves at once), then the half; the run ends
+        // in word 0 at the latest
+        uint32_t r = excl, wsel = 0, rsel = 0;
+        int isel = 0;
+        bool done = false;
+#pragma unroll
+        for (int i = W - 1; i >= 0; --i) {
+            const uint32_t c2 = (wd[i] & 0xFFFFu) + (wd[i] >> 16);
+            if (!done && (i == 0 || r + c2 >= target)) {
+                wsel = wd[i];
+                isel = i;
+                rsel = r;
+                done = true;
+            }
+            r += c2;
+        }
+        const uint32_t hi = wsel >> 16, lo = wsel & 0xFFFFu;
+        const bool in_hi = rsel + hi >= target;
+        sh.res[0] = 2 * (W * threadIdx.x + static_cast<uint32_t>(isel)) + (in_hi ? 1u : 0u);
+        sh.res[1] = in_hi ? rsel : rsel + hi;
+        sh.res[2] = in_hi ? hi : lo;
+    }
+    return total;
 }
 
 __device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, const Shared& sh) {
@@ -955,25 +1018,100 @@ __device__ bool finish_candidates(SelState& st, uint32_t bin1, uint32_t n, uint3
     return true;
 }
 
+// The register route's finish once the selection prefix is known: every
+// tile element whose prefix (key >> shift) is above tau (at least tau when
+// exact) is selected and goes to its slot in a slot-ordered list (one block
+// scan of both counts orders the slots), the elements equal to it (not
+// exact) go to a tie list in the candidate buffer, which rank_threshold_bin
+// orders into the last `need` slots, and the list is written out coalesced.
+template <bool kPaged>
+__device__ void finish_registers(const int4 (&v)[kTileVecs], uint32_t valid, int rem, int shift, uint32_t tau,
+                                 bool exact, uint32_t need, uint32_t n_tie, uint32_t k, const Shared& sh,
+                                 const Emitter<kPaged>& em) {
+    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
+    uint32_t def = 0, tie = 0;
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e) {
+        const uint32_t pf = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> shift;
+        def |= static_cast<uint32_t>(exact ? pf >= tau : pf > tau) << e;
+        tie |= static_cast<uint32_t>(pf == tau) << e;
+    }
+    def &= valid;
+    tie = exact ? 0u : (tie & valid);
+    // both counts in one scan: selected in the low half, ties in the high
+    // half (a CTA holds at most 8192 elements)
+    const uint32_t c = static_cast<uint32_t>(__popc(def)) | (static_cast<uint32_t>(__popc(tie)) << 16);
+    const uint32_t incl = warp_inclusive_scan(c);
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    if (lane_id() == 31) sh.red[warp] = incl;
+    __syncthreads();
+    uint32_t base = incl - c;
+    for (int w = 0; w < warp; ++w) base += sh.red[w];
+    uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
+    int32_t* slots = reinterpret_cast<int32_t*>(sh.hist + kBins - TOPK_MAX_K);  // slot-ordered positions
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e) {
+        const int32_t pos = 4 * ((e / 4) * kThreads + static_cast<int>(threadIdx.x)) - rem + (e % 4);
+        const bool w = (def >> e) & 1u;
+        const bool t = (tie >> e) & 1u;
+        if (w && slot < k) slots[slot] = pos;
+        if (t) {
+            sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
+            sh.cand_pos[tslot] = pos;
+        }
+        slot += w;
+        tslot += t;
+    }
+    em.flag_if(slot > k - (exact ? 0u : need));
+    __syncthreads();
+    if (!exact) {
+        rank_threshold_bin(n_tie, need, k, sh.cand_key, sh.cand_pos, sh.hist,
+                           [&](uint32_t s, int32_t pos) { slots[s] = pos; });
+        __syncthreads();
+    }
+    write_slots<kPaged>(slots, k, em);
+}
+
 // Register route: the whole aligned window (nv <= kTileVecs * kThreads
-// vectors) is one register tile, and level 1 is a full histogram of it.
-// Unless level 1 is exact, level 2 (the next 8 key bits) is histogrammed
-// from the registers over the level-1 threshold bin.
-//  * Level-2 threshold bin of at most kThreads elements (the usual case): one
-//    more look at the tile writes every element above the 20-bit threshold
-//    prefix straight to its output slot and copies the elements equal to it
-//    to the candidate buffer (one block scan of both counts orders the
-//    slots), where rank_threshold_bin finishes the row.
-//  * Otherwise (many equal scores) the radix levels continue on the candidate
-//    buffer, or on the registers when the bins do not fit it.
+// vectors) is one register tile.
+//  * The first digit is 14 bits wide: 16384 16-bit counters (two per word,
+//    in the candidate buffer's storage), one shared atomic per element. When
+//    its threshold bin holds at most kThreads elements (the usual case; about
+//    40 for a row of 8192 normal scores), finish_registers writes every
+//    element above it to its slot and ranks the bin's members for the rest.
+//  * Otherwise (many equal scores) the 12-bit levels run: level 1 from the
+//    tile, level 2 over its threshold bin from the registers, the same finish
+//    when that bin is small, else the radix levels on the candidate buffer
+//    (or on the registers when the bins do not fit it).
 template <bool kPaged>
 __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
                              const Shared& sh, const Emitter<kPaged>& em) {
     int4 v[kTileVecs];
     load_bits(v, vbase, 0, nv);  // in flight while the histogram is cleared
-    clear_hist(sh.hist, kBins);
+    static_assert(kFineWords <= 2 * kCandCap, "the fine histogram lives in the candidate buffer");
+    uint32_t* fine = sh.cand_key;
+    clear_hist(fine, kFineWords);
     __syncthreads();
     const uint32_t valid = tile_valid(0, nv, rem, len);
+#pragma unroll
+    for (int e = 0; e < 4 * kTileVecs; ++e) {
+        const uint32_t d = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> kFineShift;
+        if ((valid >> e) & 1u) atomicAdd(&fine[d >> 1], (d & 1u) ? 0x10000u : 1u);
+    }
+    __syncthreads();
+    {
+        const uint32_t total = find_fine_publish(fine, k, sh);
+        __syncthreads();  // the fine bins are read: the candidate buffer is free again
+        const Threshold tf = find_wide_result(total, k, sh);
+        const uint32_t need = k - tf.above;
+        const bool exact = tf.count == need;
+        if (exact || tf.count <= static_cast<uint32_t>(kThreads)) {
+            finish_registers<kPaged>(v, valid, rem, kFineShift, tf.bin, exact, need, tf.count, k, sh, em);
+            return;
+        }
+    }
+    clear_hist(sh.hist, kBins);
+    __syncthreads();
 #pragma unroll
     for (int e = 0; e < 4 * kTileVecs; ++e)
         if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> 20], 1u);
@@ -1006,49 +1144,7 @@ __device__ void register_row(const float4* vbase, int nv, int rem, int len, uint
         n_tie = t2.count;
     }
     if (st.exact || n_tie <= static_cast<uint32_t>(kThreads)) {
-        if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
-        const bool exact = st.exact;
-        uint32_t def = 0, tie = 0;
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e) {
-            const uint32_t pf = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> shift;
-            def |= static_cast<uint32_t>(exact ? pf >= tau : pf > tau) << e;
-            tie |= static_cast<uint32_t>(pf == tau) << e;
-        }
-        def &= valid;
-        tie = exact ? 0u : (tie & valid);
-        // both counts in one scan: selected in the low half, ties in the high
-        // half (a CTA holds at most 8192 elements)
-        const uint32_t c = static_cast<uint32_t>(__popc(def)) | (static_cast<uint32_t>(__popc(tie)) << 16);
-        const uint32_t incl = warp_inclusive_scan(c);
-        const int warp = static_cast<int>(threadIdx.x >> 5);
-        if (lane_id() == 31) sh.red[warp] = incl;
-        __syncthreads();
-        uint32_t base = incl - c;
-        for (int w = 0; w < warp; ++w) base += sh.red[w];
-        uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
-        int32_t* slots = reinterpret_cast<int32_t*>(sh.hist + kBins - TOPK_MAX_K);  // slot-ordered positions
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e) {
-            const int32_t pos = 4 * ((e / 4) * kThreads + static_cast<int>(threadIdx.x)) - rem + (e % 4);
-            const bool w = (def >> e) & 1u;
-            const bool t = (tie >> e) & 1u;
-            if (w && slot < k) slots[slot] = pos;
-            if (t) {
-                sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
-                sh.cand_pos[tslot] = pos;
-            }
-            slot += w;
-            tslot += t;
-        }
-        em.flag_if(slot > k - (exact ? 0u : st.need));
-        __syncthreads();
-        if (!exact) {
-            rank_threshold_bin(n_tie, st.need, k, sh.cand_key, sh.cand_pos, sh.hist,
-                               [&](uint32_t s, int32_t pos) { slots[s] = pos; });
-            __syncthreads();
-        }
-        write_slots<kPaged>(slots, k, em);
+        finish_registers<kPaged>(v, valid, rem, shift, tau, st.exact, st.need, n_tie, k, sh, em);
         return;
     }
     // A threshold bin too full to rank (many equal scores): the radix levels

@@ -1480,23 +1480,29 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
         if (valid && (peers & lt) == 0) atomicAdd(&count[band], __popc(peers));
     }
     __syncthreads();
-    if (tid == 0) {
-        uint32_t run = 0;
-        for (int bnd = 0; bnd <= kBandTrivial; ++bnd) {
-            offset[bnd] = run;
-            run += count[bnd];
-        }
-        offset[kBandCluster] = 0;
+    if (tid < 32) {  // band offsets: warp 0, lane l holding bands 2l and 2l + 1
+        static_assert(kBandTrivial + 1 <= 64, "two ordered bands per lane");
+        const int b0 = 2 * tid, b1 = 2 * tid + 1;
+        const uint32_t c0 = b0 <= kBandTrivial ? count[b0] : 0u, c1 = b1 <= kBandTrivial ? count[b1] : 0u;
+        const uint32_t incl = warp_inclusive_scan(c0 + c1);
+        const uint32_t excl = incl - c0 - c1;
+        if (b0 <= kBandTrivial) offset[b0] = excl;
+        if (b1 <= kBandTrivial) offset[b1] = excl + c0;
+        const uint32_t run = __shfl_sync(kFull, incl, 31);
         // one band holds every row: the rows keep their own order
-        in_place = false;
-        for (int bnd = 0; bnd <= kBandTrivial; ++bnd) in_place |= count[bnd] == static_cast<uint32_t>(batch);
-        hdr->n_order = static_cast<int32_t>(run);
-        hdr->n_cluster = static_cast<int32_t>(count[kBandCluster]);
-        hdr->error_rows = n_err;
-        hdr->flags = 0;
-        hdr->batch = batch;
-        hdr->k = k;
-        hdr->magic = kPlanMagic;
+        const bool one_band = __any_sync(kFull, (b0 <= kBandTrivial && c0 == static_cast<uint32_t>(batch)) ||
+                                                    (b1 <= kBandTrivial && c1 == static_cast<uint32_t>(batch)));
+        if (tid == 0) {
+            offset[kBandCluster] = 0;
+            in_place = one_band;
+            hdr->n_order = static_cast<int32_t>(run);
+            hdr->n_cluster = static_cast<int32_t>(count[kBandCluster]);
+            hdr->error_rows = n_err;
+            hdr->flags = 0;
+            hdr->batch = batch;
+            hdr->k = k;
+            hdr->magic = kPlanMagic;
+        }
     }
     __syncthreads();
     if (in_place) {

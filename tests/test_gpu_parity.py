@@ -138,6 +138,8 @@ def _rows(rng, lens, kind="normal"):
             e = (code % 1600) // 8 - 100
             m = code % 8
             rows.append((sign * np.ldexp(1.0 + m / 8.0, e)).astype(np.float32).tolist())
+        elif kind == "narrow":  # one 14-bit prefix for every score, spread below it: the 12-bit levels' small-tie finish
+            rows.append((1.0 + rng.random(L) / 64.0).astype(np.float32).tolist())
         elif kind == "negative":  # every score below zero: negative thresholds and bounds
             rows.append((-1.0 - np.abs(rng.standard_normal(L))).astype(np.float32).tolist())
         elif kind == "bf16":  # N(0, 0.01) rounded to bf16: long runs of equal keys at the threshold
@@ -166,14 +168,16 @@ def test_boundary_lengths(cuda_lib, k, mode):
 
 
 @pytest.mark.parametrize("kind", ["ties", "equal", "ascending", "descending", "special", "spread", "bf16",
-                                  "negative"])
+                                  "negative", "narrow"])
 @pytest.mark.parametrize("L", [3000, 8000, 12000, 50000])
 def test_adversarial_values(cuda_lib, kind, L):
     """Heavy ties, one value everywhere, sorted rows (the first-tile estimate is
     then wrong or the candidate buffer overflows: the exact fallbacks run),
     infinities, signed zeros and the largest finite values; one value per
     level-1 bin (level 1 is exact); bf16-rounded values (equal keys beyond
-    the second level); all-negative rows (negative thresholds and bounds).
+    the second level); all-negative rows (negative thresholds and bounds);
+    scores sharing one 14-bit key prefix (the register route falls back to
+    its 12-bit levels and finishes there).
     L = 8000 puts a one-value row on the register route's fallback that
     keeps the levels in registers."""
     rng = np.random.default_rng(L)

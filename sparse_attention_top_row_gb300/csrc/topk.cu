@@ -811,13 +811,13 @@ __device__ __forceinline__ uint32_t tile_valid(int j0, int je, int rem, int len)
     return m;
 }
 
-// Bit mask of the tile's in-window elements whose key is at least bound_key,
+// Bit mask of the tile's elements whose key is at least bound_key (tile_ge),
 // by one compare of the raw bits per element: for bound_key >= 2^31 (a
 // non-negative bound) key >= bound_key <=> bits >= bound_key ^ 2^31 as signed
 // integers; below it, key >= bound_key <=> bits <= ~bound_key as unsigned
-// ones. Only a tile that reaches past either end of the window is masked.
-__device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0, int je, int rem, int len,
-                                              uint32_t bound_key) {
+// ones. tile_pass keeps the in-window ones: only a tile that reaches past
+// either end of the window is masked.
+__device__ __forceinline__ uint32_t tile_ge(const int4 (&v)[kTileVecs], uint32_t bound_key) {
     uint32_t pass = 0;
     if (bound_key >= 0x80000000u) {
         const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
@@ -829,6 +829,12 @@ __device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0
         for (int e = 0; e < 4 * kTileVecs; ++e)
             pass |= static_cast<uint32_t>(static_cast<uint32_t>(tile_elem(v, e)) <= ub) << e;
     }
+    return pass;
+}
+
+__device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0, int je, int rem, int len,
+                                              uint32_t bound_key) {
+    const uint32_t pass = tile_ge(v, bound_key);
     const bool interior =
         4 * j0 - rem >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
     return interior ? pass : pass & tile_valid(j0, je, rem, len);
@@ -1029,15 +1035,13 @@ __device__ void finish_registers(const int4 (&v)[kTileVecs], uint32_t valid, int
                                  bool exact, uint32_t need, uint32_t n_tie, uint32_t k, const Shared& sh,
                                  const Emitter<kPaged>& em) {
     if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
-    uint32_t def = 0, tie = 0;
-#pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e) {
-        const uint32_t pf = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> shift;
-        def |= static_cast<uint32_t>(exact ? pf >= tau : pf > tau) << e;
-        tie |= static_cast<uint32_t>(pf == tau) << e;
-    }
-    def &= valid;
-    tie = exact ? 0u : (tie & valid);
+    // prefix >= tau and prefix > tau as raw-bit compares against the
+    // smallest keys with prefix tau and tau + 1
+    const uint32_t ge_tau = tile_ge(v, tau << shift);
+    const bool top_bin = tau + 1u == (1u << (32 - shift));
+    const uint32_t gt_tau = (exact || top_bin) ? 0u : tile_ge(v, (tau + 1u) << shift);
+    const uint32_t def = (exact ? ge_tau : gt_tau) & valid;
+    const uint32_t tie = exact ? 0u : (ge_tau & ~gt_tau & valid);
     // both counts in one scan: selected in the low half, ties in the high
     // half (a CTA holds at most 8192 elements)
     const uint32_t c = static_cast<uint32_t>(__popc(def)) | (static_cast<uint32_t>(__popc(tie)) << 16);
@@ -1049,18 +1053,18 @@ __device__ void finish_registers(const int4 (&v)[kTileVecs], uint32_t valid, int
     for (int w = 0; w < warp; ++w) base += sh.red[w];
     uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
     int32_t* slots = reinterpret_cast<int32_t*>(sh.hist + kBins - TOPK_MAX_K);  // slot-ordered positions
-#pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e) {
-        const int32_t pos = 4 * ((e / 4) * kThreads + static_cast<int>(threadIdx.x)) - rem + (e % 4);
-        const bool w = (def >> e) & 1u;
-        const bool t = (tie >> e) & 1u;
-        if (w && slot < k) slots[slot] = pos;
-        if (t) {
-            sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
-            sh.cand_pos[tslot] = pos;
-        }
-        slot += w;
-        tslot += t;
+    const int32_t p0 = 4 * static_cast<int32_t>(threadIdx.x) - rem;  // position of element 0
+    // walk the set bits only (a warp loops as often as its busiest lane)
+    for (uint32_t rest = def; rest != 0; rest &= rest - 1u) {
+        const int e = __ffs(static_cast<int>(rest)) - 1;
+        if (slot < k) slots[slot] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
+        ++slot;
+    }
+    for (uint32_t rest = tie; rest != 0; rest &= rest - 1u) {
+        const int e = __ffs(static_cast<int>(rest)) - 1;
+        sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem_at(v, e)));
+        sh.cand_pos[tslot] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
+        ++tslot;
     }
     em.flag_if(slot > k - (exact ? 0u : need));
     __syncthreads();

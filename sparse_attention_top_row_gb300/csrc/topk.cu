@@ -27,10 +27,11 @@
 //    first and hands long rows of small batches to the cluster path):
 //      trivial   L <= k: positions 0..L-1 then -1, scores never read;
 //      register  L <= 8192: the window lives in registers (16-byte loads);
-//                levels 1 and 2 are histogrammed from the registers, the
-//                elements above the 20-bit threshold prefix are written
-//                straight to their slots and the few equal to it are ranked
-//                against each other (every remaining digit at once);
+//                a 14-bit first digit in packed 16-bit counters finds the
+//                threshold bin, the elements above it go to a slot-ordered
+//                list and the few in it are ranked against each other (every
+//                remaining digit at once); the list is written out coalesced.
+//                Very full threshold bins fall back to the 12-bit levels;
 //      streaming longer rows: one pass over HBM builds the level-1 histogram
 //                while collecting into shared memory every element whose top
 //                12 key bits clear a lower bound estimated from the first tile
@@ -468,7 +469,7 @@ struct SoloMerge {
 struct ClusterMerge {
     static constexpr bool kSolo = false;
     // hist (local) -> mhist (sum over the cluster), identical in every CTA.
-    // CTA r sums the 16-byte words w = r, r + 8, ... over all CTAs
+    // CTA r sums the 16-byte words w = r, r + kClusterSize, ... over all CTAs
     // (reduce-scatter); then every CTA gathers the words it does not own.
     __device__ const uint32_t* merge(const Shared& sh, int nb) const {
         cg::cluster_group cluster = cg::this_cluster();

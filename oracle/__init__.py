@@ -50,13 +50,13 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
     with _LOCK:
         if mutant not in _LIBS:
             lib = ctypes.CDLL(build(mutant))
-            fn = lib.oracle_topk_transform
+            fn = lib.oracle_topk_transform_packed
             fn.restype = ctypes.c_int64
             fn.argtypes = [
                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
             ]
             _LIBS[mutant] = lib
         return _LIBS[mutant]
@@ -72,19 +72,23 @@ def _i32(a):
 
 def topk_transform(mode, scores, score_stride, row_starts, seq_lens, k, *,
                    out_offsets=None, page_table=None, page_table_stride=0, page_size=1,
-                   batch=None, mutant: int = 0):
+                   page_table_row_starts=None, row_to_batch=None, batch=None, mutant: int = 0):
     """Run the oracle on host arrays.
 
     ``scores`` is a flat (or any contiguous) float32 array; row ``b``'s window
-    begins at element ``b*score_stride + row_starts[b]``. Returns
-    ``(out, out_raw, n_error_rows)`` with ``out``/``out_raw`` int32 ``[batch, k]``.
-    Selected positions are listed in ascending order, then ``-1`` padding.
+    begins at element ``b*score_stride + row_starts[b]``. PAGED rows may carry
+    the packed layout's ``page_table_row_starts`` and ``row_to_batch``.
+    Returns ``(out, out_raw, n_error_rows)`` with ``out``/``out_raw`` int32
+    ``[batch, k]``. Selected positions are listed in ascending order, then
+    ``-1`` padding.
     """
     scores = np.ascontiguousarray(scores, dtype=np.float32)
     seq_lens = _i32(seq_lens)
     row_starts = _i32(row_starts)
     out_offsets = _i32(out_offsets)
     page_table = _i32(page_table)
+    page_table_row_starts = _i32(page_table_row_starts)
+    row_to_batch = _i32(row_to_batch)
     if batch is None:
         batch = int(seq_lens.shape[0])
     if mode == RAGGED and out_offsets is None:
@@ -93,10 +97,10 @@ def topk_transform(mode, scores, score_stride, row_starts, seq_lens, k, *,
         raise ValueError("PAGED mode needs page_table")
     out = np.empty((batch, k), dtype=np.int32)
     out_raw = np.empty((batch, k), dtype=np.int32)
-    errors = _load(mutant).oracle_topk_transform(
+    errors = _load(mutant).oracle_topk_transform_packed(
         int(mode), _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens),
         _ptr(out_offsets), _ptr(page_table), int(page_table_stride), int(page_size),
-        int(batch), int(k), _ptr(out), _ptr(out_raw))
+        _ptr(page_table_row_starts), _ptr(row_to_batch), int(batch), int(k), _ptr(out), _ptr(out_raw))
     return out, out_raw, int(errors)
 
 
@@ -117,6 +121,8 @@ def run_workload(w, rows=None, mutant: int = 0):
     page_table = host(w.get("page_table"))
     if page_table is not None:
         page_table = page_table.reshape(-1)
+    pt_row_starts = host(w.get("page_table_row_starts"))
+    row_to_batch = host(w.get("row_to_batch"))
     scores = host(w["scores"]).reshape(-1)
     stride = int(w["score_stride"])
     k = int(w["k"])
@@ -125,20 +131,23 @@ def run_workload(w, rows=None, mutant: int = 0):
         return topk_transform(mode, scores, stride, row_starts, seq_lens, k,
                               out_offsets=out_offsets, page_table=page_table,
                               page_table_stride=int(w.get("page_table_stride", 0)),
-                              page_size=int(w.get("page_size", 1)), mutant=mutant)
+                              page_size=int(w.get("page_size", 1)),
+                              page_table_row_starts=pt_row_starts, row_to_batch=row_to_batch, mutant=mutant)
     rows = np.asarray(rows, dtype=np.int64)
     outs, raws, errs = [], [], 0
     for b in rows:
         b = int(b)
         base = b * stride
+        t = b if row_to_batch is None else int(row_to_batch[b])  # the row's page-table row
+        pts = int(w.get("page_table_stride", 0))
         o, r, e = topk_transform(
             mode, scores[base:], 0,
             None if row_starts is None else row_starts[b:b + 1], seq_lens[b:b + 1], k,
             out_offsets=None if out_offsets is None else out_offsets[b:b + 1],
-            page_table=None if page_table is None else
-            page_table[b * int(w["page_table_stride"]):(b + 1) * int(w["page_table_stride"])],
-            page_table_stride=int(w.get("page_table_stride", 0)),
-            page_size=int(w.get("page_size", 1)), mutant=mutant)
+            page_table=None if page_table is None else page_table[t * pts:(t + 1) * pts],
+            page_table_stride=pts, page_size=int(w.get("page_size", 1)),
+            page_table_row_starts=None if pt_row_starts is None else pt_row_starts[b:b + 1],
+            mutant=mutant)
         outs.append(o)
         raws.append(r)
         errs += e

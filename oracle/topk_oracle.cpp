@@ -26,6 +26,16 @@
 //   * PAGED emit: page_table[b * pt_stride + p / page_size] * page_size
 //     + p % page_size (PR #35175 page, TopKProblem::transform_output through
 //     page_to_indices; page_size = 1 << page_bits).
+//   * Packed PAGED emit (oracle_topk_transform_packed): the score window
+//     keeps its batch-global start row_starts[b], while the page-table lookup
+//     uses the row's request table, row r = row_to_batch[b] (b when null), at
+//     the request-local token t = page_table_row_starts[b] + p (p when null):
+//     page_table[r * pt_stride + t / page_size] * page_size + t % page_size
+//     (the PR #33006 report, "fix(dsa): use FlashInfer fused top-k for packed
+//     PAGED rows": "功能与动机", and "实现拆解" item 2 with its snippet, where
+//     page_table_row_starts = row_starts - cu_seqlens_k[row_to_batch]).
+//     A negative page_table_row_starts[b] is a data error like a negative
+//     row_start.
 //   * Slots past the selected count hold -1, never biased or transformed
 //     (PR #35175 page, "Review highlights": the trivial path cannot reuse a
 //     helper whose -1 padding would pick up the bias).
@@ -99,20 +109,29 @@ extern "C" {
 
 // mode: 0 = RAGGED (out_offsets used), 1 = PAGED (page_table used).
 // scores: host fp32; row b's window starts at scores + b*score_stride + row_start.
+// page_table_row_starts, row_to_batch: PAGED only, may be null (packed PAGED).
 // out, out_raw: [batch, k] int32 (out_raw may be null).
-// Returns the number of rows with a data error (seq_len < 0 or row_start < 0).
-int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_stride,
-                              const int32_t* row_starts, const int32_t* seq_lens,
-                              const int32_t* out_offsets, const int32_t* page_table,
-                              int64_t page_table_stride, int32_t page_size, int32_t batch,
-                              int32_t k, int32_t* out, int32_t* out_raw) {
+// Returns the number of rows with a data error (seq_len < 0, row_start < 0 or
+// page_table_row_start < 0).
+int64_t oracle_topk_transform_packed(int32_t mode, const float* scores, int64_t score_stride,
+                                     const int32_t* row_starts, const int32_t* seq_lens,
+                                     const int32_t* out_offsets, const int32_t* page_table,
+                                     int64_t page_table_stride, int32_t page_size,
+                                     const int32_t* page_table_row_starts, const int32_t* row_to_batch,
+                                     int32_t batch, int32_t k, int32_t* out, int32_t* out_raw) {
     int64_t errors = 0;
     std::vector<Entry> window;
     std::vector<int32_t> selected;
     for (int32_t b = 0; b < batch; ++b) {
         int32_t L = seq_lens[b];
         const int32_t start = row_starts ? row_starts[b] : 0;
-        if (L < 0 || start < 0) {
+#if ORACLE_MUTANT == 7
+        const int32_t token0 = 0;  // mutant: the packed page-table start is ignored
+#else
+        const int32_t token0 = (mode == 1 && page_table_row_starts) ? page_table_row_starts[b] : 0;
+#endif
+        const int64_t table_row = (mode == 1 && row_to_batch) ? row_to_batch[b] : b;
+        if (L < 0 || start < 0 || token0 < 0) {
             ++errors;
             L = 0;
         }
@@ -144,7 +163,7 @@ int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_s
             if (t < (int32_t)selected.size()) {
                 raw = selected[t];
                 if (mode == 1)
-                    value = paged_index(page_table + (int64_t)b * page_table_stride, page_size, raw);
+                    value = paged_index(page_table + table_row * page_table_stride, page_size, token0 + raw);
                 else
                     value = ragged_index(raw, out_offsets[b]);
             }
@@ -158,6 +177,17 @@ int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_s
         }
     }
     return errors;
+}
+
+// The plain form: every page-table lookup in the row's own table from token 0.
+int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_stride,
+                              const int32_t* row_starts, const int32_t* seq_lens,
+                              const int32_t* out_offsets, const int32_t* page_table,
+                              int64_t page_table_stride, int32_t page_size, int32_t batch,
+                              int32_t k, int32_t* out, int32_t* out_raw) {
+    return oracle_topk_transform_packed(mode, scores, score_stride, row_starts, seq_lens, out_offsets,
+                                        page_table, page_table_stride, page_size, nullptr, nullptr, batch, k,
+                                        out, out_raw);
 }
 
 }  // extern "C"

@@ -21,6 +21,10 @@ A workload is a plain dict:
     out_offsets     int32 [B] (RAGGED) or None
     page_table      int32 [B, P] (PAGED) or None
     page_table_stride, page_size
+    page_table_row_starts, row_to_batch
+                    int32 [B] or absent (packed PAGED: the page-table lookup
+                    of row b starts at request-local token
+                    page_table_row_starts[b] of table row row_to_batch[b])
     batch           B
     name            short description
 
@@ -138,6 +142,45 @@ def paged_long(device="cpu", sub_id=0, batch=1, seq_len=131072, k=2048, page_siz
                 page_size=page_size, batch=batch)
 
 
+def paged_packed(device="cpu", sub_id=0, n_req=4, q_rows=4, min_tokens=12000, max_tokens=40000, window=16384,
+                 k=2048, page_size=64):
+    """Packed PAGED rows (multi-query extend): ``n_req`` requests, the last
+    ``q_rows`` tokens of each a query row.
+
+    Request r holds T_r ~ U{min_tokens..max_tokens} tokens and its own page
+    table row (a seeded random permutation over all requests' pages). Every
+    query row's scores live in one flattened key space of all requests
+    (stride = sum T_r): request r's keys at batch-global offset cu[r], N(0,1)
+    there, the 1e3 sentinel elsewhere. Query token i of request r sees the
+    sliding window of request-local tokens [max(0, i + 1 - window), i], so
+    page_table_row_starts = that start, row_starts = cu[r] + the start,
+    seq_len = its length, row_to_batch = r.
+    """
+    g = _gen(device, seed_for(6, sub_id))
+    T = torch.randint(min_tokens, max_tokens + 1, (n_req,), generator=g, device=device)
+    cu = torch.zeros(n_req + 1, dtype=torch.int64, device=device)
+    cu[1:] = torch.cumsum(T, 0)
+    stride = (int(cu[-1].item()) + 3) // 4 * 4
+    B = n_req * q_rows
+    rtb = torch.arange(n_req, device=device).repeat_interleave(q_rows)
+    qi = torch.arange(q_rows, device=device).repeat(n_req)
+    tok = T[rtb] - q_rows + qi                       # request-local token of each query
+    pt_start = torch.clamp(tok + 1 - window, min=0)
+    seq_lens = tok + 1 - pt_start
+    row_starts = cu[:-1][rtb] + pt_start
+    scores = torch.full((B, stride), SENTINEL, dtype=torch.float32, device=device)
+    for b in range(B):
+        r = int(rtb[b].item())
+        a, e = int(cu[r].item()), int(cu[r + 1].item())
+        scores[b, a:e] = torch.randn(e - a, generator=g, device=device)
+    pages = (int(T.max().item()) + page_size - 1) // page_size
+    table = torch.randperm(n_req * pages, generator=g, device=device).view(n_req, pages)
+    return dict(name=f"paged packed {n_req} requests x {q_rows} queries k={k}", mode="paged", k=k,
+                scores=scores, score_stride=stride, row_starts=_i32(row_starts), seq_lens=_i32(seq_lens),
+                out_offsets=None, page_table=_i32(table), page_table_stride=pages, page_size=page_size,
+                page_table_row_starts=_i32(pt_start), row_to_batch=_i32(rtb), batch=B)
+
+
 BOUNDARY_LENGTHS = (8192, 8193, 16384, 16385, 65535, 65536, 65537)
 
 
@@ -253,9 +296,9 @@ def select_rows(w, rows):
     out = dict(w)
     out.update(scores=scores, batch=len(rows), seq_lens=w["seq_lens"][idx].clone(),
                name=w["name"] + f" rows={rows[:4]}...")
-    for key in ("row_starts", "out_offsets"):
+    for key in ("row_starts", "out_offsets", "page_table_row_starts", "row_to_batch"):
         if w.get(key) is not None:
             out[key] = w[key][idx].clone()
-    if w.get("page_table") is not None:
-        out["page_table"] = w["page_table"][idx].clone()
+    if w.get("page_table") is not None and w.get("row_to_batch") is None:
+        out["page_table"] = w["page_table"][idx].clone()  # packed rows keep the request tables
     return out

@@ -38,8 +38,12 @@ def _golden_workload(case):
                     out_offsets=torch.tensor(case["out_offsets"], dtype=torch.int32),
                     page_table=None, page_table_stride=0, page_size=1,
                     batch=len(case["seq_lens"]), name=case["name"])
-    return wl.custom(mode, case["k"], case["rows"], page_size=case.get("page_size", 1),
-                     page_table=case.get("page_table"))
+    w = wl.custom(mode, case["k"], case["rows"], page_size=case.get("page_size", 1),
+                  page_table=case.get("page_table"))
+    for key in ("page_table_row_starts", "row_to_batch"):  # packed PAGED cases
+        if key in case:
+            w[key] = torch.tensor(case[key], dtype=torch.int32)
+    return w
 
 
 def golden_cases():
@@ -143,6 +147,29 @@ def pin_paged_expansion(mutant=0, seed=4):
             assert [inv[int(s)] for s in out[b]] == raw[b].tolist()
 
 
+def pin_packed_expansion(mutant=0, seed=9):
+    """Packed PAGED rows: each output is the request table, expanded slot by
+    slot, read at page_table_row_starts + p (an expansion written here, not
+    the oracle's division); with both arrays absent the plain PAGED result."""
+    for ps in (1, 16, 64):
+        w = wl.paged_packed("cpu", sub_id=ps, n_req=3, q_rows=3, min_tokens=600, max_tokens=1500,
+                            window=700, k=50, page_size=ps)
+        out, raw, err = oracle.run_workload(w, mutant=mutant)
+        assert err == 0
+        pt = w["page_table"].numpy()
+        ptrs, rtb = w["page_table_row_starts"].numpy(), w["row_to_batch"].numpy()
+        for b in range(w["batch"]):
+            phys = expand_page_table(pt[rtb[b]], ps, int(ptrs[b]) + int(w["seq_lens"][b]))
+            np.testing.assert_array_equal(out[b], phys[int(ptrs[b]) + raw[b]])
+        plain = dict(w, page_table_row_starts=None, row_to_batch=None)
+        plain["page_table"] = w["page_table"][w["row_to_batch"].long()]
+        out2, raw2, _ = oracle.run_workload(plain, mutant=mutant)
+        np.testing.assert_array_equal(raw2, raw)
+        if ps == 1:  # token t of a request is slot pt[r][t]: shifting the start shifts the slots
+            for b in range(w["batch"]):
+                np.testing.assert_array_equal(out[b], pt[rtb[b]][int(ptrs[b]) + raw[b]])
+
+
 def pin_invariants(mutant=0):
     cases = [
         wl.ragged_tiny("cpu", sub_id=0),
@@ -151,6 +178,7 @@ def pin_invariants(mutant=0):
         wl.paged_long("cpu", batch=2, seq_len=8192, k=512),
         wl.mixed("cpu", mode="ragged", k=64, batch=12, max_len=4000, min_len=16),
         wl.mixed("cpu", mode="paged", k=64, batch=12, max_len=4000, min_len=16),
+        wl.paged_packed("cpu", n_req=2, q_rows=3, min_tokens=500, max_tokens=2000, window=900, k=100),
     ]
     for w in cases:
         hw = HostWorkload(w)
@@ -162,7 +190,8 @@ def pin_invariants(mutant=0):
         np.testing.assert_array_equal(hw.scores.view(np.uint32), before.view(np.uint32))
 
 
-PINS = [pin_golden, pin_bruteforce, pin_exhaustive, pin_partition, pin_paged_expansion, pin_invariants]
+PINS = [pin_golden, pin_bruteforce, pin_exhaustive, pin_partition, pin_paged_expansion, pin_packed_expansion,
+        pin_invariants]
 
 
 # ------------------------------------------------------------------ tests
@@ -185,7 +214,7 @@ def test_error_rows_are_empty_and_counted():
 
 def test_planted_mistakes_are_caught():
     """Each planted mistake in the oracle fails at least one pin family."""
-    for mutant in range(1, 7):
+    for mutant in range(1, 8):
         caught = []
         for pin in PINS:
             try:

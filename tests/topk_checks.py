@@ -68,6 +68,10 @@ class HostWorkload:
         pt = w.get("page_table")
         self.page_table = None if pt is None else host(pt).reshape(-1).astype(np.int64)
         self.pt_stride = int(w.get("page_table_stride", 0))
+        ptrs = w.get("page_table_row_starts")
+        self.pt_row_starts = None if ptrs is None else host(ptrs).astype(np.int64)
+        rtb = w.get("row_to_batch")
+        self.row_to_batch = None if rtb is None else host(rtb).astype(np.int64)
         self.page_size = int(w.get("page_size", 1))
         self.batch = int(w["batch"])
 
@@ -85,9 +89,12 @@ class HostWorkload:
     def transform(self, b, raw):
         raw = np.asarray(raw, dtype=np.int64)
         if self.mode == "paged":
-            row = self.page_table[b * self.pt_stride:(b + 1) * self.pt_stride]
-            phys = expand_page_table(row, self.page_size, max(self.length(b), 1))
-            return phys[raw]
+            # packed rows: table row row_to_batch[b], tokens from page_table_row_starts[b]
+            t = b if self.row_to_batch is None else int(self.row_to_batch[b])
+            t0 = 0 if self.pt_row_starts is None else int(self.pt_row_starts[b])
+            row = self.page_table[t * self.pt_stride:(t + 1) * self.pt_stride]
+            phys = expand_page_table(row, self.page_size, t0 + max(self.length(b), 1))
+            return phys[t0 + raw]
         return raw + self.out_offsets[b]
 
 

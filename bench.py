@@ -173,6 +173,8 @@ def make_workload(name, device, rank=0):
         return [wl.ragged_extend(device, chunk=c) for c in range(16)]
     if name == "ragged_extend_chunk":  # one 1024-row chunk (profiling size)
         return [wl.ragged_extend(device, chunk=0)]
+    if name == "paged_packed":  # packed PAGED extend rows: 8 requests x 16 queries, sliding window 16384
+        return [wl.paged_packed(device, sub_id=rank, n_req=8, q_rows=16)]
     if name.startswith("paged_long_b"):
         b = int(name[len("paged_long_b"):])
         return [wl.paged_long(device, batch=b, sub_id=b + 100 * rank)]
@@ -194,11 +196,15 @@ def algorithmic_bytes(w, out_raw):
     nontrivial = lens > k
     scores = int((4 * lens[nontrivial]).sum().item())
     out = 4 * k * int(w["batch"])
-    meta = 4 * int(w["batch"]) * (1 + (w.get("row_starts") is not None) + (w["mode"] == "ragged"))
+    packed = [w.get(key) for key in ("page_table_row_starts", "row_to_batch")]
+    meta = 4 * int(w["batch"]) * (1 + (w.get("row_starts") is not None) + (w["mode"] == "ragged") +
+                                  sum(a is not None for a in packed))
     pages = 0
     if w["mode"] == "paged":
         ps = int(w["page_size"])
         r = out_raw.to(torch.int64)
+        if packed[0] is not None:  # packed rows read their tables from token page_table_row_starts[b]
+            r = torch.where(r >= 0, r + packed[0].to(torch.int64)[:, None], r)
         pg = torch.where(r >= 0, r // ps, torch.full_like(r, -1))
         srt, _ = torch.sort(pg, dim=1)
         distinct = ((srt[:, 1:] != srt[:, :-1]) & (srt[:, 1:] >= 0)).sum(1) + (srt[:, 0] >= 0).to(torch.int64)
@@ -221,7 +227,12 @@ class Launch:
 
     def transform(self, stream, out_raw=None):
         w = self.w
-        if w["mode"] == "paged":
+        if w["mode"] == "paged" and w.get("row_to_batch") is not None:
+            topk.topk_transform_paged_packed(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                                             w["page_table"], w["page_table_stride"], w["page_size"],
+                                             w.get("page_table_row_starts"), w["row_to_batch"], self.k,
+                                             self.ws, self.out, out_raw, self.flags, stream=stream)
+        elif w["mode"] == "paged":
             topk.topk_transform_paged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                                       w["page_table"], w["page_table_stride"], w["page_size"], self.k,
                                       self.ws, self.out, out_raw, self.flags, stream=stream)
@@ -448,7 +459,8 @@ def main():
     if not args.no_configs:
         for name, steps in (("ragged_tiny", args.steps), ("ragged_extend", max(3, args.steps // 10)),
                             ("paged_long_b1", args.steps), ("paged_long_b30", args.steps),
-                            ("paged_long_b31", args.steps), ("mixed", max(3, args.steps // 10))):
+                            ("paged_long_b31", args.steps), ("paged_packed", args.steps),
+                            ("mixed", max(3, args.steps // 10))):
             extra[name] = measure(name, steps, args.warmup if name != "ragged_extend" else 3,
                                   world, rank, stream, peak)
 

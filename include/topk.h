@@ -150,6 +150,33 @@ TOPK_API int topk_transform_paged(const float* scores, int64_t score_stride,
                                   uint32_t flags, topk_stream_t stream);
 
 /*
+ * PAGED top-k + page-table transform for packed rows (multi-query extend):
+ * the score window keeps its batch-global start row_starts[b] while the
+ * page-table lookup uses the row's request table and a request-local token
+ * offset (the PR #33006 report, "fix(dsa): use FlashInfer fused top-k for
+ * packed PAGED rows": "功能与动机" and "实现拆解" item 2, where
+ * page_table_row_starts = row_starts - cu_seqlens_k[row_to_batch]).
+ * A selected position p of row b writes
+ *   page_table[r * page_table_stride + t / page_size] * page_size + t % page_size
+ * with r = row_to_batch[b] and t = page_table_row_starts[b] + p.
+ * Arguments as for topk_transform_paged, plus
+ *   page_table_row_starts  int32 [batch] or NULL (0 for every row); a
+ *                          negative entry is a data error (the row comes out
+ *                          all -1 and the device error count goes up).
+ *   row_to_batch           int32 [batch] or NULL (row b uses table row b);
+ *                          caller's contract: each entry names a table row.
+ * The page table must hold the entries t / page_size for every t of every
+ * window. With both arrays NULL this is topk_transform_paged.
+ */
+TOPK_API int topk_transform_paged_packed(const float* scores, int64_t score_stride,
+                                         const int32_t* row_starts, const int32_t* seq_lens,
+                                         const int32_t* page_table, int64_t page_table_stride,
+                                         int32_t page_size, const int32_t* page_table_row_starts,
+                                         const int32_t* row_to_batch, int32_t batch, int32_t k,
+                                         void* workspace, size_t workspace_bytes, int32_t* out,
+                                         int32_t* out_raw, uint32_t flags, topk_stream_t stream);
+
+/*
  * RAGGED top-k + offset transform (prefill / extend).
  * Counterpart of topk_transform_ragged_v2 / topk_ragged_kernel (PR #35175
  * page, "Implementation breakdown" items 2-3 and "Key source snippets").

@@ -29,8 +29,9 @@ _LOCK = threading.Lock()
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
 
-EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_ragged",
-            "topk_read_device_errors", "topk_status_string", "topk_transform_ragged_noalloc")
+EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_paged_packed",
+            "topk_transform_ragged", "topk_read_device_errors", "topk_status_string",
+            "topk_transform_ragged_noalloc")
 TOPK_NOALLOC_MAX_BATCH = 16384
 
 
@@ -61,6 +62,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.topk_transform_paged.restype = ctypes.c_int
         lib.topk_transform_paged.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_i32,
                                              c_p, c_sz, c_p, c_p, c_u32, c_p]
+        lib.topk_transform_paged_packed.restype = ctypes.c_int
+        lib.topk_transform_paged_packed.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i64, c_i32, c_p, c_p, c_i32, c_i32,
+                                                    c_p, c_sz, c_p, c_p, c_u32, c_p]
         lib.topk_transform_ragged.restype = ctypes.c_int
         lib.topk_transform_ragged.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32,
                                               c_p, c_sz, c_p, c_p, c_u32, c_p]
@@ -118,6 +122,18 @@ def topk_transform_paged(scores, score_stride: int, row_starts, seq_lens, page_t
         _stream(stream)))
 
 
+def topk_transform_paged_packed(scores, score_stride: int, row_starts, seq_lens, page_table,
+                                page_table_stride: int, page_size: int, page_table_row_starts, row_to_batch,
+                                k: int, workspace, out, out_raw=None, flags: int = 0, stream=None):
+    lib = load()
+    batch = int(seq_lens.numel())
+    _check("topk_transform_paged_packed", lib.topk_transform_paged_packed(
+        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(page_table),
+        int(page_table_stride), int(page_size), _ptr(page_table_row_starts), _ptr(row_to_batch), batch, int(k),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_raw), int(flags),
+        _stream(stream)))
+
+
 def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int,
                           workspace, out, out_raw=None, flags: int = 0, stream=None):
     lib = load()
@@ -162,7 +178,12 @@ def run_workload(w, out=None, out_raw=None, workspace=None, flags: int = 0, plan
         workspace = new_workspace(B, dev)
     if plan:
         topk_plan(w["seq_lens"], k, workspace, stream=stream)
-    if w["mode"] == "paged":
+    if w["mode"] == "paged" and (w.get("page_table_row_starts") is not None or w.get("row_to_batch") is not None):
+        topk_transform_paged_packed(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                                    w["page_table"], w["page_table_stride"], w["page_size"],
+                                    w.get("page_table_row_starts"), w.get("row_to_batch"), k, workspace,
+                                    out, out_raw, flags, stream=stream)
+    elif w["mode"] == "paged":
         topk_transform_paged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                              w["page_table"], w["page_table_stride"], w["page_size"], k, workspace,
                              out, out_raw, flags, stream=stream)

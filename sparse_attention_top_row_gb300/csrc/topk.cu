@@ -171,6 +171,8 @@ struct Params {
     PlanHeader* hdr;
     const int32_t* order;
     const int32_t* cluster_rows;
+    const int32_t* pt_row_starts;  // packed PAGED: request-local token of each row's position 0, or null
+    const int32_t* row_to_batch;   // packed PAGED: each row's page-table row, or null
 };
 
 // ----------------------------------------------------------------------------
@@ -644,8 +646,10 @@ template <bool kPaged>
 struct Emitter {
     int32_t* out;
     int32_t* out_raw;
-    const int32_t* pt_row;
-    const int32_t* pt_cached;  // the row's page-table entries in shared memory, or null
+    const int32_t* pt_row;     // the row's page-table row (packed rows: its request's)
+    const int32_t* pt_cached;  // the row's page-table entries from pt_first on, in shared memory, or null
+    int32_t token0;            // page-table token of position 0 (0 unless packed)
+    int32_t pt_first;          // first page-table entry the window touches
     int32_t page_bits;
     int32_t offset;
     uint32_t k;
@@ -657,8 +661,9 @@ struct Emitter {
         }
         int32_t v;
         if (kPaged) {
-            const int32_t page = pt_cached ? pt_cached[pos >> page_bits] : __ldg(pt_row + (pos >> page_bits));
-            v = (page << page_bits) | (pos & ((1 << page_bits) - 1));
+            const int32_t t = pos + token0;
+            const int32_t page = pt_cached ? pt_cached[(t >> page_bits) - pt_first] : __ldg(pt_row + (t >> page_bits));
+            v = (page << page_bits) | (t & ((1 << page_bits) - 1));
         } else {
             v = pos + offset;
         }
@@ -672,9 +677,10 @@ struct Emitter {
         const bool ok = w && slot < k;
         int32_t v;
         if (kPaged) {
-            const int32_t q = ok ? (pos >> page_bits) : 0;  // entry 0 exists: the row is not empty
-            const int32_t page = pt_cached ? pt_cached[q] : __ldg(pt_row + q);
-            v = (page << page_bits) | (pos & ((1 << page_bits) - 1));
+            const int32_t t = pos + token0;
+            const int32_t q = ok ? (t >> page_bits) : pt_first;  // pt_first exists: the row is not empty
+            const int32_t page = pt_cached ? pt_cached[q - pt_first] : __ldg(pt_row + q);
+            v = (page << page_bits) | (t & ((1 << page_bits) - 1));
         } else {
             v = pos + offset;
         }
@@ -1309,12 +1315,15 @@ __device__ __forceinline__ bool plan_matches(const Params& p) {
 }
 
 template <bool kPaged>
-__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, int32_t offset) {
+__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, int32_t offset, int32_t table_row,
+                                                        int32_t token0) {
     Emitter<kPaged> em;
     em.out = p.out + static_cast<int64_t>(b) * p.k;
     em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
-    em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(b) * p.page_table_stride : nullptr;
+    em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(table_row) * p.page_table_stride : nullptr;
     em.pt_cached = nullptr;
+    em.token0 = token0;
+    em.pt_first = kPaged ? (token0 >> p.page_bits) : 0;
     em.page_bits = p.page_bits;
     em.offset = offset;
     em.k = static_cast<uint32_t>(p.k);
@@ -1322,17 +1331,19 @@ __device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, 
     return em;
 }
 
-// PAGED, non-trivial row: starts asynchronous copies of the row's page-table
-// entries 0..ceil(len / page_size)-1 (each one a page some window position
-// maps to) into shared memory when they fit; emit_selected waits for them.
+// PAGED, non-trivial row: starts asynchronous copies of the page-table
+// entries its window's tokens token0 .. token0 + len - 1 map to (each one a
+// page some window position maps to) into shared memory when they fit; the
+// emit waits for them.
 template <bool kPaged>
 __device__ __forceinline__ void prefetch_pages(Emitter<kPaged>& em, int32_t len, const Shared& sh) {
     if (!kPaged) return;
-    const int n = ((len - 1) >> em.page_bits) + 1;
+    const int n = ((em.token0 + len - 1) >> em.page_bits) - em.pt_first + 1;
     if (n > kPageCache) return;
     for (int i = threadIdx.x; i < n; i += kThreads) {
         const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sh.pages + i));
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(em.pt_row + i) : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(em.pt_row + em.pt_first + i)
+                     : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     em.pt_cached = sh.pages;
@@ -1358,6 +1369,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
     const int32_t len0 = p.seq_lens[b0];
     const int32_t start0 = p.row_starts ? p.row_starts[b0] : 0;
     const int32_t off0 = kPaged ? 0 : p.out_offsets[b0];
+    const int32_t table0 = (kPaged && p.row_to_batch) ? p.row_to_batch[b0] : b0;
+    const int32_t token00 = (kPaged && p.pt_row_starts) ? p.pt_row_starts[b0] : 0;
     const bool planned = magic == kPlanMagic && h_batch == p.batch && h_k == p.k;
     if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
     int b = b0;
@@ -1371,13 +1384,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
     int32_t len = same ? len0 : p.seq_lens[b];
     const int32_t start = same ? start0 : (p.row_starts ? p.row_starts[b] : 0);
     const int32_t offset = kPaged ? 0 : (same ? off0 : p.out_offsets[b]);
-    if (len < 0 || start < 0) {
+    const int32_t table_row = same ? table0 : ((kPaged && p.row_to_batch) ? p.row_to_batch[b] : b);
+    const int32_t token0 = same ? token00 : ((kPaged && p.pt_row_starts) ? p.pt_row_starts[b] : 0);
+    if (len < 0 || start < 0 || token0 < 0) {
         // seq_len < 0 was counted by the plan; count the rest here
         if (threadIdx.x == 0 && (!planned || len >= 0)) atomicAdd(&p.hdr->error_rows, 1u);
         len = 0;
     }
     const uint32_t k = static_cast<uint32_t>(p.k);
-    Emitter<kPaged> em = make_emitter<kPaged>(p, b, offset);
+    Emitter<kPaged> em = make_emitter<kPaged>(p, b, offset, table_row, token0 < 0 ? 0 : token0);
     if (len <= p.k) {
         trivial_row<kPaged>(len, k, em);
         return;
@@ -1420,11 +1435,15 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         const int b = p.cluster_rows[i];
         int32_t len = p.seq_lens[b];
         const int32_t start = p.row_starts ? p.row_starts[b] : 0;
-        if (len < 0 || start < 0) {
-            if (rank == 0 && threadIdx.x == 0 && start < 0) atomicAdd(&p.hdr->error_rows, 1u);
+        const int32_t table_row = (kPaged && p.row_to_batch) ? p.row_to_batch[b] : b;
+        const int32_t token0 = (kPaged && p.pt_row_starts) ? p.pt_row_starts[b] : 0;
+        if (len < 0 || start < 0 || token0 < 0) {
+            // seq_len < 0 was counted by the plan (cluster rows have seq_len > 32768)
+            if (rank == 0 && threadIdx.x == 0 && len >= 0) atomicAdd(&p.hdr->error_rows, 1u);
             len = 0;
         }
-        Emitter<kPaged> em = make_emitter<kPaged>(p, b, kPaged ? 0 : p.out_offsets[b]);
+        Emitter<kPaged> em =
+            make_emitter<kPaged>(p, b, kPaged ? 0 : p.out_offsets[b], table_row, token0 < 0 ? 0 : token0);
         if (len <= p.k) {
             if (rank == 0) trivial_row<kPaged>(len, k, em);
             cluster.sync();
@@ -1679,11 +1698,12 @@ int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }
 
-int topk_transform_paged(const float* scores, int64_t score_stride, const int32_t* row_starts,
-                         const int32_t* seq_lens, const int32_t* page_table, int64_t page_table_stride,
-                         int32_t page_size, int32_t batch, int32_t k, void* workspace,
-                         size_t workspace_bytes, int32_t* out, int32_t* out_raw, uint32_t flags,
-                         topk_stream_t stream) {
+int topk_transform_paged_packed(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                                const int32_t* seq_lens, const int32_t* page_table, int64_t page_table_stride,
+                                int32_t page_size, const int32_t* page_table_row_starts,
+                                const int32_t* row_to_batch, int32_t batch, int32_t k, void* workspace,
+                                size_t workspace_bytes, int32_t* out, int32_t* out_raw, uint32_t flags,
+                                topk_stream_t stream) {
     const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out, flags);
     if (st != TOPK_OK) return st;
     if (page_size < 1 || page_size > TOPK_MAX_PAGE_SIZE || (page_size & (page_size - 1)) != 0)
@@ -1693,10 +1713,22 @@ int topk_transform_paged(const float* scores, int64_t score_stride, const int32_
     Params p = make_params(scores, score_stride, row_starts, seq_lens, batch, k, workspace, out, out_raw, flags);
     p.page_table = page_table;
     p.page_table_stride = page_table_stride;
+    p.pt_row_starts = page_table_row_starts;
+    p.row_to_batch = row_to_batch;
     int bits = 0;
     while ((1 << bits) < page_size) ++bits;
     p.page_bits = bits;
     return launch_transform<true>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topk_transform_paged(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                         const int32_t* seq_lens, const int32_t* page_table, int64_t page_table_stride,
+                         int32_t page_size, int32_t batch, int32_t k, void* workspace,
+                         size_t workspace_bytes, int32_t* out, int32_t* out_raw, uint32_t flags,
+                         topk_stream_t stream) {
+    return topk_transform_paged_packed(scores, score_stride, row_starts, seq_lens, page_table, page_table_stride,
+                                       page_size, nullptr, nullptr, batch, k, workspace, workspace_bytes, out,
+                                       out_raw, flags, stream);
 }
 
 int topk_transform_ragged(const float* scores, int64_t score_stride, const int32_t* row_starts,

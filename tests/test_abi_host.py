@@ -86,6 +86,17 @@ def test_transform_validation(lib):
     assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 4096, FAKE, ws, FAKE, None, 0, None) == 3
     assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 16, None, ws, FAKE, None, 0, None) == 5
     assert ragged(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, None, 3, None) == 1
+    packed = lib.topk_transform_paged_packed
+    # scores, stride, row_starts, seq_lens, page_table, pt_stride, page_size, pt_row_starts, row_to_batch,
+    # batch, k, ws, ws_bytes, out, out_raw, flags, stream
+    assert packed(FAKE, 64, None, FAKE, FAKE, 4, 64, FAKE, FAKE, 8, 0, FAKE, ws, FAKE, None, 0, None) == 3
+    assert packed(FAKE, 64, None, FAKE, FAKE, 4, 48, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, None, 0, None) == 4
+    assert packed(FAKE, 64, None, FAKE, None, 4, 64, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, None, 0, None) == 1
+    assert packed(FAKE_UNALIGNED, 64, None, FAKE, FAKE, 4, 64, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, None, 0, None) == 2
+    assert packed(FAKE, 64, None, FAKE, FAKE, 4, 64, FAKE, FAKE, 8, 16, FAKE, ws - 1, FAKE, None, 0, None) == 5
+    assert packed(FAKE, 64, None, FAKE, FAKE, 4, 64, None, None, 8, 16, FAKE, ws, FAKE, None, 4, None) == 1
+    assert packed(None, 0, None, None, None, 0, 1, None, None, 0, 16, FAKE, lib.topk_workspace_bytes(0),
+                  None, None, 0, None) == 0
     # an empty batch is a no-op that enqueues nothing
     assert ragged(None, 0, None, None, None, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, None, 0, None) == 0
     assert paged(None, 0, None, None, None, 0, 1, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, None, 0, None) == 0

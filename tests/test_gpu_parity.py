@@ -42,8 +42,11 @@ def assert_windows_in_bounds(w):
         hi = lo + 4 * ((L + rem + 3) // 4)
         assert 0 <= lo and hi <= n, f"row {b}: window [{lo}, {hi}) outside the {n}-element buffer"
         if hw.mode == "paged":
-            need = (L + hw.page_size - 1) // hw.page_size
-            assert b * hw.pt_stride + need <= hw.page_table.size, f"row {b}: page table too short"
+            t = b if hw.row_to_batch is None else int(hw.row_to_batch[b])
+            t0 = 0 if hw.pt_row_starts is None else max(int(hw.pt_row_starts[b]), 0)
+            need = (t0 + L + hw.page_size - 1) // hw.page_size
+            assert need <= hw.pt_stride or hw.row_to_batch is None, f"row {b}: page-table row too short"
+            assert t * hw.pt_stride + need <= hw.page_table.size, f"row {b}: page table too short"
 
 
 def run_gpu(topk, w, flags, raw=True):
@@ -222,6 +225,40 @@ def test_small_tie_lists(cuda_lib, k):
         v[idx] = thr  # the k-th largest value now occurs reps (+1) times
         rows.append(v.tolist())
     w = wl.custom("paged", k, rows, page_size=16, seed=k)
+    check_full(cuda_lib, w)
+
+
+@pytest.mark.parametrize("window,page_size", [(6000, 64), (16384, 16), (40000, 64), (20000, 1)])
+def test_packed_paged_rows(cuda_lib, window, page_size):
+    """Packed PAGED rows (topk_transform_paged_packed): batch-global score
+    windows, request-local page-table starts, shared request tables; windows
+    that put rows on the register, streaming and cluster routes."""
+    w = wl.paged_packed("cpu", sub_id=window + page_size, n_req=3, q_rows=4, min_tokens=window // 2,
+                        max_tokens=window + 9000, window=window, k=2048, page_size=page_size)
+    check_full(cuda_lib, w)
+
+
+def test_packed_paged_without_arrays_is_plain_paged(cuda_lib):
+    """With neither packed array the packed entry point is the PAGED one."""
+    w = wl.paged_decode("cpu", batch=6, seq_len=9000, k=700)
+    d = wl.to_device(w, "cuda")
+    ws = cuda_lib.new_workspace(6)
+    cuda_lib.topk_plan(d["seq_lens"], 700, ws)
+    a = torch.empty((6, 700), dtype=torch.int32, device="cuda")
+    b = torch.empty_like(a)
+    cuda_lib.topk_transform_paged(d["scores"], d["score_stride"], None, d["seq_lens"], d["page_table"],
+                                  d["page_table_stride"], d["page_size"], 700, ws, a, flags=DET)
+    cuda_lib.topk_transform_paged_packed(d["scores"], d["score_stride"], None, d["seq_lens"], d["page_table"],
+                                         d["page_table_stride"], d["page_size"], None, None, 700, ws, b, flags=DET)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.sort(a, dim=1).values, torch.sort(b, dim=1).values)
+
+
+def test_packed_negative_table_start_is_a_data_error(cuda_lib):
+    w = wl.paged_packed("cpu", sub_id=5, n_req=2, q_rows=3, min_tokens=3000, max_tokens=5000, window=4000,
+                        k=512, page_size=64)
+    w["page_table_row_starts"] = w["page_table_row_starts"].clone()
+    w["page_table_row_starts"][2] = -1
     check_full(cuda_lib, w)
 
 

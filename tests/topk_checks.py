@@ -80,7 +80,8 @@ class HostWorkload:
 
     def length(self, b):
         L = int(self.seq_lens[b])
-        return 0 if (L < 0 or self.start(b) < 0) else L
+        bad_table_start = self.pt_row_starts is not None and int(self.pt_row_starts[b]) < 0
+        return 0 if (L < 0 or self.start(b) < 0 or bad_table_start) else L
 
     def window(self, b):
         base = b * self.stride + self.start(b)

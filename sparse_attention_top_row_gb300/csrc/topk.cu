@@ -1491,10 +1491,11 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
     if (tid == 0) n_err = 0;
     __syncthreads();
     const bool allow_cluster = batch <= kClusterMaxBatch;
-    const int n_iter = (batch + kPlanThreads - 1) / kPlanThreads;
+    const int nt = static_cast<int>(blockDim.x);  // a multiple of 32, at least 64
+    const int n_iter = (batch + nt - 1) / nt;
     const uint32_t lt = lanemask_lt();
     for (int it = 0; it < n_iter; ++it) {
-        const int i = it * kPlanThreads + tid;
+        const int i = it * nt + tid;
         const bool valid = i < batch;
         const int32_t len = valid ? seq_lens[i] : 0;
         const uint32_t merr = __ballot_sync(kFull, valid && len < 0);
@@ -1530,11 +1531,11 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
     }
     __syncthreads();
     if (in_place) {
-        for (int i = tid; i < batch; i += kPlanThreads) order[i] = i;
+        for (int i = tid; i < batch; i += nt) order[i] = i;
         return;
     }
     for (int it = 0; it < n_iter; ++it) {
-        const int i = it * kPlanThreads + tid;
+        const int i = it * nt + tid;
         const bool valid = i < batch;
         const int32_t len = valid ? seq_lens[i] : 0;
         const int band = valid ? band_of(max(len, 0), k, allow_cluster) : kBands;
@@ -1693,7 +1694,9 @@ int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace
     if (workspace == nullptr || workspace_bytes < workspace_bytes_for(batch)) return TOPK_ERR_WORKSPACE;
     PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + sizeof(PlanHeader));
-    const cudaError_t e = launch_pdl(topk_plan_kernel, 1, kPlanThreads, 0, reinterpret_cast<cudaStream_t>(stream),
+    // one thread per row up to kPlanThreads (small batches get a small block)
+    const int threads = min(kPlanThreads, max(64, (batch + 31) / 32 * 32));
+    const cudaError_t e = launch_pdl(topk_plan_kernel, 1, threads, 0, reinterpret_cast<cudaStream_t>(stream),
                                      seq_lens, batch, k, hdr, order, order + batch);
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }

@@ -1,0 +1,38 @@
+"""The benchmark's roofline numerator (algorithmic bytes per launch), counted
+by hand on small cases: 4 B per score of every non-trivial row, 4 B per
+output slot, 4 B per per-row array read, and 4 B per distinct page-table
+entry the selected positions touch (packed rows: counted at their
+page-table start). CPU only."""
+
+from __future__ import annotations
+
+import torch
+
+import bench
+from sparse_attention_top_row_gb300 import workloads as wl
+
+
+def test_ragged_bytes():
+    w = wl.custom("ragged", 4, [[1.0] * 10, [2.0] * 3, [0.5] * 7], row_starts=[0, 1, 2], out_offsets=[0, 0, 0])
+    raw = torch.full((3, 4), -1, dtype=torch.int32)
+    # rows 0 and 2 are non-trivial (10 and 7 > k = 4); row 1 is trivial (3 <= 4)
+    scores = 4 * (10 + 7)
+    out = 4 * 4 * 3
+    meta = 4 * 3 * 3  # seq_lens, row_starts, out_offsets
+    assert bench.algorithmic_bytes(w, raw) == scores + out + meta
+
+
+def test_paged_bytes_count_distinct_pages():
+    w = wl.custom("paged", 3, [[float(i) for i in range(12)]], page_size=4, seed=1)
+    raw = torch.tensor([[0, 5, 6]], dtype=torch.int32)  # pages 0, 1, 1: two distinct entries
+    assert bench.algorithmic_bytes(w, raw) == 4 * 12 + 4 * 3 + 4 * 1 + 4 * 2
+
+
+def test_packed_bytes_count_pages_from_the_table_start():
+    w = wl.custom("paged", 3, [[float(i) for i in range(12)]], page_size=4, seed=1)
+    w["page_table"] = torch.arange(16, dtype=torch.int32).view(2, 8)
+    w["page_table_stride"] = 8
+    w["page_table_row_starts"] = torch.tensor([3], dtype=torch.int32)
+    w["row_to_batch"] = torch.tensor([1], dtype=torch.int32)
+    raw = torch.tensor([[0, 1, 5]], dtype=torch.int32)  # tokens 3, 4, 8: pages 0, 1, 2
+    assert bench.algorithmic_bytes(w, raw) == 4 * 12 + 4 * 3 + 4 * 3 + 4 * 3

@@ -113,9 +113,12 @@ size_t workspace_bytes_for(int32_t batch) {
     return (bytes + 255) / 256 * 256;
 }
 
-// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each, the
-// candidate buffer is (key, position) pairs, then the row's page-table
-// entries (PAGED) and small scratch.
+// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each plus
+// kHistExtra words merged with them, the candidate buffer is (key, position)
+// pairs, then the row's page-table entries (PAGED) and small scratch. The
+// register route overlays its 16384 packed 16-bit counters on the candidate
+// buffer, and the finishes keep their slot-ordered position list in hist's
+// upper half and short tie lists in its lower half.
 struct Shared {
     uint32_t* hist;      // local histogram
     uint32_t* mhist;     // merged histogram (== hist on a single CTA)
@@ -245,9 +248,8 @@ __device__ __forceinline__ int level_bins(int lvl) { return lvl == 0 ? kBins : l
 // 16 (h 16-byte aligned); target >= 1. All threads call it.
 //  * nb = 4096 (find_threshold_wide): thread t holds bins Rt..Rt+R-1
 //    (R = 4096 / threads); a warp-shuffle suffix sum plus the warp totals in
-//    shared memory give
-//    every thread the count above its run, and the one thread whose run
-//    crosses the target resolves the bin. Two barriers.
+//    shared memory give every thread the count above its run, and the one
+//    thread whose run crosses the target resolves the bin. Two barriers.
 //  * nb <= 256: warp 0 holds the bins (lane l: 8l..8l+7), one warp-shuffle
 //    suffix sum; the other warps wait at the single barrier.
 struct Threshold {

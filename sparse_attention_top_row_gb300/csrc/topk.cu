@@ -77,14 +77,12 @@ namespace {
 constexpr int kThreads = 512;                 // threads per CTA, all routes
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
-constexpr int kHistExtra = 8;                 // words after the bins, merged (summed) with them
 constexpr int kFineShift = 18;                // register route: a 14-bit first digit ...
 constexpr int kFineWords = 8192;              // ... two 16-bit counters per word
 constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
 constexpr int kPageCache = 4096;              // page-table entries of a row held in shared memory
 constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
 constexpr int kClusterSize = 4;               // CTAs per long row on the cluster path
-static_assert(kHistExtra == 2 * kClusterSize, "a bound word and an overflow word per part");
 constexpr int kPlanThreads = 1024;
 constexpr int32_t kClusterFloor = 32768;      // rows longer than this may use the cluster path
 constexpr int32_t kClusterMaxBatch = 64;      // ... when the batch is at most this
@@ -113,8 +111,8 @@ size_t workspace_bytes_for(int32_t batch) {
     return (bytes + 255) / 256 * 256;
 }
 
-// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each plus
-// kHistExtra words merged with them, the candidate buffer is (key, position)
+// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each, the
+// candidate buffer is (key, position)
 // pairs, then the row's page-table entries (PAGED) and small scratch. The
 // register route overlays its 16384 packed 16-bit counters on the candidate
 // buffer, and the finishes keep their slot-ordered position list in hist's
@@ -131,17 +129,17 @@ struct Shared {
 };
 
 constexpr size_t kScratchWords = 2 * kWarps + 32;  // red: 2 words per warp; res: 16; cnt: 16
-constexpr size_t kSmemRows = (kBins + kHistExtra + 2 * kCandCap + kPageCache + kScratchWords) * 4;
-constexpr size_t kSmemCluster = (2 * (kBins + kHistExtra) + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
 
 __device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
     Shared s;
     uint32_t* w = reinterpret_cast<uint32_t*>(base);
     s.hist = w;
-    w += kBins + kHistExtra;
+    w += kBins;
     if (merged_separate) {
         s.mhist = w;
-        w += kBins + kHistExtra;
+        w += kBins;
     } else {
         s.mhist = s.hist;
     }
@@ -467,6 +465,13 @@ struct SoloMerge {
         __syncthreads();
         return sh.hist;
     }
+    // The level-1 merge: this CTA's bound and overflow flag are the row's.
+    __device__ __forceinline__ const uint32_t* merge_level1(const Shared& sh, uint32_t bound, bool ovf,
+                                                            uint32_t& max_bound, bool& any_ovf) const {
+        max_bound = bound;
+        any_ovf = ovf;
+        return merge(sh, kBins);
+    }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt[i]; }
 };
 
@@ -476,11 +481,53 @@ struct ClusterMerge {
     // CTA r sums the 16-byte words w = r, r + kClusterSize, ... over all CTAs
     // (reduce-scatter); then every CTA gathers the words it does not own.
     __device__ const uint32_t* merge(const Shared& sh, int nb) const {
+        cg::this_cluster().sync();  // every local histogram is complete
+        return merge_words(sh, 0, nb / 4);
+    }
+    // The level-1 merge limited to the bins the slices' candidates occupy:
+    // each CTA publishes its bound, its highest occupied bin and its overflow
+    // flag, and only 16-byte words from the highest bound to the highest bin
+    // are summed (mhist is zero elsewhere: it is cleared at the row's start).
+    // Bins below the highest bound cannot hold an exact level-1 threshold.
+    __device__ const uint32_t* merge_level1(const Shared& sh, uint32_t bound, bool ovf, uint32_t& max_bound,
+                                            bool& any_ovf) const {
+        cg::cluster_group cluster = cg::this_cluster();
+        // highest occupied bin at or above the bound
+        uint32_t top = 0;
+        for (int b = kBins - 1 - static_cast<int>(threadIdx.x); b >= static_cast<int>(bound); b -= kThreads)
+            if (sh.hist[b] != 0u) {
+                top = static_cast<uint32_t>(b);
+                break;
+            }
+        top = __reduce_max_sync(kFull, top);
+        if (lane_id() == 0 && top != 0u) atomicMax(&sh.cnt[5], top);
+        if (threadIdx.x == 0) {
+            sh.cnt[4] = bound;
+            sh.cnt[6] = ovf ? 1u : 0u;
+        }
+        cluster.sync();  // every local histogram and every published word is complete
+        uint32_t lo = 0, hi = 0, o = 0;
+#pragma unroll
+        for (int q = 0; q < kClusterSize; ++q) {
+            const uint32_t* c = cluster.map_shared_rank(sh.cnt, q);
+            lo = max(lo, c[4]);
+            hi = max(hi, c[5]);
+            o |= c[6];
+        }
+        max_bound = lo;
+        any_ovf = o != 0u;
+        hi = max(hi, lo);
+        return merge_words(sh, static_cast<int>(lo / 4), static_cast<int>(hi / 4) + 1);
+    }
+    // Sums the 16-byte words [w0, w1) of the CTAs' histograms into mhist; the
+    // CTAs must have passed a cluster barrier since their last histogram write.
+    __device__ const uint32_t* merge_words(const Shared& sh, int w0, int w1) const {
         cg::cluster_group cluster = cg::this_cluster();
         const int rank = static_cast<int>(cluster.block_rank());
-        const int words = nb / 4;
-        cluster.sync();  // every local histogram is complete
-        for (int w = rank + kClusterSize * static_cast<int>(threadIdx.x); w < words; w += kClusterSize * kThreads) {
+        const int words = w1;
+        for (int w = w0 + ((rank - w0 % kClusterSize + kClusterSize) % kClusterSize) +
+                     kClusterSize * static_cast<int>(threadIdx.x);
+             w < words; w += kClusterSize * kThreads) {
             uint4 t = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int q = 0; q < kClusterSize; ++q) {
@@ -490,7 +537,7 @@ struct ClusterMerge {
             reinterpret_cast<uint4*>(sh.mhist)[w] = t;
         }
         cluster.sync();  // every owned word of the sum is complete
-        for (int w = threadIdx.x; w < words; w += kThreads) {
+        for (int w = w0 + static_cast<int>(threadIdx.x); w < words; w += kThreads) {
             const int q = w % kClusterSize;
             if (q != rank)
                 reinterpret_cast<uint4*>(sh.mhist)[w] =
@@ -1190,20 +1237,21 @@ __device__ __forceinline__ int window_count(int ja, int jb, int rem, int len) {
 
 
 // Streaming route over vectors [jb, je) of the aligned window: the whole row
-// on one CTA, or slice `part` of a row cut over a thread-block cluster.
+// on one CTA, or this CTA's slice of a row cut over a thread-block cluster.
 //  1. The slice's head tile gets a full level-1 histogram, which sets the
 //     slice's own lower bound on the threshold bin, aiming about 4 sigma
 //     above the slice head's expected share of the top-k (no cluster
 //     exchange).
 //  2. One pass over the rest collects every element at or above the bound.
-//  3. Level 1 comes from the merged histograms. It is exact when its
+//  3. Level 1 comes from the merged histograms (on a cluster, merged only
+//     over the bins the slices' candidates occupy). It is exact when its
 //     threshold bin clears every slice's bound (each slice's counts are
 //     exact from its bound up); otherwise, or if a buffer overflowed, a full
 //     histogram pass and a re-collection run (always exact, only slower).
 //  4. Solo rows finish with finish_candidates; cluster rows run the radix
 //     levels and emit_selected over the slices' candidate buffers.
 template <bool kPaged, class Merge>
-__device__ void streaming_row(const float4* vbase, int jb, int je, int part, int rem, int len, uint32_t k, bool det,
+__device__ void streaming_row(const float4* vbase, int jb, int je, int rem, int len, uint32_t k, bool det,
                               const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
@@ -1240,22 +1288,14 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int part, int
     // Each part's histogram holds every head-tile element and every candidate
     // after it, so its counts are exact for every bin at or above its bound;
     // the merged level 1 is exact when its threshold bin clears every part's
-    // bound. The words after the bins carry each part's bound and overflow
-    // flag through the same merge.
-    if (threadIdx.x == 0) {
-        sh.hist[kBins + part] = bound_bin;
-        sh.hist[kBins + kClusterSize + part] = sh.cnt[0] > static_cast<uint32_t>(kCandCap) ? 1u : 0u;
-    }
-    const uint32_t* merged = mg.merge(sh, kBins + kHistExtra);
-    uint32_t max_bound = 0, overflow = 0;
-#pragma unroll
-    for (int r = 0; r < kClusterSize; ++r) {
-        max_bound = max(max_bound, merged[kBins + r]);
-        overflow |= merged[kBins + kClusterSize + r];
-    }
+    // bound.
+    uint32_t max_bound = 0;
+    bool overflow = false;
+    const uint32_t* merged =
+        mg.merge_level1(sh, bound_bin, sh.cnt[0] > static_cast<uint32_t>(kCandCap), max_bound, overflow);
     Threshold t1 = find_threshold(merged, kBins, k, sh);
     bool cands_ok = true;
-    if (overflow != 0 || !t1.found || t1.bin < max_bound) {  // uniform over a cluster
+    if (overflow || !t1.found || t1.bin < max_bound) {  // uniform over a cluster
         // full level-1 histogram of this CTA's elements, then re-collect
         clear_hist(sh.hist, kBins);
         __syncthreads();
@@ -1409,9 +1449,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_con
     if (nv <= kTileVecs * kThreads) {
         register_row<kPaged>(vbase, nv, rem, len, k, det, sh, em);
     } else {
-        clear_hist(sh.hist, kBins + kHistExtra);
+        clear_hist(sh.hist, kBins);
         __syncthreads();
-        streaming_row<kPaged>(vbase, 0, nv, 0, rem, len, k, det, sh, SoloMerge{}, em);
+        streaming_row<kPaged>(vbase, 0, nv, rem, len, k, det, sh, SoloMerge{}, em);
     }
 }
 
@@ -1453,7 +1493,8 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         }
         prefetch_pages<kPaged>(em, len, sh);
         if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
-        clear_hist(sh.hist, kBins + kHistExtra);
+        clear_hist(sh.hist, kBins);
+        clear_hist(sh.mhist, kBins);
         const int rem = start & 3;
         const float4* vbase = reinterpret_cast<const float4*>(
             p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
@@ -1464,7 +1505,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads,
         // counters of the leader CTA must be zero before any CTA emits: the
         // merges below pass several cluster barriers first
         __syncthreads();
-        streaming_row<kPaged>(vbase, jb, je, rank, rem, len, k, det, sh, mg, em);
+        streaming_row<kPaged>(vbase, jb, je, rem, len, k, det, sh, mg, em);
         cluster.sync();  // all emits done before the leader's counters are reset
     }
 }

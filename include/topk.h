@@ -36,8 +36,9 @@
  * Errors. Argument errors are found on the host before anything is enqueued
  * and returned as a topk_status; the call then has no effect. A failed launch
  * returns TOPK_ERR_CUDA and leaves the CUDA error for cudaGetLastError().
- * Per-row data errors found on the device (seq_len < 0, row_start < 0) make
- * that row empty (all -1) and are counted in the workspace; read the count
+ * Per-row data errors found on the device (seq_len < 0, row_start < 0, and
+ * for packed PAGED rows page_table_row_start < 0) make that row empty (all
+ * -1) and are counted in the workspace; read the count
  * with topk_read_device_errors().
  */
 #ifndef SPARSE_ATTENTION_TOP_ROW_GB300_TOPK_H

@@ -1393,8 +1393,11 @@ __device__ __forceinline__ void prefetch_pages(Emitter<kPaged>& em, int32_t len,
 
 // One CTA per row; rows come from the plan's order (longest first), rows the
 // plan gave to the cluster path are skipped (their CTAs exit at once).
-template <bool kPaged>
-__global__ void __launch_bounds__(kThreads, 2) topk_rows_kernel(const __grid_constant__ Params p) {
+// kMinBlocks = 2 keeps two CTAs per SM (64 registers a thread); batches that
+// fit one CTA per SM use kMinBlocks = 1, which lets the code keep more in
+// registers.
+template <bool kPaged, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const Shared sh = carve(smem, false);
     grid_dependency_wait();
@@ -1603,6 +1606,7 @@ struct DeviceState {
     bool ready = false;
     cudaError_t err = cudaSuccess;
     int max_clusters = 0;  // co-resident clusters of the cluster kernel
+    int sms = 0;           // streaming multiprocessors
 };
 
 constexpr int kMaxDevices = 64;
@@ -1611,8 +1615,11 @@ std::mutex g_mutex;
 
 template <bool kPaged>
 cudaError_t prepare_kernels(int& max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemRows));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemRows));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemCluster));
@@ -1653,6 +1660,8 @@ cudaError_t device_state(DeviceState** out) {
         if (e == cudaSuccess) e = prepare_kernels<false>(mc);
         if (e != cudaSuccess) return e;
         st.max_clusters = mc > 0 ? mc : 1;
+        e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         st.ready = true;
     }
     *out = &st;
@@ -1683,8 +1692,10 @@ template <bool kPaged>
 int launch_transform(const Params& prm, cudaStream_t stream) {
     DeviceState* ds = nullptr;
     if (device_state(&ds) != cudaSuccess) return TOPK_ERR_CUDA;
-    if (launch_pdl(topk_rows_kernel<kPaged>, prm.batch, kThreads, kSmemRows, stream, prm) != cudaSuccess)
-        return TOPK_ERR_CUDA;
+    const cudaError_t le =
+        prm.batch <= ds->sms ? launch_pdl(topk_rows_kernel<kPaged, 1>, prm.batch, kThreads, kSmemRows, stream, prm)
+                             : launch_pdl(topk_rows_kernel<kPaged, 2>, prm.batch, kThreads, kSmemRows, stream, prm);
+    if (le != cudaSuccess) return TOPK_ERR_CUDA;
     if (prm.batch <= kClusterMaxBatch) {
         const int slots = min(prm.batch, ds->max_clusters);
         if (launch_pdl(topk_cluster_kernel<kPaged>, kClusterSize * slots, kThreads, kSmemCluster, stream, prm) !=

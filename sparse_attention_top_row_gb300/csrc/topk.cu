@@ -1459,8 +1459,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const _
 }
 
 // One thread-block cluster per long row (looping over the plan's cluster list).
-template <bool kPaged>
-__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads, 2)
+// As for the rows kernel, kMinBlocks = 1 (no 64-register cap) serves launches
+// whose clusters all fit one CTA per SM.
+template <bool kPaged, int kMinBlocks>
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads, kMinBlocks)
     topk_cluster_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint8_t smem[];
     const Shared sh = carve(smem, true);
@@ -1605,24 +1607,20 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
 struct DeviceState {
     bool ready = false;
     cudaError_t err = cudaSuccess;
-    int max_clusters = 0;  // co-resident clusters of the cluster kernel
-    int sms = 0;           // streaming multiprocessors
+    int max_clusters = 0;       // co-resident clusters of the two-CTA-per-SM cluster build
+    int max_clusters_wide = 0;  // ... of the one-CTA-per-SM build
+    int sms = 0;                // streaming multiprocessors
 };
 
 constexpr int kMaxDevices = 64;
 DeviceState g_devices[kMaxDevices];
 std::mutex g_mutex;
 
-template <bool kPaged>
-cudaError_t prepare_kernels(int& max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemRows));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemRows));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemCluster));
+// Shared-memory size and co-resident cluster count of one cluster-kernel build.
+template <bool kPaged, int kMinBlocks>
+cudaError_t prepare_cluster_kernel(int& max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged, kMinBlocks>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemCluster));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterSize, 1, 1);
@@ -1636,15 +1634,28 @@ cudaError_t prepare_kernels(int& max_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kPaged>, &cfg) != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();  // the query is advisory: fall back to one cluster per 8 SMs
+    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kPaged, kMinBlocks>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();  // the query is advisory: fall back to a conservative count
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        n = sms > kClusterSize ? sms / kClusterSize : 1;
+        n = sms > 2 * kClusterSize ? sms / (2 * kClusterSize) : 1;
     }
     max_clusters = max_clusters == 0 ? n : min(max_clusters, n);
     return cudaSuccess;
+}
+
+template <bool kPaged>
+cudaError_t prepare_kernels(int& max_clusters, int& max_clusters_wide) {
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemRows));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemRows));
+    if (e != cudaSuccess) return e;
+    e = prepare_cluster_kernel<kPaged, 2>(max_clusters);
+    if (e != cudaSuccess) return e;
+    return prepare_cluster_kernel<kPaged, 1>(max_clusters_wide);
 }
 
 cudaError_t device_state(DeviceState** out) {
@@ -1655,11 +1666,12 @@ cudaError_t device_state(DeviceState** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
     if (!st.ready) {
-        int mc = 0;
-        e = prepare_kernels<true>(mc);
-        if (e == cudaSuccess) e = prepare_kernels<false>(mc);
+        int mc = 0, mcw = 0;
+        e = prepare_kernels<true>(mc, mcw);
+        if (e == cudaSuccess) e = prepare_kernels<false>(mc, mcw);
         if (e != cudaSuccess) return e;
         st.max_clusters = mc > 0 ? mc : 1;
+        st.max_clusters_wide = mcw > 0 ? mcw : 1;
         e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         st.ready = true;
@@ -1697,10 +1709,14 @@ int launch_transform(const Params& prm, cudaStream_t stream) {
                              : launch_pdl(topk_rows_kernel<kPaged, 2>, prm.batch, kThreads, kSmemRows, stream, prm);
     if (le != cudaSuccess) return TOPK_ERR_CUDA;
     if (prm.batch <= kClusterMaxBatch) {
-        const int slots = min(prm.batch, ds->max_clusters);
-        if (launch_pdl(topk_cluster_kernel<kPaged>, kClusterSize * slots, kThreads, kSmemCluster, stream, prm) !=
-            cudaSuccess)
-            return TOPK_ERR_CUDA;
+        // every row's cluster resident at once with one CTA per SM: the wide build
+        const cudaError_t ce =
+            prm.batch <= ds->max_clusters_wide
+                ? launch_pdl(topk_cluster_kernel<kPaged, 1>, kClusterSize * prm.batch, kThreads, kSmemCluster, stream,
+                             prm)
+                : launch_pdl(topk_cluster_kernel<kPaged, 2>, kClusterSize * min(prm.batch, ds->max_clusters),
+                             kThreads, kSmemCluster, stream, prm);
+        if (ce != cudaSuccess) return TOPK_ERR_CUDA;
     }
     return TOPK_OK;
 }

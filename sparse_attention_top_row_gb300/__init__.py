@@ -1,9 +1,9 @@
 """Sparse-attention indexer top-k + transform on GB300: Python binding.
 
 Thin ctypes marshalling over the C ABI of ``include/topk.h`` (the
-``_build/libtopk.so`` library): the functions take torch CUDA tensors, pass
-their device pointers and the current CUDA stream, and raise on a non-zero
-status. Every step of the computation runs in the library's CUDA kernels;
+``_build/libtopk.so`` library): the functions take torch CUDA tensors, check
+each one's dtype, device, size and layout, pass their device pointers and the
+current CUDA stream, and raise on a non-zero status. Every step of the computation runs in the library's CUDA kernels;
 there is no fallback of any kind, and calling without the built library
 raises.
 """
@@ -45,6 +45,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     """Loads the built library (``build()`` in ``__graft_entry__`` or
     ``python -m sparse_attention_top_row_gb300.build`` makes it)."""
     global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
     with _LOCK:
         if _LIB is not None:
             return _LIB
@@ -82,6 +84,60 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _arg(t, name, dtype=None, numel=0, required=True, dense=True):
+    """Checks one tensor argument before its pointer crosses the C ABI: a CUDA
+    tensor of the given dtype, at least `numel` elements, dense (row arrays,
+    outputs, the workspace) or with a unit innermost stride (arrays whose row
+    stride is a separate argument). None passes where the argument is optional
+    (or the batch is empty). Raises TypeError / ValueError; returns the pointer.
+    The common case costs a handful of attribute reads."""
+    if t is None:
+        if required and numel > 0:
+            raise ValueError(f"{name} is required")
+        return None
+    try:
+        ok = ((dtype is None or t.dtype is dtype) and t.is_cuda
+              and (t.is_contiguous() if dense else (t.dim() == 0 or t.numel() <= 1 or t.stride(-1) == 1))
+              and t.numel() >= numel)
+    except AttributeError:
+        ok = False
+    if not ok:
+        _reject(t, name, dtype, numel, dense)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _reject(t, name, dtype, numel, dense):
+    """Raises the error that says why `t` failed `_arg`."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (it is on {t.device})")
+    if dense and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not dense and t.dim() > 0 and t.numel() > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have a unit innermost stride")
+    raise ValueError(f"{name} has {t.numel()} elements, fewer than the {numel} required")
+
+
+def _rows(seq_lens):
+    """The batch, from seq_lens (a CUDA int32 vector, one entry per row)."""
+    import torch
+    if seq_lens is None:
+        raise ValueError("seq_lens is required")
+    _arg(seq_lens, "seq_lens", torch.int32)
+    return int(seq_lens.numel())
+
+
+def _ws(workspace):
+    """The workspace pointer and its size in bytes (any dtype; dense)."""
+    if workspace is None:
+        raise ValueError("workspace is required")
+    return _arg(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
 def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -105,54 +161,70 @@ def new_workspace(batch: int, device="cuda"):
 
 def topk_plan(seq_lens, k: int, workspace, stream=None):
     lib = load()
-    batch = int(seq_lens.numel())
-    _check("topk_plan", lib.topk_plan(_ptr(seq_lens), batch, int(k), _ptr(workspace),
-                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+    batch = _rows(seq_lens)
+    ws, ws_bytes = _ws(workspace)
+    _check("topk_plan", lib.topk_plan(_ptr(seq_lens), batch, int(k), ws, ws_bytes, _stream(stream)))
 
 
 def topk_transform_paged(scores, score_stride: int, row_starts, seq_lens, page_table,
                          page_table_stride: int, page_size: int, k: int, workspace, out,
                          out_raw=None, flags: int = 0, stream=None):
+    import torch
     lib = load()
-    batch = int(seq_lens.numel())
-    _check("topk_transform_paged", lib.topk_transform_paged(
-        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(page_table),
-        int(page_table_stride), int(page_size), batch, int(k), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_raw), int(flags),
-        _stream(stream)))
+    batch = _rows(seq_lens)
+    i32 = torch.int32
+    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
+            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
+            _arg(page_table, "page_table", i32, 1 if batch else 0, dense=False), int(page_table_stride),
+            int(page_size), batch, int(k), *_ws(workspace), _arg(out, "out", i32, batch * int(k)),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
+    _check("topk_transform_paged", lib.topk_transform_paged(*args, _stream(stream)))
 
 
 def topk_transform_paged_packed(scores, score_stride: int, row_starts, seq_lens, page_table,
                                 page_table_stride: int, page_size: int, page_table_row_starts, row_to_batch,
                                 k: int, workspace, out, out_raw=None, flags: int = 0, stream=None):
+    import torch
     lib = load()
-    batch = int(seq_lens.numel())
-    _check("topk_transform_paged_packed", lib.topk_transform_paged_packed(
-        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(page_table),
-        int(page_table_stride), int(page_size), _ptr(page_table_row_starts), _ptr(row_to_batch), batch, int(k),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(out_raw), int(flags),
-        _stream(stream)))
+    batch = _rows(seq_lens)
+    i32 = torch.int32
+    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
+            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
+            _arg(page_table, "page_table", i32, 1 if batch else 0, dense=False), int(page_table_stride),
+            int(page_size), _arg(page_table_row_starts, "page_table_row_starts", i32, batch, required=False),
+            _arg(row_to_batch, "row_to_batch", i32, batch, required=False), batch, int(k),
+            *_ws(workspace), _arg(out, "out", i32, batch * int(k)),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
+    _check("topk_transform_paged_packed", lib.topk_transform_paged_packed(*args, _stream(stream)))
 
 
 def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int,
                           workspace, out, out_raw=None, flags: int = 0, stream=None):
+    import torch
     lib = load()
-    batch = int(seq_lens.numel())
-    _check("topk_transform_ragged", lib.topk_transform_ragged(
-        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(out_offsets),
-        batch, int(k), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
-        _ptr(out_raw), int(flags), _stream(stream)))
+    batch = _rows(seq_lens)
+    i32 = torch.int32
+    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
+            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
+            _arg(out_offsets, "out_offsets", i32, batch), batch, int(k), *_ws(workspace),
+            _arg(out, "out", i32, batch * int(k)), _arg(out_raw, "out_raw", i32, batch * int(k), required=False),
+            int(flags))
+    _check("topk_transform_ragged", lib.topk_transform_ragged(*args, _stream(stream)))
 
 
 def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int, out,
                                   out_raw=None, flags: int = 0, stream=None):
     """Plan + RAGGED transform without a caller workspace (the library's
     built-in one; batch <= TOPK_NOALLOC_MAX_BATCH). See include/topk.h."""
+    import torch
     lib = load()
-    batch = int(seq_lens.numel())
-    _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(
-        _ptr(scores), int(score_stride), _ptr(row_starts), _ptr(seq_lens), _ptr(out_offsets), batch, int(k),
-        _ptr(out), _ptr(out_raw), int(flags), _stream(stream)))
+    batch = _rows(seq_lens)
+    i32 = torch.int32
+    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
+            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
+            _arg(out_offsets, "out_offsets", i32, batch), batch, int(k), _arg(out, "out", i32, batch * int(k)),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
+    _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(*args, _stream(stream)))
 
 
 def topk_read_device_errors(workspace, stream=None):
@@ -160,8 +232,9 @@ def topk_read_device_errors(workspace, stream=None):
     lib = load()
     n = ctypes.c_int32(0)
     f = ctypes.c_uint32(0)
+    ws, _ = _ws(workspace)
     _check("topk_read_device_errors",
-           lib.topk_read_device_errors(_ptr(workspace), ctypes.byref(n), ctypes.byref(f), _stream(stream)))
+           lib.topk_read_device_errors(ws, ctypes.byref(n), ctypes.byref(f), _stream(stream)))
     return int(n.value), int(f.value)
 
 

@@ -2,7 +2,7 @@
 by hand on small cases: 4 B per score of every non-trivial row, 4 B per
 output slot, 4 B per per-row array read, and 4 B per distinct page-table
 entry the selected positions touch (packed rows: counted at their
-page-table start). CPU only."""
+page-table start). Also the end-to-end leg's packed input copy. CPU only."""
 
 from __future__ import annotations
 
@@ -36,3 +36,21 @@ def test_packed_bytes_count_pages_from_the_table_start():
     w["row_to_batch"] = torch.tensor([1], dtype=torch.int32)
     raw = torch.tensor([[0, 1, 5]], dtype=torch.int32)  # tokens 3, 4, 8: pages 0, 1, 2
     assert bench.algorithmic_bytes(w, raw) == 4 * 12 + 4 * 3 + 4 * 3 + 4 * 3
+
+
+def test_e2e_inputs_pack_into_one_copy(monkeypatch):
+    """The end-to-end leg copies a launch's inputs as one packed buffer: every
+    tensor comes back bit for bit from its 256-byte-aligned slot."""
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)   # no CUDA here
+    for w in (wl.paged_decode("cpu", batch=8, seq_len=1024, k=64), wl.ragged_tiny("cpu"),
+              wl.paged_packed("cpu", n_req=2, q_rows=2, min_tokens=500, max_tokens=900, window=300, k=50,
+                              page_size=16)):
+        host, dev, dw = bench.packed_inputs(w, "cpu")
+        dev.copy_(host)
+        payload = 0
+        for key, v in w.items():
+            if isinstance(v, torch.Tensor):
+                payload += v.numel() * v.element_size()
+                assert dw[key].dtype == v.dtype and torch.equal(dw[key], v), key
+                assert (dw[key].data_ptr() - dev.data_ptr()) % 256 == 0 and dw[key].is_contiguous()
+        assert payload <= host.numel() < payload + 256 * len(w)

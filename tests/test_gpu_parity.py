@@ -254,6 +254,35 @@ def test_packed_paged_without_arrays_is_plain_paged(cuda_lib):
     assert torch.equal(torch.sort(a, dim=1).values, torch.sort(b, dim=1).values)
 
 
+@pytest.mark.parametrize("mode", ["paged", "ragged"])
+def test_cluster_floor_lengths(cuda_lib, mode):
+    """Rows either side of the cluster floor (32768) in a small batch: 32768
+    stays on the streaming route, 32769 and longer take the cluster route."""
+    rng = np.random.default_rng(32768)
+    lens = [32767, 32768, 32769, 32772, 36000]
+    starts = [int(x) for x in rng.integers(0, 4, size=len(lens))]
+    w = wl.custom(mode, 2048, _rows(rng, lens), row_starts=starts,
+                  out_offsets=[int(x) for x in rng.integers(0, 1 << 20, size=len(lens))], page_size=64, seed=5)
+    check_full(cuda_lib, w)
+
+
+@pytest.mark.parametrize("batch", [39, 64, 65])
+def test_cluster_batch_limits(cuda_lib, batch):
+    """Mixed lengths up to 70000 around the cluster path's batch limits: up to
+    64 rows the long rows take the cluster kernel (its two-CTA-per-SM build
+    once the rows outnumber the clusters that fit one CTA per SM, 36 on a
+    GB300), at 65 they stay on the streaming route."""
+    w = wl.mixed("cpu", mode="paged", k=1024, batch=batch, max_len=70000, sub_id=batch)
+    check_full(cuda_lib, w)
+
+
+def test_largest_batch_in_one_launch(cuda_lib):
+    """16384 rows (the largest batch of the pages' workloads) in one plan and
+    one transform: short RAGGED rows at unaligned starts, k=256."""
+    w = wl.mixed("cpu", mode="ragged", k=256, batch=16384, max_len=3000, min_len=16, sub_id=16384)
+    check_full(cuda_lib, w)
+
+
 def test_packed_negative_table_start_is_a_data_error(cuda_lib):
     w = wl.paged_packed("cpu", sub_id=5, n_req=2, q_rows=3, min_tokens=3000, max_tokens=5000, window=4000,
                         k=512, page_size=64)

@@ -103,8 +103,8 @@ TOPK_API size_t topk_workspace_bytes(int32_t batch);
  *              or more.
  *
  * One small kernel on `stream`. The plan sorts rows into length bands
- * (longest first) and, for small batches, hands rows longer than 32768 to a
- * thread-block-cluster path that splits each such row over 8 SMs. A
+ * (longest first) and, in batches of at most 64 rows, hands rows longer than
+ * 32768 to a thread-block-cluster path that splits each such row over 4 SMs. A
  * transform run after it on the same stream (or otherwise ordered after it)
  * consumes the plan; one plan serves any number of transforms with the same
  * seq_lens, batch and k (e.g. every layer of a decode step). A transform whose
@@ -197,8 +197,9 @@ TOPK_API int topk_transform_ragged(const float* scores, int64_t score_stride,
 
 /*
  * Reads the workspace's device error count (rows with seq_len < 0 seen by the
- * plan, plus rows with row_start < 0 seen by each transform since the plan)
- * and the device flags word into HOST memory. Synchronises `stream`.
+ * plan, plus rows with row_start < 0, or for packed PAGED rows
+ * page_table_row_start < 0, seen by each transform since the plan) and the
+ * device flags word into HOST memory. Synchronises `stream`.
  *   host_error_rows  host int32*, required.
  *   host_flags       host uint32*, or NULL.
  */

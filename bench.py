@@ -392,6 +392,21 @@ def measure_e2e(name, steps, warmup, rank, stream):
         b.record(stream)
         torch.cuda.synchronize()
     t = a.elapsed_time(b) / 1e3
+    # One more step, untimed and in deterministic mode (a unique result), read
+    # back to the host, must match a run on inputs copied the ordinary way
+    # (sorted rows: the slot order is unspecified).
+    for ln in launches:
+        ln.flags = topk.TOPK_DETERMINISTIC
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    for w, ho in zip(hosts, outs):
+        ref = Launch(wl.to_device(w, "cuda"), flags=topk.TOPK_DETERMINISTIC)
+        ref.plan(stream)
+        ref.transform(stream)
+        torch.cuda.synchronize()
+        if not torch.equal(torch.sort(ho, dim=1).values, torch.sort(ref.out.cpu(), dim=1).values):
+            raise RuntimeError("end-to-end outputs differ from the device-resident run")
     rows = sum(ln.B for ln in launches)
     return {"value": rows * steps / t, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 

@@ -129,7 +129,9 @@ TOPK_API int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* 
  *                     (0: all rows share one buffer).
  *   row_starts        int32 [batch] or NULL (NULL: every window starts at 0).
  *                     The logical position p counts from the window start.
- *   seq_lens          int32 [batch], the same values the plan saw.
+ *   seq_lens          int32 [batch], the same values the plan saw; each at
+ *                     most 2^31 - 8 (the window's 16-byte span is counted
+ *                     in int32).
  *   page_table        int32, row b at page_table + b*page_table_stride; it must
  *                     hold ceil(seq_len / page_size) valid entries, and
  *                     page * page_size + page_size - 1 must fit int32.
@@ -163,7 +165,9 @@ TOPK_API int topk_transform_paged(const float* scores, int64_t score_stride,
  * Arguments as for topk_transform_paged, plus
  *   page_table_row_starts  int32 [batch] or NULL (0 for every row); a
  *                          negative entry is a data error (the row comes out
- *                          all -1 and the device error count goes up).
+ *                          all -1 and the device error count goes up);
+ *                          page_table_row_starts[b] + seq_lens[b] must fit
+ *                          int32.
  *   row_to_batch           int32 [batch] or NULL (row b uses table row b);
  *                          caller's contract: each entry names a table row.
  * The page table must hold the entries t / page_size for every t of every

@@ -2,23 +2,27 @@
 """Benchmark of the indexer top-k + transform on GB300.
 
 One step = the whole hot path on one batch: topk_plan + the transform
-(route, 16-byte window loads, key map, 12- or 14-bit first-digit
-histogram, radix refine, compaction, fused page-table / offset emit).
+(route, 16-byte window loads, key map, histogram threshold search, radix
+refine, compaction, fused page-table / offset emit).
 
-Default workload (the headline line): PAGED decode, 128 rows x 8192 fp32
-scores, k = 2048, page_size 64, a random page permutation. Those inputs
-(5.3 MB) fit in L2, so every step uses the next of enough rotating input sets
-to span more than twice the L2. The other workloads (RAGGED tiny, RAGGED
-prefill extend, PAGED long, packed PAGED, the mixed sweep) are measured
-after it and reported under "configs" in the same line.
+Headline workload: RAGGED prefill extend, 4 requests x (28672 cached + 4096
+new tokens) = 16384 causal query rows of 28673..32768 fp32 scores, k = 2048,
+out_offsets = row_start, stored as a [16384, 131072] fp32 buffer and run as 16
+launches of 1024 rows. Its 8 GiB of scores span far more than twice the L2, so
+no timed step finds its inputs there. The other workloads (RAGGED tiny, PAGED
+decode, PAGED long, packed PAGED, the mixed sweep) are measured after it and
+reported under "configs"; those small enough to fit in L2 are rotated through
+at least ceil(2 * L2 / set bytes) + 1 copies of their inputs.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU with
 its own seed (weak scaling; rows are independent, so there is no data-path
 collective); the barrier and the max-over-ranks time use torch.distributed.
-``--impl reference`` times the CPU oracle, as it stands, on host cores:
-W untimed steps, then K timed steps of the headline workload.
+``--impl reference`` times the CPU oracle, as it stands, on the host cores
+(every core, each thread running the unchanged single-threaded routine on its
+own block of rows): W untimed steps, then K timed steps, each a bounded
+sample of the headline workload's rows.
 """
 
 from __future__ import annotations
@@ -28,7 +32,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -46,8 +49,9 @@ from sparse_attention_top_row_gb300 import workloads as wl  # noqa: E402
 METRIC = "rows/sec and achieved HBM GB/s (fraction of ~8 TB/s) for top-k transform, 1×GB300"
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 126 * 1024 * 1024
-HEADLINE = "paged_decode"
-REF_BUDGET_S = 150.0     # the whole reference-arm run, warm-up included
+HEADLINE = "ragged_extend"
+REF_BUDGET_S = 120.0     # the whole reference-arm run, warm-up included
+MAX_ROTATION_BYTES = 6 << 30   # device memory a rotation of small input sets may take
 KERNEL_SRC = os.path.join(ROOT, "sparse_attention_top_row_gb300", "csrc", "topk.cu")
 
 
@@ -67,18 +71,18 @@ def kernel_source_hash():
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"rows_kernel_{workload}.md")
+def profiled_traffic(kernel, workload):
+    """DRAM bytes (read + written) per launch of `kernel` on `workload` from
+    the committed ncu record ``profiles/<kernel>_<workload>.json``, if that
+    record was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
-    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return int(m_tr.group(1))
+    return int(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -165,6 +169,23 @@ def max_over_ranks(x, world):
 
 # ----------------------------------------------------------------------------- workloads
 
+DESCRIPTIONS = {
+    "ragged_extend": "RAGGED prefill extend: 4 requests x (28672 cached + 4096 new) = 16384 causal rows, "
+                     "L = 28673..32768, k=2048, out_offsets = row_start, [16384, 131072] fp32 run as 16 "
+                     "launches of 1024 rows; N(0,1) with 1% +4.0",
+    "ragged_tiny": "RAGGED tiny: B=8, k=512, L ~ U{1..4096}, windows back to back in one buffer",
+    "paged_decode": "PAGED decode: B=128, L=8192, k=2048, page_size=64, random page permutation",
+    "paged_long_b1": "PAGED long: B=1, L=131072, k=2048, page_size=64, bf16-rounded 0.1*N(0,1)",
+    "paged_long_b30": "PAGED long: B=30, L=131072, k=2048, page_size=64, bf16-rounded 0.1*N(0,1)",
+    "paged_long_b31": "PAGED long: B=31, L=131072, k=2048, page_size=64, bf16-rounded 0.1*N(0,1)",
+    "paged_packed": "packed PAGED: 8 requests x 16 query rows, sliding window 16384, k=2048, page_size=64",
+    "mixed": "mixed sweep: k in {512,1024,2048} x B in {1,31,129,1024} x {PAGED, RAGGED}, "
+             "L log-uniform in [256, 131072] plus boundary rows (24 launches)",
+}
+EXTRA = ("ragged_tiny", "paged_decode", "paged_long_b1", "paged_long_b30", "paged_long_b31", "paged_packed",
+         "mixed")
+
+
 def make_workload(name, device, rank=0):
     """The named workload as a list of launches (each a workload dict)."""
     if name == "paged_decode":
@@ -172,7 +193,7 @@ def make_workload(name, device, rank=0):
     if name == "ragged_tiny":
         return [wl.ragged_tiny(device, sub_id=rank)]
     if name == "ragged_extend":
-        return [wl.ragged_extend(device, chunk=c) for c in range(16)]
+        return [wl.ragged_extend(device, chunk=c, sub_id=c + 16 * rank) for c in range(16)]
     if name == "ragged_extend_chunk":  # one 1024-row chunk (profiling size)
         return [wl.ragged_extend(device, chunk=0)]
     if name == "paged_packed":  # packed PAGED extend rows: 8 requests x 16 queries, sliding window 16384
@@ -188,6 +209,14 @@ def make_workload(name, device, rank=0):
                     launches.append(wl.mixed(device, mode=mode, k=k, batch=b, sub_id=b + 100 * rank))
         return launches
     raise ValueError(name)
+
+
+def headline_sample(device="cpu"):
+    """The bounded sample of the headline workload the CPU oracle is timed on:
+    rows 2048..2303 of the 16384 (query tokens 2048..2303 of request 0, L =
+    30721..30976, about the workload's mean length of 30720.5), drawn by the
+    same recipe from their own seed."""
+    return wl.ragged_extend(device, chunk=8, rows_per_chunk=256)
 
 
 def algorithmic_bytes(w, out_raw):
@@ -212,6 +241,17 @@ def algorithmic_bytes(w, out_raw):
         distinct = ((srt[:, 1:] != srt[:, :-1]) & (srt[:, 1:] >= 0)).sum(1) + (srt[:, 0] >= 0).to(torch.int64)
         pages = 4 * int(distinct.sum().item())
     return scores + out + meta + pages
+
+
+def input_bytes(w):
+    return sum(v.numel() * v.element_size() for v in w.values() if isinstance(v, torch.Tensor))
+
+
+def transform_kernels(batch):
+    """Kernels one transform of `batch` rows launches (the library's host
+    rule): the rows kernel, plus the cluster kernel for batches of at most 64
+    rows."""
+    return 1 + (1 if batch <= 64 else 0)
 
 
 class Launch:
@@ -244,16 +284,31 @@ class Launch:
                                        stream=stream)
 
     def launches_per_step(self):
-        return 2 + (1 if self.B <= 64 else 0)
+        return 1 + transform_kernels(self.B)
 
 
-def time_workload(launch_sets, steps, warmup, world, stream):
+# ----------------------------------------------------------------------------- device timing
+
+class L2Flush:
+    """A device buffer of twice the L2; writing it evicts whatever the L2
+    held (done outside every timed region)."""
+
+    def __init__(self, l2_bytes):
+        self.buf = torch.empty(2 * l2_bytes // 4 + 1024, dtype=torch.int32, device="cuda")
+
+    def __call__(self, stream):
+        with torch.cuda.stream(stream):
+            self.buf.fill_(1)
+
+
+def time_workload(launch_sets, steps, warmup, world, stream, flush):
     """Times `steps` steps; timed step i runs every launch of set
     (warmup + i) % len(sets). The steps are captured into one CUDA graph (the
     way a serving loop launches them), so the device timeline holds no host
     launch gaps; a second graph of the transforms alone gives the per-launch
-    duration of the transform. Returns (seconds for all steps, seconds per
-    transform launch)."""
+    duration of the transform. The L2 is flushed before each of the two
+    replays, and the sets a replay cycles through span more than twice the
+    L2. Returns (seconds for all steps, seconds per transform launch)."""
     n_launch = len(launch_sets[0])
 
     def sets_for(i):
@@ -280,10 +335,7 @@ def time_workload(launch_sets, steps, warmup, world, stream):
                 ln.transform(None)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    # transforms alone (untimed for the headline value)
-    ev[2].record(stream)
-    g_tr.replay()
-    ev[3].record(stream)
+    flush(stream)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -292,28 +344,34 @@ def time_workload(launch_sets, steps, warmup, world, stream):
     ev[1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    flush(stream)                   # the transforms alone, on cold inputs too
+    ev[2].record(stream)
+    g_tr.replay()
+    ev[3].record(stream)
+    torch.cuda.synchronize()
     total = ev[0].elapsed_time(ev[1]) / 1e3
     per_transform = ev[2].elapsed_time(ev[3]) / 1e3 / (steps * n_launch)
     del g_steps, g_tr
     return total, per_transform
 
 
-def rotating_sets(name, device, rank, max_sets, flags=0):
-    """Copies of a workload so that the timed steps never re-read a set that
-    may still sit in L2: either one set already spans > 2x L2, or every step
-    (warm-up and timed) gets a set of its own, up to `max_sets`."""
+def rotating_sets(name, device, rank, l2_bytes, flags=0):
+    """Copies of a workload's inputs such that the sets span more than twice
+    the L2: one set when it alone does, else ceil(2 * L2 / set bytes) + 1
+    sets (capped by MAX_ROTATION_BYTES), whatever the step count."""
     base = make_workload(name, device, rank)
-    size = sum(w["scores"].numel() * 4 for w in base)
-    n = 1 if size > 2 * L2_BYTES else min(max_sets, int(math.ceil(2 * L2_BYTES / max(size, 1))) + 1)
+    size = sum(input_bytes(w) for w in base)
+    n = 1 if size > 2 * l2_bytes else int(math.ceil(2 * l2_bytes / max(size, 1))) + 1
+    n = max(1, min(n, MAX_ROTATION_BYTES // max(size, 1)))
     sets = [[Launch(w, flags) for w in base]]
     for c in range(1, n):
         sets.append([Launch({kk: (v.clone() if isinstance(v, torch.Tensor) else v) for kk, v in w.items()},
                             flags) for w in base])
-    return sets, n
+    return sets, n, size
 
 
-def measure(name, steps, warmup, world, rank, stream, peak):
-    sets, n_sets = rotating_sets(name, "cuda", rank, max_sets=steps + warmup)
+def measure(name, steps, warmup, world, rank, stream, peak, l2_bytes, flush):
+    sets, n_sets, set_bytes = rotating_sets(name, "cuda", rank, l2_bytes)
     # algorithmic bytes, from one run with out_raw
     alg = 0
     for ln in sets[0]:
@@ -323,7 +381,7 @@ def measure(name, steps, warmup, world, rank, stream, peak):
         torch.cuda.synchronize()
         alg += algorithmic_bytes(ln.w, raw)
     rows = sum(ln.B for ln in sets[0])
-    total, t_launch = time_workload(sets, steps, warmup, world, stream)
+    total, t_launch = time_workload(sets, steps, warmup, world, stream, flush)
     total = max_over_ranks(total, world)
     t_transform = t_launch * len(sets[0])
     res = {
@@ -335,13 +393,24 @@ def measure(name, steps, warmup, world, rank, stream, peak):
         "frac_of_measured_hbm": alg / t_transform / 1e9 / peak,
         "frac_of_nominal_8tbs": alg / t_transform / 1e9 / NOMINAL_HBM_GBS,
         "input_sets": n_sets,
+        "input_set_bytes": set_bytes,
+        "l2": l2_text(n_sets, set_bytes, l2_bytes),
         "launches_per_step": sum(ln.launches_per_step() for ln in sets[0]),
         "rows_per_step": rows,
+        "steps": steps,
     }
     del sets
     torch.cuda.empty_cache()
     return res
 
+
+def l2_text(n_sets, set_bytes, l2_bytes):
+    ok = n_sets * set_bytes >= 2 * l2_bytes
+    return (f"{n_sets} input set(s) x {set_bytes} B = {n_sets * set_bytes} B "
+            f"{'>=' if ok else '<'} 2 x L2 = {2 * l2_bytes} B; L2 flushed before each timed replay")
+
+
+# ----------------------------------------------------------------------------- end to end
 
 def packed_inputs(w, device):
     """The workload's input tensors packed into one pinned host buffer and one
@@ -363,11 +432,30 @@ def packed_inputs(w, device):
     return host, dev, out
 
 
+def e2e_host_workloads(name, rank):
+    """Host copies of the workload's launches for the end-to-end leg. Rows
+    whose score windows sit in a wider strided buffer keep only their windows,
+    packed back to back (the bytes a caller actually holds and moves; outputs
+    are unchanged: RAGGED positions get out_offsets[b], PAGED positions count
+    from the window start)."""
+    hosts = []
+    devs = make_workload(name, "cuda", rank)
+    for w in devs:
+        windows = int(w["seq_lens"].clamp(min=0).sum().item())
+        if int(w["score_stride"]) > 0 and w["scores"].numel() > 2 * windows:
+            w = wl.pack_windows(w)
+        hosts.append(wl.to_device(w, "cpu"))
+    del devs
+    torch.cuda.empty_cache()
+    return hosts
+
+
 def measure_e2e(name, steps, warmup, rank, stream):
     """Same metric through the public API with HOST buffers: each step copies
-    the inputs from pinned host memory (all of a launch's inputs in one packed
-    copy), plans, transforms and reads the output back to pinned host memory."""
-    hosts = make_workload(name, "cpu", rank)
+    every launch's inputs from pinned host memory (one packed copy per
+    launch), plans, transforms and reads the output back to pinned host
+    memory; the timed region holds all of it."""
+    hosts = e2e_host_workloads(name, rank)
     packs = [packed_inputs(w, "cuda") for w in hosts]
     h2d = sum(hb.numel() for hb, _, _ in packs)
     d2h = sum(4 * int(w["batch"]) * int(w["k"]) for w in hosts)
@@ -393,100 +481,147 @@ def measure_e2e(name, steps, warmup, rank, stream):
         torch.cuda.synchronize()
     t = a.elapsed_time(b) / 1e3
     # One more step, untimed and in deterministic mode (a unique result), read
-    # back to the host, must match a run on inputs copied the ordinary way
-    # (sorted rows: the slot order is unspecified).
+    # back to the host: sampled rows of every launch must match the oracle.
     for ln in launches:
         ln.flags = topk.TOPK_DETERMINISTIC
     with torch.cuda.stream(stream):
         step()
     torch.cuda.synchronize()
-    for w, ho in zip(hosts, outs):
-        ref = Launch(wl.to_device(w, "cuda"), flags=topk.TOPK_DETERMINISTIC)
-        ref.plan(stream)
-        ref.transform(stream)
-        torch.cuda.synchronize()
-        if not torch.equal(torch.sort(ho, dim=1).values, torch.sort(ref.out.cpu(), dim=1).values):
-            raise RuntimeError("end-to-end outputs differ from the device-resident run")
-    rows = sum(ln.B for ln in launches)
-    return {"value": rows * steps / t, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-
-def cpu_baseline(name, budget_s, rank):
-    """The CPU oracle, as it stands (single-threaded), on a bounded sample of
-    the workload: whole launches repeated, or a prefix of rows for the big
-    ones, until about `budget_s` seconds of CPU work."""
     import oracle
-    launches = make_workload(name, "cpu", rank) if name not in ("ragged_extend",) else \
-        [wl.ragged_extend("cpu", chunk=0, rows_per_chunk=64)]
-    rows_done, t0 = 0, time.perf_counter()
-    reps = 0
-    while time.perf_counter() - t0 < budget_s:
-        for w in launches:
-            oracle.run_workload(w)
-            rows_done += int(w["batch"])
-        reps += 1
-    t = time.perf_counter() - t0
-    sample = (f"{reps} pass(es) over {'the first 64 rows of chunk 0' if name == 'ragged_extend' else 'the whole batch'}"
-              f" of the {name} workload ({rows_done} rows)")
-    return {"value": rows_done / t, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
+    for w, ho in zip(hosts, outs):
+        B = int(w["batch"])
+        rows = sorted({0, B // 3, B // 2, B - 1})
+        ref, _, _ = oracle.run_workload(w, rows=rows)
+        got = torch.sort(ho[rows], dim=1).values.numpy()
+        if not (got == __import__("numpy").sort(ref, axis=1)).all():
+            raise RuntimeError(f"end-to-end outputs differ from the oracle on {w['name']}")
+    rows = sum(ln.B for ln in launches)
+    res = {"value": rows * steps / t, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": 1e3 * t / steps}
+    del packs, launches, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(name, rank):
+    """Host copies of a bounded row sample of every launch of the workload
+    (up to 64 evenly spaced rows each; the headline's sample is
+    headline_sample())."""
+    if name == HEADLINE:
+        return [headline_sample("cpu")], "rows 2048..2303 of the 16384 (L 30721..30976), their own seed"
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    out = []
+    for w in make_workload(name, dev, rank):
+        B = int(w["batch"])
+        rows = sorted({int(round(i * (B - 1) / 63)) for i in range(64)}) if B > 64 else list(range(B))
+        out.append(wl.to_device(wl.select_rows(w, rows) if len(rows) < B else w, "cpu"))
+    return out, "up to 64 evenly spaced rows of every launch"
+
+
+def time_oracle(samples, threads, budget_s):
+    """Rows per second of the oracle, as it stands, over repeated passes of
+    the sample (whole passes, at least one) until `budget_s` has passed; with
+    threads > 1 every launch's rows are split over that many threads, each
+    running the unchanged single-threaded routine. Returns (rows/s, rows,
+    seconds)."""
+    import oracle
+    rows, t0 = 0, time.perf_counter()
+    while True:
+        for w in samples:
+            oracle.run_workload_threads(w, threads=threads)
+            rows += int(w["batch"])
+        t = time.perf_counter() - t0
+        if t >= budget_s:
+            return rows / t, rows, t
+
+
+def cpu_baselines(name, rank, budget_s):
+    """The CPU oracle on one thread and on every host core."""
+    import oracle
+    samples, what = oracle_sample(name, rank)
+    cores = oracle.host_cores()
+    v1, r1, t1 = time_oracle(samples, 1, budget_s)
+    vn, rn, tn = time_oracle(samples, cores, budget_s)
+    return {"value": vn, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what} of the {name} workload: {rn} rows in {tn:.1f} s on {cores} threads",
+            "single_thread": {"value": v1, "unit": "rows/s", "cores": 1,
+                              "sample": f"{r1} rows in {t1:.1f} s on 1 thread"}}
 
 
 # ----------------------------------------------------------------------------- main
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle, as it stands (single-threaded), on
-    the headline workload. W untimed steps, then exactly K timed steps; a step
-    is the oracle over the whole batch, or over its first R rows when K + W
-    whole batches would take longer than REF_BUDGET_S (R is chosen from the
-    time of the first warm-up step). Rank 0 alone runs it."""
+    """The reference arm: the CPU oracle, as it stands, on every host core
+    (each thread running the unchanged single-threaded routine on its own
+    block of rows) over a bounded sample of the headline workload. W untimed
+    steps, then exactly K timed steps; a step is the oracle over R rows of
+    the sample, R chosen from the first warm-up step so that the whole run
+    stays within about REF_BUDGET_S. Rank 0 alone runs it."""
     if rank != 0:
         return
+    import numpy as np
     import oracle
-    w = make_workload(HEADLINE, "cpu", rank)[0]
+    w = headline_sample("cpu")
+    cores = oracle.host_cores()
     B = int(w["batch"])
     t0 = time.perf_counter()
-    oracle.run_workload(w)                      # the first warm-up step
-    t_batch = time.perf_counter() - t0
+    oracle.run_workload_threads(w, threads=cores)          # the first warm-up step, every sample row
+    t_row = (time.perf_counter() - t0) / B
     n_steps = args.steps + args.warmup
-    rows_per_step = B
-    if t_batch * n_steps > REF_BUDGET_S:
-        rows_per_step = max(1, int(B * REF_BUDGET_S / (t_batch * n_steps)))
-    rows = None if rows_per_step == B else list(range(rows_per_step))
+    rows_per_step = max(1, min(B, int(REF_BUDGET_S / max(t_row * n_steps, 1e-9))))
+    rows = np.arange(rows_per_step)
     for _ in range(args.warmup - 1):
-        oracle.run_workload(w, rows=rows)
+        oracle.run_workload_threads(w, rows=rows, threads=cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.run_workload(w, rows=rows)
+        oracle.run_workload_threads(w, rows=rows, threads=cores)
     t = time.perf_counter() - t0
     value = rows_per_step * args.steps / t
-    what = "the whole batch" if rows is None else f"the first {rows_per_step} of its {B} rows"
-    base = {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+    base = {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": f"{args.steps} timed step(s) after {args.warmup} warm-up step(s), each the oracle over "
-                      f"{what} of the {HEADLINE} workload"}
+                      f"{rows_per_step} of rows 2048..2303 (L 30721..30976) of the {HEADLINE} workload "
+                      f"on {cores} threads"}
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": "PAGED decode B=128 L=8192 k=2048 page_size=64",
-                   "global_batch": 128, "seq_len": 8192, "parallelism": f"rows x{args.gpus} (weak)"},
+        "config": headline_config(world or 1),
         "cpu_baseline": base,
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def headline_config(world, l2=None):
+    cfg = {"workload": DESCRIPTIONS[HEADLINE], "global_batch": 16384 * world, "seq_len": "28673..32768",
+           "k": 2048, "parallelism": f"rows x{world} (weak)"}
+    if l2 is not None:
+        cfg["l2"] = l2
+    return cfg
+
+
+def device_l2_bytes():
+    try:
+        return max(int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size),
+                   126 * 1024 * 1024)
+    except (RuntimeError, AttributeError):
+        return 126 * 1024 * 1024
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-configs", action="store_true", help="headline workload only")
-    ap.add_argument("--workload", default=HEADLINE, help="headline workload (default: paged_decode)")
+    ap.add_argument("--workload", default=HEADLINE, help="the workload of a --quick run")
     ap.add_argument("--quick", action="store_true",
-                    help="the headline workload only: no other configs, no e2e, no CPU baseline")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+                    help="one workload only: device timings, no e2e, no CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=1.5, help="oracle time budget per config and thread count")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
@@ -499,28 +634,31 @@ def main():
     topk.load()
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.current_stream()
+    l2 = device_l2_bytes()
+    flush = L2Flush(l2)
 
+    name = args.workload if args.quick else HEADLINE
     with ClockSampler(local) as clocks:
-        head = measure(args.workload, args.steps, args.warmup, world, rank, stream, peak)
+        head = measure(name, args.steps, args.warmup, world, rank, stream, peak, l2, flush)
     clk = clocks.summary()
     if args.quick:
         if rank == 0:
-            print(json.dumps({"workload": args.workload, **head, "clocks": clk}), flush=True)
+            print(json.dumps({"workload": name, **head, "clocks": clk}), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return
 
+    e2e = measure_e2e(HEADLINE, args.steps, args.warmup, rank, stream)
+    base = cpu_baselines(HEADLINE, rank, 3 * args.cpu_seconds) if (rank == 0 and world == 1) else None
+
     extra = {}
     if not args.no_configs:
-        for name, steps in (("ragged_tiny", args.steps), ("ragged_extend", max(3, args.steps // 10)),
-                            ("paged_long_b1", args.steps), ("paged_long_b30", args.steps),
-                            ("paged_long_b31", args.steps), ("paged_packed", args.steps),
-                            ("mixed", max(3, args.steps // 10))):
-            extra[name] = measure(name, steps, args.warmup if name != "ragged_extend" else 3,
-                                  world, rank, stream, peak)
-
-    e2e = measure_e2e(HEADLINE, args.steps, args.warmup, rank, stream)
-    base = cpu_baseline(HEADLINE, args.cpu_seconds, rank) if (rank == 0 and world == 1) else None
+        for cname in EXTRA:
+            steps = max(3, args.steps // 4) if cname == "mixed" else args.steps
+            extra[cname] = measure(cname, steps, args.warmup, world, rank, stream, peak, l2, flush)
+            extra[cname]["workload"] = DESCRIPTIONS[cname]
+            if rank == 0 and world == 1:
+                extra[cname]["cpu_baseline"] = cpu_baselines(cname, rank, args.cpu_seconds)
 
     if rank == 0:
         achieved = head["gbs_transform"]
@@ -537,17 +675,16 @@ def main():
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic (seeded torch generators)",
-            "config": {"workload": "PAGED decode B=128 L=8192 k=2048 page_size=64 (random page permutation)",
-                       "global_batch": 128 * world, "seq_len": 8192, "k": 2048,
-                       "parallelism": f"rows x{world} (weak)",
-                       "l2": f"{head['input_sets']} rotating input sets (> 2x L2 per cycle)"},
+            "config": headline_config(world, head["l2"]),
             "hbm_gbs": achieved,
             "hbm_frac_of_nominal_8tbs": head["frac_of_nominal_8tbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profiled_traffic(HEADLINE),
-                         "kernel": "topk_rows_kernel<paged> (transform launches in a CUDA graph, CUDA events)",
-                         "alg_bytes_per_launch": head["alg_bytes_per_step"]},
+                         "traffic": profiled_traffic("topk_rows_kernel", "ragged_extend_chunk"),
+                         "traffic_scope": "one 1024-row launch (ncu), per launch",
+                         "kernel": "topk_rows_kernel<ragged> (transform launches in a CUDA graph, CUDA events)",
+                         "alg_bytes_per_launch": head["alg_bytes_per_step"] // 16,
+                         "us_per_launch": head["us_transform_per_step"] / 16},
             "gpu_launches": head["launches_per_step"] * args.steps,
             "clocks": clk,
             "e2e": e2e,

@@ -15,6 +15,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -152,3 +153,30 @@ def run_workload(w, rows=None, mutant: int = 0):
         raws.append(r)
         errs += e
     return np.concatenate(outs), np.concatenate(raws), errs
+
+
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def run_workload_threads(w, rows=None, threads=None, mutant: int = 0):
+    """``run_workload`` with the rows split into ``threads`` contiguous blocks,
+    each run on its own thread through the unchanged single-threaded routine
+    (the C call releases the GIL, so the blocks run in parallel on the host
+    cores). Returns the same ``(out, out_raw, n_error_rows)`` as
+    ``run_workload`` over ``rows`` (all rows when None), in row order."""
+    if rows is None:
+        rows = np.arange(int(w["batch"]))
+    rows = np.asarray(rows, dtype=np.int64)
+    threads = max(1, min(threads or host_cores(), rows.size))
+    if threads == 1:
+        return run_workload(w, rows=rows, mutant=mutant)
+    blocks = [b for b in np.array_split(rows, threads) if b.size]
+    with ThreadPoolExecutor(len(blocks)) as ex:
+        parts = list(ex.map(lambda b: run_workload(w, rows=b, mutant=mutant), blocks))
+    return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]),
+            sum(p[2] for p in parts))

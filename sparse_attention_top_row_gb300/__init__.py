@@ -84,12 +84,13 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _arg(t, name, dtype=None, numel=0, required=True, dense=True):
+def _arg(t, name, dtype=None, numel=0, required=True, dense=True, device=None):
     """Checks one tensor argument before its pointer crosses the C ABI: a CUDA
-    tensor of the given dtype, at least `numel` elements, dense (row arrays,
-    outputs, the workspace) or with a unit innermost stride (arrays whose row
-    stride is a separate argument). None passes where the argument is optional
-    (or the batch is empty). Raises TypeError / ValueError; returns the pointer.
+    tensor on `device` (the index of the device the call launches on) of the
+    given dtype, at least `numel` elements, dense (row arrays, outputs, the
+    workspace) or with a unit innermost stride (arrays whose row stride is a
+    separate argument). None passes where the argument is optional (or the
+    batch is empty). Raises TypeError / ValueError; returns the pointer.
     The common case costs a handful of attribute reads."""
     if t is None:
         if required and numel > 0:
@@ -97,16 +98,17 @@ def _arg(t, name, dtype=None, numel=0, required=True, dense=True):
         return None
     try:
         ok = ((dtype is None or t.dtype is dtype) and t.is_cuda
+              and (device is None or t.get_device() == device)
               and (t.is_contiguous() if dense else (t.dim() == 0 or t.numel() <= 1 or t.stride(-1) == 1))
               and t.numel() >= numel)
     except AttributeError:
         ok = False
     if not ok:
-        _reject(t, name, dtype, numel, dense)
+        _reject(t, name, dtype, numel, dense, device)
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _reject(t, name, dtype, numel, dense):
+def _reject(t, name, dtype, numel, dense, device=None):
     """Raises the error that says why `t` failed `_arg`."""
     import torch
     if not isinstance(t, torch.Tensor):
@@ -115,6 +117,8 @@ def _reject(t, name, dtype, numel, dense):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (it is on {t.device})")
+    if device is not None and t.get_device() != device:
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, but the call runs on cuda:{device}")
     if dense and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if not dense and t.dim() > 0 and t.numel() > 1 and t.stride(-1) != 1:
@@ -122,26 +126,41 @@ def _reject(t, name, dtype, numel, dense):
     raise ValueError(f"{name} has {t.numel()} elements, fewer than the {numel} required")
 
 
-def _rows(seq_lens):
+def _strided_numel(batch, stride):
+    """Fewest elements a buffer of `batch` rows `stride` apart can hold: the
+    last row starts at (batch - 1) * stride and holds at least one element."""
+    return 0 if batch == 0 else (batch - 1) * max(int(stride), 0) + 1
+
+
+def _rows(seq_lens, device):
     """The batch, from seq_lens (a CUDA int32 vector, one entry per row)."""
     import torch
     if seq_lens is None:
         raise ValueError("seq_lens is required")
-    _arg(seq_lens, "seq_lens", torch.int32)
+    _arg(seq_lens, "seq_lens", torch.int32, device=device)
     return int(seq_lens.numel())
 
 
-def _ws(workspace):
+def _ws(workspace, device=None):
     """The workspace pointer and its size in bytes (any dtype; dense)."""
     if workspace is None:
         raise ValueError("workspace is required")
-    return _arg(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    return _arg(workspace, "workspace", device=device), workspace.numel() * workspace.element_size()
 
 
 def _stream(stream):
+    """The stream handle and the index of the device the call launches on
+    (the current device; a given stream must belong to it). Without CUDA
+    there is no device: the tensor checks then reject every argument (none can
+    be a CUDA tensor) before anything else happens."""
     import torch
+    if not torch.cuda.is_available():
+        return None, None
+    dev = torch.cuda.current_device()
     s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if s.device.index is not None and s.device.index != dev:
+        raise ValueError(f"the stream belongs to cuda:{s.device.index}, but cuda:{dev} is current")
+    return ctypes.c_void_p(s.cuda_stream), dev
 
 
 def _check(fn, status):
@@ -161,9 +180,10 @@ def new_workspace(batch: int, device="cuda"):
 
 def topk_plan(seq_lens, k: int, workspace, stream=None):
     lib = load()
-    batch = _rows(seq_lens)
-    ws, ws_bytes = _ws(workspace)
-    _check("topk_plan", lib.topk_plan(_ptr(seq_lens), batch, int(k), ws, ws_bytes, _stream(stream)))
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
+    ws, ws_bytes = _ws(workspace, dev)
+    _check("topk_plan", lib.topk_plan(_ptr(seq_lens), batch, int(k), ws, ws_bytes, st))
 
 
 def topk_transform_paged(scores, score_stride: int, row_starts, seq_lens, page_table,
@@ -171,14 +191,17 @@ def topk_transform_paged(scores, score_stride: int, row_starts, seq_lens, page_t
                          out_raw=None, flags: int = 0, stream=None):
     import torch
     lib = load()
-    batch = _rows(seq_lens)
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
     i32 = torch.int32
-    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
-            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
-            _arg(page_table, "page_table", i32, 1 if batch else 0, dense=False), int(page_table_stride),
-            int(page_size), batch, int(k), *_ws(workspace), _arg(out, "out", i32, batch * int(k)),
-            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
-    _check("topk_transform_paged", lib.topk_transform_paged(*args, _stream(stream)))
+    args = (_arg(scores, "scores", torch.float32, _strided_numel(batch, score_stride), dense=False, device=dev),
+            int(score_stride), _arg(row_starts, "row_starts", i32, batch, required=False, device=dev),
+            _ptr(seq_lens),
+            _arg(page_table, "page_table", i32, _strided_numel(batch, page_table_stride), dense=False, device=dev),
+            int(page_table_stride), int(page_size), batch, int(k), *_ws(workspace, dev),
+            _arg(out, "out", i32, batch * int(k), device=dev),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
+    _check("topk_transform_paged", lib.topk_transform_paged(*args, st))
 
 
 def topk_transform_paged_packed(scores, score_stride: int, row_starts, seq_lens, page_table,
@@ -186,30 +209,38 @@ def topk_transform_paged_packed(scores, score_stride: int, row_starts, seq_lens,
                                 k: int, workspace, out, out_raw=None, flags: int = 0, stream=None):
     import torch
     lib = load()
-    batch = _rows(seq_lens)
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
     i32 = torch.int32
-    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
-            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
-            _arg(page_table, "page_table", i32, 1 if batch else 0, dense=False), int(page_table_stride),
-            int(page_size), _arg(page_table_row_starts, "page_table_row_starts", i32, batch, required=False),
-            _arg(row_to_batch, "row_to_batch", i32, batch, required=False), batch, int(k),
-            *_ws(workspace), _arg(out, "out", i32, batch * int(k)),
-            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
-    _check("topk_transform_paged_packed", lib.topk_transform_paged_packed(*args, _stream(stream)))
+    # with row_to_batch the table's row count is the caller's; without it,
+    # row b reads table row b
+    pt_rows = (1 if batch else 0) if row_to_batch is not None else batch
+    args = (_arg(scores, "scores", torch.float32, _strided_numel(batch, score_stride), dense=False, device=dev),
+            int(score_stride), _arg(row_starts, "row_starts", i32, batch, required=False, device=dev),
+            _ptr(seq_lens),
+            _arg(page_table, "page_table", i32, _strided_numel(pt_rows, page_table_stride), dense=False,
+                 device=dev),
+            int(page_table_stride), int(page_size),
+            _arg(page_table_row_starts, "page_table_row_starts", i32, batch, required=False, device=dev),
+            _arg(row_to_batch, "row_to_batch", i32, batch, required=False, device=dev), batch, int(k),
+            *_ws(workspace, dev), _arg(out, "out", i32, batch * int(k), device=dev),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
+    _check("topk_transform_paged_packed", lib.topk_transform_paged_packed(*args, st))
 
 
 def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int,
                           workspace, out, out_raw=None, flags: int = 0, stream=None):
     import torch
     lib = load()
-    batch = _rows(seq_lens)
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
     i32 = torch.int32
-    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
-            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
-            _arg(out_offsets, "out_offsets", i32, batch), batch, int(k), *_ws(workspace),
-            _arg(out, "out", i32, batch * int(k)), _arg(out_raw, "out_raw", i32, batch * int(k), required=False),
-            int(flags))
-    _check("topk_transform_ragged", lib.topk_transform_ragged(*args, _stream(stream)))
+    args = (_arg(scores, "scores", torch.float32, _strided_numel(batch, score_stride), dense=False, device=dev),
+            int(score_stride), _arg(row_starts, "row_starts", i32, batch, required=False, device=dev),
+            _ptr(seq_lens), _arg(out_offsets, "out_offsets", i32, batch, device=dev), batch, int(k),
+            *_ws(workspace, dev), _arg(out, "out", i32, batch * int(k), device=dev),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
+    _check("topk_transform_ragged", lib.topk_transform_ragged(*args, st))
 
 
 def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int, out,
@@ -218,13 +249,15 @@ def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_len
     built-in one; batch <= TOPK_NOALLOC_MAX_BATCH). See include/topk.h."""
     import torch
     lib = load()
-    batch = _rows(seq_lens)
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
     i32 = torch.int32
-    args = (_arg(scores, "scores", torch.float32, 1 if batch else 0, dense=False), int(score_stride),
-            _arg(row_starts, "row_starts", i32, batch, required=False), _ptr(seq_lens),
-            _arg(out_offsets, "out_offsets", i32, batch), batch, int(k), _arg(out, "out", i32, batch * int(k)),
-            _arg(out_raw, "out_raw", i32, batch * int(k), required=False), int(flags))
-    _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(*args, _stream(stream)))
+    args = (_arg(scores, "scores", torch.float32, _strided_numel(batch, score_stride), dense=False, device=dev),
+            int(score_stride), _arg(row_starts, "row_starts", i32, batch, required=False, device=dev),
+            _ptr(seq_lens), _arg(out_offsets, "out_offsets", i32, batch, device=dev), batch, int(k),
+            _arg(out, "out", i32, batch * int(k), device=dev),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
+    _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(*args, st))
 
 
 def topk_read_device_errors(workspace, stream=None):
@@ -232,9 +265,9 @@ def topk_read_device_errors(workspace, stream=None):
     lib = load()
     n = ctypes.c_int32(0)
     f = ctypes.c_uint32(0)
-    ws, _ = _ws(workspace)
-    _check("topk_read_device_errors",
-           lib.topk_read_device_errors(ws, ctypes.byref(n), ctypes.byref(f), _stream(stream)))
+    st, dev = _stream(stream)
+    ws, _ = _ws(workspace, dev)
+    _check("topk_read_device_errors", lib.topk_read_device_errors(ws, ctypes.byref(n), ctypes.byref(f), st))
     return int(n.value), int(f.value)
 
 

@@ -94,7 +94,7 @@ def paged_decode(device="cpu", sub_id=0, batch=128, seq_len=8192, k=2048, page_s
 
 
 def ragged_extend(device="cpu", chunk=0, rows_per_chunk=1024, n_req=4, prefix=28672, new=4096,
-                  k=2048, outlier_frac=0.01, outlier_value=4.0):
+                  k=2048, outlier_frac=0.01, outlier_value=4.0, sub_id=None):
     """One chunk of a prefill-extend problem.
 
     ``n_req`` requests, each with a ``prefix``-token cached prefix and ``new``
@@ -104,9 +104,9 @@ def ragged_extend(device="cpu", chunk=0, rows_per_chunk=1024, n_req=4, prefix=28
     row_start. Window scores are N(0,1) with ``outlier_frac`` of them set to
     exactly ``outlier_value``; every other column holds the 1e3 sentinel.
     Chunk c covers global rows c*rows_per_chunk ... and is generated from its
-    own seed, so any chunk can be drawn alone.
+    own seed (sub_id, default c), so any chunk can be drawn alone.
     """
-    g = _gen(device, seed_for(3, chunk))
+    g = _gen(device, seed_for(3, chunk if sub_id is None else sub_id))
     stride = n_req * (prefix + new)
     rows = torch.arange(chunk * rows_per_chunk, (chunk + 1) * rows_per_chunk, device=device)
     req = rows // new
@@ -276,6 +276,37 @@ def custom(mode, k, rows, *, device="cpu", score_stride=None, row_starts=None, o
     return w
 
 
+def pack_windows(w):
+    """The same rows with only their windows kept, packed back to back in one
+    flat buffer: score_stride 0, row_starts = the exclusive prefix sum of
+    seq_lens (so the starts' residues mod 4 vary), every other array as in
+    ``w``. This is the input a caller that holds just the windows would move;
+    RAGGED outputs (position + out_offsets[b]) and PAGED outputs (positions
+    count from the window start) are the same as for ``w``. The 1e3 sentinel
+    pads the tail to a multiple of 4 floats plus 64. Needs seq_lens >= 0 and
+    row_starts >= 0; works on any device."""
+    dev = w["seq_lens"].device
+    B = int(w["batch"])
+    lens = w["seq_lens"].to(torch.int64)
+    if bool((lens < 0).any()):
+        raise ValueError("pack_windows needs non-negative seq_lens")
+    starts = (w["row_starts"].to(torch.int64) if w.get("row_starts") is not None
+              else torch.zeros(B, dtype=torch.int64, device=dev))
+    flat = w["scores"].reshape(-1)
+    total = int(lens.sum().item())
+    new_starts = torch.cumsum(lens, 0) - lens
+    row_of = torch.repeat_interleave(torch.arange(B, device=dev), lens)
+    src = (row_of * int(w["score_stride"]) + starts[row_of] +
+           torch.arange(total, device=dev) - new_starts[row_of])
+    packed = torch.full(((total + 3) // 4 * 4 + 64,), SENTINEL, dtype=torch.float32, device=dev)
+    packed[:total] = flat[src]
+    del src, row_of
+    out = dict(w)
+    out.update(scores=packed, score_stride=0, row_starts=_i32(new_starts),
+               name=w["name"] + " (windows packed)")
+    return out
+
+
 def to_device(w, device):
     """Copy every tensor of a workload to ``device``."""
     return {key: (val.to(device) if isinstance(val, torch.Tensor) else val) for key, val in w.items()}
@@ -302,3 +333,13 @@ def select_rows(w, rows):
     if w.get("page_table") is not None and w.get("row_to_batch") is None:
         out["page_table"] = w["page_table"][idx].clone()  # packed rows keep the request tables
     return out
+
+
+def shard_rows(w, rank, world):
+    """Rank `rank`'s contiguous block of the batch's rows when the rows are
+    partitioned over `world` GPUs (rows are independent: each GPU needs only
+    its rows' scores, lengths, starts, offsets and page-table rows, and no
+    exchange follows). Block r holds rows [r*B//world, (r+1)*B//world)."""
+    B = int(w["batch"])
+    lo, hi = rank * B // world, (rank + 1) * B // world
+    return select_rows(w, range(lo, hi)) if hi > lo else None

@@ -69,7 +69,7 @@ def run_gpu(topk, w, flags, raw=True):
 
 def check_full(topk, w, flags_list=(DET, 0)):
     hw = HostWorkload(w)
-    ref_out, ref_raw, ref_err = oracle.run_workload(w)
+    ref_out, ref_raw, ref_err = oracle.run_workload_threads(w)
     for flags in flags_list:
         o, r, ws = run_gpu(topk, w, flags)
         compare_with_oracle(hw, o, r, ref_out, ref_raw, deterministic=bool(flags & DET))
@@ -311,6 +311,38 @@ def test_no_row_starts_and_no_out_raw(cuda_lib):
     np.testing.assert_array_equal(np.sort(o, axis=1), np.sort(ref_out, axis=1))
 
 
+@pytest.mark.parametrize("route", ["trivial", "register", "streaming", "cluster", "streaming_many"])
+@pytest.mark.parametrize("mode", ["paged", "ragged"])
+def test_without_out_raw_on_every_route(cuda_lib, route, mode):
+    """out_raw = NULL on each route (trivial L <= k; register L <= 8192;
+    streaming longer rows; cluster rows: L > 32768 in a batch of at most 64;
+    streaming_many: the same long rows in a batch of 65, off the cluster
+    path): the outputs alone match the oracle."""
+    rng = np.random.default_rng(len(route) + (7 if mode == "paged" else 0))
+    lens = {"trivial": [1, 300, 512], "register": [513, 4000, 8192], "streaming": [8193, 20000, 32768],
+            "cluster": [32769, 70000, 131072], "streaming_many": [40000] * 65}[route]
+    starts = [int(x) for x in rng.integers(0, 4, size=len(lens))]
+    w = wl.custom(mode, 512, _rows(rng, lens), row_starts=starts,
+                  out_offsets=[int(x) for x in rng.integers(0, 1 << 20, size=len(lens))], page_size=16,
+                  seed=len(lens))
+    ref_out, _, _ = oracle.run_workload_threads(w)
+    for flags in (DET, 0):
+        o, _, _ = run_gpu(cuda_lib, w, flags, raw=False)
+        if flags & DET:
+            np.testing.assert_array_equal(np.sort(o, axis=1), np.sort(ref_out, axis=1))
+        else:  # equal scores may swap: the positions behind the outputs select the same scores
+            hw = HostWorkload(w)
+            for b in range(hw.batch):
+                L = hw.length(b)
+                slots = hw.transform(b, np.arange(L))           # position -> output value
+                pos_of = {int(v): p for p, v in enumerate(slots)}
+                got = [pos_of[int(v)] for v in o[b] if v >= 0]
+                ref = [pos_of[int(v)] for v in ref_out[b] if v >= 0]
+                win = hw.window(b)
+                assert len(got) == len(set(got)) == len(ref), f"row {b}"
+                np.testing.assert_array_equal(np.sort(win[got].view(np.uint32)), np.sort(win[ref].view(np.uint32)))
+
+
 @pytest.mark.parametrize("page_size", [1, 2, 4096, 1 << 19])
 def test_page_sizes(cuda_lib, page_size):
     rng = np.random.default_rng(page_size)
@@ -381,6 +413,43 @@ def test_non_default_stream(cuda_lib):
         out, _, _ = cuda_lib.run_workload(w, flags=DET, stream=s)
     s.synchronize()
     np.testing.assert_array_equal(np.sort(out.cpu().numpy(), 1), np.sort(ref_out, 1))
+
+
+# ---------------------------------------------------------------- full sizes, every row
+
+def _check_every_row(topk, w_dev, flags=(DET, 0)):
+    """The whole launch, as the benchmark times it (one plan + one transform
+    over every row), against the oracle on every row."""
+    assert_windows_in_bounds(w_dev)
+    w_host = wl.to_device(w_dev, "cpu")
+    hw = HostWorkload(w_host)
+    ref_out, ref_raw, ref_err = oracle.run_workload_threads(w_host)
+    B, k = int(w_dev["batch"]), int(w_dev["k"])
+    for f in flags:
+        out = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+        raw = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+        _, _, ws = topk.run_workload(w_dev, out=out, out_raw=raw, flags=f)
+        torch.cuda.synchronize()
+        o, r = out.cpu().numpy(), raw.cpu().numpy()
+        assert not np.any(o == CANARY) and not np.any(r == CANARY)
+        compare_with_oracle(hw, o, r, ref_out, ref_raw, deterministic=bool(f & DET))
+        assert topk.topk_read_device_errors(ws) == (ref_err, 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("chunk", [0, 9])
+def test_full_ragged_extend_chunk_every_row(cuda_lib, chunk):
+    """A full 1024-row chunk of the prefill-extend workload (rows of
+    28673..32768 scores at stride 131072): every row, both modes."""
+    _check_every_row(cuda_lib, wl.ragged_extend("cuda", chunk=chunk))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["paged", "ragged"])
+def test_full_mixed_b1024_k2048_every_row(cuda_lib, mode):
+    """The mixed sweep's largest launch (1024 rows, log-uniform lengths up to
+    131072 plus the boundary rows, k = 2048): every row, both modes."""
+    _check_every_row(cuda_lib, wl.mixed("cuda", mode=mode, k=2048, batch=1024, sub_id=1024))
 
 
 # ---------------------------------------------------------------- full sizes, sampled rows

@@ -79,6 +79,44 @@ def test_noalloc_matches_the_ordinary_entry_points_twice(cuda_lib, flags):
             assert torch.equal((raw >= 0).sum(1), (ref_raw >= 0).sum(1))
 
 
+def _det_equal(a, b):
+    return torch.equal(torch.sort(a, 1).values, torch.sort(b, 1).values)
+
+
+def test_noalloc_back_to_back_on_one_stream(cuda_lib):
+    """Two calls queued on one stream with no synchronisation between them,
+    on batches of different sizes and lengths (so the second call's plan
+    rewrites the row lists the first call's kernels read): stream order alone
+    keeps them apart, and each output matches the ordinary entry points."""
+    lib = cuda_lib.load()
+    a = wl.to_device(wl.mixed("cpu", mode="ragged", k=512, batch=40, max_len=70000, sub_id=11), "cuda")
+    b = wl.to_device(wl.ragged_tiny("cpu", sub_id=4), "cuda")
+    ref_a, _ = _reference(cuda_lib, a, DET)
+    ref_b, _ = _reference(cuda_lib, b, DET)
+    torch.cuda.synchronize()
+    out_a, _ = _noalloc(lib, a, DET)
+    out_b, _ = _noalloc(lib, b, DET)   # queued right behind the first call
+    out_c, _ = _noalloc(lib, a, DET)   # and the first batch once more
+    torch.cuda.synchronize()
+    assert _det_equal(out_a, ref_a) and _det_equal(out_b, ref_b) and _det_equal(out_c, ref_a)
+
+
+def test_noalloc_data_error_row_comes_out_empty(cuda_lib):
+    """A row with a negative length is a data error: its slots all hold -1
+    (this entry point does not report the error count), and the other rows
+    are unaffected."""
+    lib = cuda_lib.load()
+    w = wl.mixed("cpu", mode="ragged", k=256, batch=6, max_len=40000, sub_id=13)
+    w["seq_lens"] = w["seq_lens"].clone()
+    w["seq_lens"][2] = -7
+    d = wl.to_device(w, "cuda")
+    ref_out, _ = _reference(cuda_lib, d, DET)
+    out, raw = _noalloc(lib, d, DET)
+    torch.cuda.synchronize()
+    assert bool((out[2] == -1).all()) and bool((raw[2] == -1).all())
+    assert _det_equal(out, ref_out)
+
+
 def test_noalloc_rejects_a_batch_beyond_its_limit(cuda_lib):
     lib = cuda_lib.load()
     B = cuda_lib.TOPK_NOALLOC_MAX_BATCH + 1

@@ -248,10 +248,9 @@ def input_bytes(w):
 
 
 def transform_kernels(batch):
-    """Kernels one transform of `batch` rows launches (the library's host
-    rule): the rows kernel, plus the cluster kernel for batches of at most 64
-    rows."""
-    return 1 + (1 if batch <= 64 else 0)
+    """Kernels one transform of `batch` rows launches (the library's own
+    count for the current device)."""
+    return topk.topk_transform_launches(batch)
 
 
 class Launch:

@@ -80,6 +80,10 @@ typedef enum {
 #define TOPK_DEVICE_FLAG_INTERNAL 2u      /* an internal consistency check failed (a library
                                              bug): an output slot index was out of range and
                                              the write was dropped */
+#define TOPK_DEVICE_FLAG_TIMEOUT 4u       /* a wait for a bulk copy into shared memory gave up
+                                             after about a second (the copy never completed);
+                                             the kernel went on, so the rows it served are
+                                             unreliable */
 
 /*
  * Bytes of device workspace that topk_plan and the transforms need for
@@ -238,6 +242,16 @@ TOPK_API int topk_transform_ragged_noalloc(const float* scores, int64_t score_st
                                            const int32_t* out_offsets, int32_t batch, int32_t k,
                                            int32_t* out, int32_t* out_raw, uint32_t flags,
                                            topk_stream_t stream);
+
+/*
+ * How many kernels one transform of `batch` rows launches on the current
+ * device (after the plan's one): 1 or 2 (0 for batch <= 0; -1 if the device
+ * cannot be queried). A batch whose every row can own a thread-block cluster
+ * runs in one kernel; batches of up to 64 rows beyond that add the cluster
+ * kernel for their long rows to the per-row kernel. Host only; the first call
+ * on a device sets up the kernels' attributes, like the first transform.
+ */
+TOPK_API int topk_transform_launches(int32_t batch);
 
 /* A static, human-readable name for a topk_status value. Host only. */
 TOPK_API const char* topk_status_string(int status);

@@ -20,6 +20,7 @@ TOPK_MAX_K = 2048
 TOPK_DETERMINISTIC = 1
 TOPK_DEVICE_FLAG_PLAN_MISMATCH = 1
 TOPK_DEVICE_FLAG_INTERNAL = 2
+TOPK_DEVICE_FLAG_TIMEOUT = 4
 
 STATUS = {0: "TOPK_OK", 1: "TOPK_ERR_ARG", 2: "TOPK_ERR_ALIGN", 3: "TOPK_ERR_K",
           4: "TOPK_ERR_PAGE_SIZE", 5: "TOPK_ERR_WORKSPACE", 6: "TOPK_ERR_CUDA"}
@@ -31,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
 
 EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_paged_packed",
             "topk_transform_ragged", "topk_read_device_errors", "topk_status_string",
-            "topk_transform_ragged_noalloc")
+            "topk_transform_ragged_noalloc", "topk_transform_launches")
 TOPK_NOALLOC_MAX_BATCH = 16384
 
 
@@ -74,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.topk_read_device_errors.argtypes = [c_p, ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_p]
         lib.topk_transform_ragged_noalloc.restype = ctypes.c_int
         lib.topk_transform_ragged_noalloc.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_p, c_p, c_u32, c_p]
+        lib.topk_transform_launches.restype = ctypes.c_int
+        lib.topk_transform_launches.argtypes = [c_i32]
         lib.topk_status_string.restype = ctypes.c_char_p
         lib.topk_status_string.argtypes = [ctypes.c_int]
         _LIB = lib
@@ -170,6 +173,15 @@ def _check(fn, status):
 
 def topk_workspace_bytes(batch: int) -> int:
     return int(load().topk_workspace_bytes(int(batch)))
+
+
+def topk_transform_launches(batch: int) -> int:
+    """Kernels one transform of `batch` rows launches on the current device
+    (1 or 2; 0 for an empty batch)."""
+    n = int(load().topk_transform_launches(int(batch)))
+    if n < 0:
+        raise TopKError("topk_transform_launches", 6)
+    return n
 
 
 def new_workspace(batch: int, device="cuda"):

@@ -10,46 +10,54 @@
 // Design (own design for sm_103a; the pages' CUDA/HIP kernels are prior art):
 //
 //  * Keys. A score's fp32 bits map to an order-preserving uint32 key. Every
-//    selection step works on keys, so no score is compared as a float.
-//  * Radix select on a 64-bit composite (key << 32 | ~position). Levels take
-//    12, 8, 8 and 4 bits of the key from the top (the 12-bit first level is
-//    the one the PR #36684 page, "Feature and motivation", describes), then,
+//    selection step works on keys (or on raw bits compared as integers), so no
+//    score is compared as a float.
+//  * Fast path, every non-trivial row: sample, filter, finish.
+//      sample  a strided sample of the window (spread over the whole row) is
+//              histogrammed on the 12-bit key prefix (the 12-bit first digit
+//              of the PR #36684 page, "Feature and motivation") and the bin
+//              holding the sample's expected share of the top-k, plus four
+//              standard deviations, gives a lower bound on the threshold;
+//      filter  one straight-line pass over the window compares every element
+//              with the bound (one integer compare of its raw bits) and
+//              appends the ones at or above it, (raw bits, position), to its
+//              warp's region of a shared-memory candidate buffer: a warp scan
+//              of the per-thread counts orders the slots, the stores are
+//              predicated, nothing branches per element;
+//      finish  the candidates are histogrammed on the 16-bit key prefix
+//              relative to the bound (4096 bins: a 12-bit first digit and a
+//              4-bit second one in one pass), a threshold search finds the
+//              bin where the count from the top reaches k (a warp-shuffle
+//              suffix sum; cf. warp_inclusive_sum on the PR #36684 page,
+//              "Key source snippets"), every candidate above it is written to
+//              a slot taken by a warp-aggregated shared-memory atomic (cf.
+//              warp_sum_bool, same page), and the few members of the
+//              threshold bin are ranked by (key, position), which settles the
+//              remaining 16 key bits and the lowest-position tie-break at once.
+//    The bound is only an estimate, so the fast path checks itself: when the
+//    candidates number fewer than k, overflow their buffer, or crowd one bin
+//    too densely to rank, the row finishes on the exact radix path below
+//    (always exact, only slower).
+//  * Exact radix path: a radix select on the 64-bit composite
+//    (key << 32 | ~position), 12/8/8/4 bits of the key from the top, then,
 //    only when equal scores straddle the threshold and TOPK_DETERMINISTIC is
-//    set, 8/8/8/8 bits of ~position, so the lowest positions win. A level
-//    stops the descent as soon as its threshold bin holds exactly the count
-//    still needed.
-//  * Threshold bin search: for the 4096-bin level every thread owns a run of
-//    bins and a warp-shuffle suffix sum plus one pass over the warp totals
-//    finds the bin where the count from the top first reaches the target
-//    (cf. warp_inclusive_sum on the PR #36684 page, "Key source snippets");
-//    the small levels use one warp.
+//    set, 8/8/8/8 bits of ~position, so the lowest positions win; a level ends
+//    the descent as soon as its threshold bin holds exactly the count still
+//    needed.
 //  * Routes, chosen per row by length (the plan kernel orders rows longest
 //    first and hands long rows of small batches to the cluster path):
 //      trivial   L <= k: positions 0..L-1 then -1, scores never read;
 //      register  L <= 8192: the window lives in registers (16-byte loads);
-//                a 14-bit first digit in packed 16-bit counters finds the
-//                threshold bin, the elements above it go to a slot-ordered
-//                list and the few in it are ranked against each other (every
-//                remaining digit at once); the list is written out coalesced.
-//                Very full threshold bins fall back to the 12-bit levels;
-//      streaming longer rows: one pass over HBM builds the level-1 histogram
-//                while collecting into shared memory every element whose top
-//                12 key bits clear a lower bound estimated from the first tile
-//                of the row; level 2 and the emit then run on that candidate
-//                buffer, and the few elements equal to the 20-bit threshold
-//                prefix are ranked. If the estimate was too high, or the
-//                buffer overflowed, the row is re-read from global memory
-//                (always exact, only slower);
-//      cluster   for few long rows: the same streaming pass split over a
-//                thread-block cluster of 4 CTAs (each slice bounds itself
-//                from its own head tile), histograms merged through
-//                distributed shared memory (reduce-scatter + all-gather) and
-//                output slots allocated with atomics on the leader CTA's
-//                shared memory (cf. TopKCluster on the PR #36684 page). A key
-//                level whose group has no bit set below its digit (scores
-//                rounded to bf16 or coarser) ends the key descent early.
-//  * Compaction uses a warp scan and one shared-memory atomic per warp; the
-//    emit gives slots by a block-wide scan (cf. warp_sum_bool, same page).
+//      streaming longer rows: two register tiles in turn, one loading while
+//                the other is filtered;
+//      cluster   few long rows: each row is cut into slices over a
+//                thread-block cluster of 4 CTAs; each CTA stages its slice in
+//                its own shared memory with 1-D bulk copies (cp.async.bulk,
+//                completing on mbarriers) and filters it from there; the
+//                candidate histograms are summed into every CTA of the
+//                cluster with distributed-shared-memory reductions, and
+//                output slots come from atomics on the leader CTA's shared
+//                memory (cf. TopKCluster on the PR #36684 page).
 //  * PAGED rows copy their page-table entries into shared memory with
 //    cp.async while the scores load, so the emit's lookups stay on chip.
 //  * Unaligned window heads: 16-byte loads start at the aligned address below
@@ -58,8 +66,9 @@
 //  * Every kernel is launched with programmatic dependent launch and waits
 //    (griddepcontrol.wait) before touching global memory, so it is scheduled
 //    while the previous kernel on the stream drains without breaking stream
-//    order. No wait here spins: all waits are __syncthreads, hardware cluster
-//    barriers or that grid dependency.
+//    order. The only spin-waits are on the bulk copies' mbarriers, and each is
+//    bounded: past its limit the kernel flags TOPK_DEVICE_FLAG_TIMEOUT and goes
+//    on, so no wait can hang the GPU.
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -67,6 +76,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "topk.h"
 
@@ -76,17 +86,30 @@ namespace {
 
 constexpr int kThreads = 512;                 // threads per CTA, all routes
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 4096;                   // histogram bins (12-bit digit)
-constexpr int kFineShift = 18;                // register route: a 14-bit first digit ...
-constexpr int kFineWords = 8192;              // ... two 16-bit counters per word
-constexpr int kCandCap = 6144;                // candidate buffer entries per CTA
+constexpr int kBins = 4096;                   // exact path: first radix level (12-bit digit)
+constexpr int kSmall = 256;                   // fast path: sample levels, candidate histogram, later levels
+constexpr int kSmallWords = kSmall + 4;       // + one word counting set bits below a level's digit
+constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per tile
+constexpr int kTileElems = 4 * kTileVecs;
+constexpr int kWarpCap = 512;                 // candidate entries per warp region (single-CTA rows)
+constexpr int kClusterWarpCap = 256;          // ... (a slice of a cluster row)
+constexpr int kXHistWords = kBins + 8;        // exact path: level bins (+ the below count), 16-byte padded
+constexpr int kCandBytes = kWarps * kWarpCap * 8;
+constexpr int kXListCap = (kCandBytes - kXHistWords * 4) / 8;  // exact path: contiguous candidate list
+constexpr int kClusterCandBytes = (kWarps * kClusterWarpCap * 8 > 2 * kXHistWords * 4)
+                                      ? kWarps * kClusterWarpCap * 8 : 2 * kXHistWords * 4;
 constexpr int kPageCache = 4096;              // page-table entries of a row held in shared memory
-constexpr int kTileVecs = 4;                  // 16-byte vectors per thread per streaming step
+constexpr int kClusterPageCache = 2048;       // ... of a slice (cluster kernel)
 constexpr int kClusterSize = 4;               // CTAs per long row on the cluster path
+constexpr int kStageVecs = kTileVecs * kThreads;  // one staged chunk: 2048 vectors (32 KB)
+constexpr int kStages = 4;                    // staged chunks in flight per CTA (128 KB)
 constexpr int kPlanThreads = 1024;
 constexpr int32_t kClusterFloor = 32768;      // rows longer than this may use the cluster path
 constexpr int32_t kClusterMaxBatch = 64;      // ... when the batch is at most this
+constexpr int kMaxRankTies = kThreads;        // largest threshold bin the finish ranks directly
+constexpr int kTieWords = 3 * (kMaxRankTies + 4);  // tie list: keys, positions, rank counters
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr long long kWaitCycles = 1ll << 31;  // bound on an mbarrier wait (about a second)
 
 constexpr int kBandTrivial = 32;              // plan bands: 0..31 by length, then these two
 constexpr int kBandCluster = 33;
@@ -111,47 +134,108 @@ size_t workspace_bytes_for(int32_t batch) {
     return (bytes + 255) / 256 * 256;
 }
 
-// Shared memory carve-up (dynamic). hist/mhist are 4096 counters each, the
-// candidate buffer is (key, position)
-// pairs, then the row's page-table entries (PAGED) and small scratch. The
-// register route overlays its 16384 packed 16-bit counters on the candidate
-// buffer, and the finishes keep their slot-ordered position list in hist's
-// upper half and short tie lists in its lower half.
+// Shared memory carve-up (dynamic), in this order:
+//   stage   the cluster kernel's staged slice chunks (kStages x 32 KB)
+//   cand    per-warp regions of (raw bits, position) on the fast path; the
+//           exact path lays out in the same bytes its 4096-bin level
+//           histogram (xhist; on a cluster also the merged one, xmhist) and a
+//           contiguous (key, position) list (xlist)
+//   pages   the row's (slice's) page-table entries
+//   ties    the threshold bin's members (keys, positions, rank counters)
+//   shist   the two 256-bin levels of the sample histogram
+//   hist    the 256-bin candidate histogram, or a later radix level's bins
+//   mhist   the cluster sum of the candidate histograms or of a later radix
+//           level (cluster kernel)
+//   whist   each warp's own 256-bin candidate histogram
+//   mbar    one mbarrier per stage (cluster kernel)
+//   scratch red (2 words per warp), res (16), cnt (16), wcnt (16)
+// lvl / mlvl name the level histogram and its cluster sum that the radix
+// levels use: hist / mhist, or xhist / xmhist on the exact path.
 struct Shared {
-    uint32_t* hist;      // local histogram
-    uint32_t* mhist;     // merged histogram (== hist on a single CTA)
-    uint32_t* cand_key;
-    int32_t* cand_pos;
-    int32_t* pages;      // kPageCache page-table entries
-    uint32_t* red;       // 2 * kWarps words for scans
-    uint32_t* res;       // threshold search results
-    uint32_t* cnt;       // [0] candidates, [1] definite slots, [2] threshold-group slots
+    float4* stage;       // null in the rows kernel
+    uint2* cand;
+    int32_t* pages;
+    uint8_t* tail;       // ties, shist, hist, mhist, mbar, scratch, at fixed offsets
+    uint32_t* lvl;
+    uint32_t* mlvl;
+    __device__ __forceinline__ uint32_t* ties() const { return reinterpret_cast<uint32_t*>(tail); }
+    __device__ __forceinline__ uint32_t* shist() const { return ties() + kTieWords; }
+    __device__ __forceinline__ uint32_t* hist() const { return shist() + 2 * kSmallWords; }
+    __device__ __forceinline__ uint32_t* mhist() const { return hist() + kSmallWords; }
+    __device__ __forceinline__ uint32_t* whist() const { return mhist() + kSmallWords; }  // kWarps x kSmall
+    __device__ __forceinline__ uint64_t* mbar() const {
+        return reinterpret_cast<uint64_t*>(whist() + kWarps * kSmall);
+    }
+    __device__ __forceinline__ uint32_t* red() const { return reinterpret_cast<uint32_t*>(mbar() + kStages); }
+    __device__ __forceinline__ uint32_t* res() const { return red() + 2 * kWarps; }
+    // [0] exact-path list length, [1] definite slots, [2] tie-list length, [3] overflow flag
+    __device__ __forceinline__ uint32_t* cnt() const { return red() + 2 * kWarps + 16; }
+    __device__ __forceinline__ uint32_t* wcnt() const { return red() + 2 * kWarps + 32; }  // per-warp counts
+    // the row's RowInfo, parked while the score pass needs the registers
+    __device__ __forceinline__ int32_t* row() const { return reinterpret_cast<int32_t*>(red() + 2 * kWarps + 48); }
 };
 
-constexpr size_t kScratchWords = 2 * kWarps + 32;  // red: 2 words per warp; res: 16; cnt: 16
-constexpr size_t kSmemRows = (kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
-constexpr size_t kSmemCluster = (2 * kBins + 2 * kCandCap + kPageCache + kScratchWords) * 4;
+constexpr size_t kScratchWords = 2 * kWarps + 56;
+constexpr size_t kTailBytes = (kTieWords + 4 * kSmallWords + kWarps * kSmall) * 4 + kStages * 8 + kScratchWords * 4;
+constexpr size_t kSmemRows = static_cast<size_t>(kCandBytes) + kPageCache * 4 + kTailBytes;
+constexpr size_t kSmemCluster = static_cast<size_t>(kStages) * kStageVecs * 16 + kClusterCandBytes +
+                                kClusterPageCache * 4 + kTailBytes;
+static_assert(kCandBytes % 16 == 0 && kClusterCandBytes % 16 == 0 && kTieWords % 4 == 0 && kSmallWords % 4 == 0,
+              "16-byte aligned parts");
 
-__device__ __forceinline__ Shared carve(uint8_t* base, bool merged_separate) {
+template <bool kCluster>
+__device__ __forceinline__ Shared carve(uint8_t* base) {
     Shared s;
-    uint32_t* w = reinterpret_cast<uint32_t*>(base);
-    s.hist = w;
-    w += kBins;
-    if (merged_separate) {
-        s.mhist = w;
-        w += kBins;
+    uint8_t* p = base;
+    if (kCluster) {
+        s.stage = reinterpret_cast<float4*>(p);
+        p += static_cast<size_t>(kStages) * kStageVecs * 16;
     } else {
-        s.mhist = s.hist;
+        s.stage = nullptr;
     }
-    s.cand_key = w;
-    w += kCandCap;
-    s.cand_pos = reinterpret_cast<int32_t*>(w);
-    w += kCandCap;
-    s.pages = reinterpret_cast<int32_t*>(w);
-    w += kPageCache;
-    s.red = w;
-    s.res = w + 2 * kWarps;
-    s.cnt = w + 2 * kWarps + 16;
+    s.cand = reinterpret_cast<uint2*>(p);
+    p += kCluster ? kClusterCandBytes : kCandBytes;
+    s.pages = reinterpret_cast<int32_t*>(p);
+    p += static_cast<size_t>(kCluster ? kClusterPageCache : kPageCache) * 4;
+    s.tail = p;
+    s.lvl = s.hist();
+    s.mlvl = kCluster ? s.mhist() : s.hist();
+    return s;
+}
+
+// The exact path's view: 4096-bin levels in the candidate bytes (on a
+// cluster also their sum, kXHistWords further on), the contiguous list after
+// the first.
+__device__ __forceinline__ Shared exact_view(const Shared& sh, bool cluster) {
+    Shared x = sh;
+    x.lvl = reinterpret_cast<uint32_t*>(sh.cand);
+    x.mlvl = cluster ? x.lvl + kXHistWords : x.lvl;
+    return x;
+}
+__device__ __forceinline__ uint2* exact_list(const Shared& sh) {
+    return reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(sh.cand) + kXHistWords);
+}
+
+// The dynamic shared memory of every kernel here. Every address in it is
+// this symbol plus a constant of the kernel's layout, so a route rebuilds its
+// Shared from the layout where it needs it instead of keeping pointers live.
+extern __shared__ __align__(128) uint8_t g_smem[];
+
+// Layouts: the rows kernel; the cluster kernel; the cluster kernel's view
+// for a single-CTA row (rows-kernel buffers inside the idle stage area).
+enum Layout { kLayRows = 0, kLayCluster = 1, kLayClusterSolo = 2 };
+
+template <int kLay>
+__device__ __forceinline__ Shared layout() {
+    if (kLay == kLayRows) return carve<false>(g_smem);
+    Shared s = carve<true>(g_smem);
+    if (kLay == kLayClusterSolo) {
+        static_assert(kCandBytes + kPageCache * 4 <= kStages * kStageVecs * 16, "solo buffers fit the stages");
+        s.cand = reinterpret_cast<uint2*>(s.stage);
+        s.pages = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(s.stage) + kCandBytes);
+        s.lvl = s.hist();
+        s.mlvl = s.hist();
+    }
     return s;
 }
 
@@ -180,22 +264,13 @@ struct Params {
 // small device helpers
 // ----------------------------------------------------------------------------
 
-// Order-preserving fp32 -> uint32: flip all bits of negatives, set the sign bit
-// of non-negatives.
-__device__ __forceinline__ uint32_t score_key(float x) {
-    const uint32_t b = __float_as_uint(x);
+// Order-preserving fp32 bits -> uint32: flip all bits of negatives, set the
+// sign bit of non-negatives.
+__device__ __forceinline__ uint32_t bits_key(uint32_t b) {
     return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
 }
 
-__device__ __forceinline__ float4 load_stream(const float4* p) {
-    float4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-        : "l"(p));
-    return r;
-}
-
-// The same 16 bytes as raw integer bits (keys and key compares are integer
+// 16 bytes of scores as raw integer bits (keys and key compares are integer
 // work; the bits never pass through a float register).
 __device__ __forceinline__ int4 load_stream_bits(const float4* p) {
     int4 r;
@@ -205,10 +280,6 @@ __device__ __forceinline__ int4 load_stream_bits(const float4* p) {
     return r;
 }
 
-// Order-preserving key of raw fp32 bits (same map as score_key).
-__device__ __forceinline__ uint32_t bits_key(uint32_t b) {
-    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
-}
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
@@ -231,12 +302,41 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, int32_t pos) {
     return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~pos);
 }
 
-// Radix levels over the 64-bit composite: 12/8/8/4 bits of the key, then
-// 8/8/8/8 bits of ~position (deterministic tie-break only).
-constexpr int kKeyLevels = 4;
-constexpr int kAllLevels = 8;
+// Shared-memory access through 32-bit shared addresses (the hot loops name
+// the state space explicitly instead of relying on generic addressing).
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void red_add_shared(uint32_t a, uint32_t v) {
+    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+    return v;
+}
+
+// Radix levels over the 64-bit composite (key << 32 | ~position). Level i
+// takes `bins` values of the digit at composite bit `shift`:
+//   0..3  the key from scratch: 12, 8, 8, 4 bits;
+//   4..5  the key's low 16 bits once its 16-bit prefix is known: 8, 8 bits;
+//   6..9  ~position, 8 bits each (deterministic tie-break only).
+constexpr int kLvlKey12 = 0, kLvlKeyLast = 3, kLvlLow16 = 4, kLvlLow16Last = 5, kLvlPos = 6, kLvlPosLast = 9;
 __device__ __forceinline__ int level_shift(int lvl) {
-    return lvl == 0 ? 52 : lvl == 1 ? 44 : lvl == 2 ? 36 : lvl == 3 ? 32 : 8 * (7 - lvl);
+    switch (lvl) {
+        case 0: return 52;
+        case 1: return 44;
+        case 2: return 36;
+        case 3: return 32;
+        case 4: return 40;
+        case 5: return 32;
+        default: return 8 * (9 - lvl);
+    }
 }
 __device__ __forceinline__ int level_bins(int lvl) { return lvl == 0 ? kBins : lvl == 3 ? 16 : 256; }
 
@@ -257,7 +357,7 @@ struct Threshold {
 
 // First half of the 4096-bin search: every thread returns the histogram's
 // total and the thread whose run crosses the target writes the bin to
-// sh.res. One barrier (after it every bin has been read); the caller reads
+// sh.res(). One barrier (after it every bin has been read); the caller reads
 // the result with find_wide_result after a barrier of its own.
 __device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const Shared& sh) {
     constexpr int R = kBins / kThreads;  // bins per thread
@@ -279,12 +379,12 @@ __device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const 
         const uint32_t y = __shfl_down_sync(kFull, x, off);
         if (lane + off < 32) x += y;
     }
-    if (lane == 0) sh.red[warp] = x;
+    if (lane == 0) sh.red()[warp] = x;
     __syncthreads();
     uint32_t above = 0, total = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-        const uint32_t r = sh.red[w];
+        const uint32_t r = sh.red()[w];
         total += r;
         above += w > warp ? r : 0u;
     }
@@ -294,9 +394,9 @@ __device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const 
 #pragma unroll
         for (int i = R - 1; i >= 0; --i) {
             if (r + b[i] >= target) {
-                sh.res[0] = R * threadIdx.x + static_cast<uint32_t>(i);
-                sh.res[1] = r;
-                sh.res[2] = b[i];
+                sh.res()[0] = R * threadIdx.x + static_cast<uint32_t>(i);
+                sh.res()[1] = r;
+                sh.res()[2] = b[i];
                 break;
             }
             r += b[i];
@@ -307,68 +407,7 @@ __device__ uint32_t find_wide_publish(const uint32_t* h, uint32_t target, const 
 
 __device__ __forceinline__ Threshold find_wide_result(uint32_t total, uint32_t target, const Shared& sh) {
     if (total < target) return Threshold{0u, total, 0u, false};
-    return Threshold{sh.res[0], sh.res[1], sh.res[2], true};
-}
-
-// find_wide_publish for the register route's 16384 bins of 16-bit counters,
-// two per word (bin 2w in the low half of word w): thread t holds words
-// 16t..16t+15. Per-thread sums add whole words (each half stays below 2^16:
-// a row holds at most 8192 elements).
-__device__ uint32_t find_fine_publish(const uint32_t* h, uint32_t target, const Shared& sh) {
-    constexpr int W = kFineWords / kThreads;
-    static_assert(W % 4 == 0 && W * kThreads == kFineWords, "whole 16-byte runs of words per thread");
-    const uint32_t lane = lane_id();
-    const int warp = static_cast<int>(threadIdx.x >> 5);
-    uint32_t wd[W];
-#pragma unroll
-    for (int q = 0; q < W / 4; ++q) {
-        const uint4 u = reinterpret_cast<const uint4*>(h)[(W / 4) * threadIdx.x + q];
-        wd[4 * q] = u.x, wd[4 * q + 1] = u.y, wd[4 * q + 2] = u.z, wd[4 * q + 3] = u.w;
-    }
-    uint32_t pair = 0;
-#pragma unroll
-    for (int i = 0; i < W; ++i) pair += wd[i];
-    const uint32_t s32 = (pair & 0xFFFFu) + (pair >> 16);
-    uint32_t x = s32;  // sum over the lanes >= this lane
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_down_sync(kFull, x, off);
-        if (lane + off < 32) x += y;
-    }
-    if (lane == 0) sh.red[warp] = x;
-    __syncthreads();
-    uint32_t above = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint32_t r = sh.red[w];
-        total += r;
-        above += w > warp ? r : 0u;
-    }
-    const uint32_t incl = above + x, excl = incl - s32;
-    if (excl < target && incl >= target) {
-        // the word first (both halves at once), then the half; the run ends
-        // in word 0 at the latest
-        uint32_t r = excl, wsel = 0, rsel = 0;
-        int isel = 0;
-        bool done = false;
-#pragma unroll
-        for (int i = W - 1; i >= 0; --i) {
-            const uint32_t c2 = (wd[i] & 0xFFFFu) + (wd[i] >> 16);
-            if (!done && (i == 0 || r + c2 >= target)) {
-                wsel = wd[i];
-                isel = i;
-                rsel = r;
-                done = true;
-            }
-            r += c2;
-        }
-        const uint32_t hi = wsel >> 16, lo = wsel & 0xFFFFu;
-        const bool in_hi = rsel + hi >= target;
-        sh.res[0] = 2 * (W * threadIdx.x + static_cast<uint32_t>(isel)) + (in_hi ? 1u : 0u);
-        sh.res[1] = in_hi ? rsel : rsel + hi;
-        sh.res[2] = in_hi ? hi : lo;
-    }
-    return total;
+    return Threshold{sh.res()[0], sh.res()[1], sh.res()[2], true};
 }
 
 __device__ Threshold find_threshold_wide(const uint32_t* h, uint32_t target, const Shared& sh) {
@@ -410,9 +449,9 @@ __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, 
 #pragma unroll
                     for (int i = 7; i >= 0; --i) {
                         if (r + b[i] >= target) {
-                            sh.res[0] = static_cast<uint32_t>(lo + i);
-                            sh.res[1] = r;
-                            sh.res[2] = b[i];
+                            sh.res()[0] = static_cast<uint32_t>(lo + i);
+                            sh.res()[1] = r;
+                            sh.res()[2] = b[i];
                             break;
                         }
                         r += b[i];
@@ -424,19 +463,19 @@ __device__ Threshold find_threshold(const uint32_t* h, int nb, uint32_t target, 
         }
         if (lane == 0) {
             if (!found) {
-                sh.res[0] = 0;
-                sh.res[1] = run;
-                sh.res[2] = 0;
+                sh.res()[0] = 0;
+                sh.res()[1] = run;
+                sh.res()[2] = 0;
             }
-            sh.res[3] = found ? 1u : 0u;
+            sh.res()[3] = found ? 1u : 0u;
         }
     }
     __syncthreads();
-    return Threshold{sh.res[0], sh.res[1], sh.res[2], sh.res[3] != 0};
+    return Threshold{sh.res()[0], sh.res()[1], sh.res()[2], sh.res()[3] != 0};
 }
 
-__device__ __forceinline__ void clear_hist(uint32_t* h, int nb) {
-    for (int i = threadIdx.x; i < nb / 4; i += kThreads) reinterpret_cast<uint4*>(h)[i] = make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void clear_words(uint32_t* h, int n) {
+    for (int i = threadIdx.x; i < n / 4; i += kThreads) reinterpret_cast<uint4*>(h)[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Sum over the CTA of h[c] for c >= from (bins of the local histogram).
@@ -447,176 +486,154 @@ __device__ uint32_t count_from(const uint32_t* h, int nb, uint32_t from, const S
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
     __syncthreads();
-    if (lane_id() == 0) sh.red[threadIdx.x >> 5] = s;
+    if (lane_id() == 0) sh.red()[threadIdx.x >> 5] = s;
     __syncthreads();
     uint32_t t = 0;
-    for (int w = 0; w < kWarps; ++w) t += sh.red[w];
+    for (int w = 0; w < kWarps; ++w) t += sh.red()[w];
     __syncthreads();
     return t;
 }
 
 // ----------------------------------------------------------------------------
-// merge policies: a single CTA, or a thread-block cluster over DSMEM
+// merge policies of the exact radix path: a single CTA, or a thread-block
+// cluster over distributed shared memory
 // ----------------------------------------------------------------------------
 
 struct SoloMerge {
     static constexpr bool kSolo = true;
     __device__ __forceinline__ const uint32_t* merge(const Shared& sh, int) const {
         __syncthreads();
-        return sh.hist;
+        return sh.lvl;
     }
-    // The level-1 merge: this CTA's bound and overflow flag are the row's.
-    __device__ __forceinline__ const uint32_t* merge_level1(const Shared& sh, uint32_t bound, bool ovf,
-                                                            uint32_t& max_bound, bool& any_ovf) const {
-        max_bound = bound;
-        any_ovf = ovf;
-        return merge(sh, kBins);
-    }
-    __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt[i]; }
+    __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const { return &sh.cnt()[i]; }
 };
 
 struct ClusterMerge {
     static constexpr bool kSolo = false;
-    // hist (local) -> mhist (sum over the cluster), identical in every CTA.
+    // lvl (local) -> mlvl (sum over the cluster), identical in every CTA.
     // CTA r sums the 16-byte words w = r, r + kClusterSize, ... over all CTAs
     // (reduce-scatter); then every CTA gathers the words it does not own.
     __device__ const uint32_t* merge(const Shared& sh, int nb) const {
-        cg::this_cluster().sync();  // every local histogram is complete
-        return merge_words(sh, 0, nb / 4);
-    }
-    // The level-1 merge limited to the bins the slices' candidates occupy:
-    // each CTA publishes its bound, its highest occupied bin and its overflow
-    // flag, and only 16-byte words from the highest bound to the highest bin
-    // are summed (mhist is zero elsewhere: it is cleared at the row's start).
-    // Bins below the highest bound cannot hold an exact level-1 threshold.
-    __device__ const uint32_t* merge_level1(const Shared& sh, uint32_t bound, bool ovf, uint32_t& max_bound,
-                                            bool& any_ovf) const {
         cg::cluster_group cluster = cg::this_cluster();
-        // highest occupied bin at or above the bound
-        uint32_t top = 0;
-        for (int b = kBins - 1 - static_cast<int>(threadIdx.x); b >= static_cast<int>(bound); b -= kThreads)
-            if (sh.hist[b] != 0u) {
-                top = static_cast<uint32_t>(b);
-                break;
-            }
-        top = __reduce_max_sync(kFull, top);
-        if (lane_id() == 0 && top != 0u) atomicMax(&sh.cnt[5], top);
-        if (threadIdx.x == 0) {
-            sh.cnt[4] = bound;
-            sh.cnt[6] = ovf ? 1u : 0u;
-        }
-        cluster.sync();  // every local histogram and every published word is complete
-        uint32_t lo = 0, hi = 0, o = 0;
-#pragma unroll
-        for (int q = 0; q < kClusterSize; ++q) {
-            const uint32_t* c = cluster.map_shared_rank(sh.cnt, q);
-            lo = max(lo, c[4]);
-            hi = max(hi, c[5]);
-            o |= c[6];
-        }
-        max_bound = lo;
-        any_ovf = o != 0u;
-        hi = max(hi, lo);
-        return merge_words(sh, static_cast<int>(lo / 4), static_cast<int>(hi / 4) + 1);
-    }
-    // Sums the 16-byte words [w0, w1) of the CTAs' histograms into mhist; the
-    // CTAs must have passed a cluster barrier since their last histogram write.
-    __device__ const uint32_t* merge_words(const Shared& sh, int w0, int w1) const {
-        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every local histogram is complete
         const int rank = static_cast<int>(cluster.block_rank());
-        const int words = w1;
-        for (int w = w0 + ((rank - w0 % kClusterSize + kClusterSize) % kClusterSize) +
-                     kClusterSize * static_cast<int>(threadIdx.x);
-             w < words; w += kClusterSize * kThreads) {
+        const int words = nb / 4;
+        for (int w = rank + kClusterSize * static_cast<int>(threadIdx.x); w < words; w += kClusterSize * kThreads) {
             uint4 t = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int q = 0; q < kClusterSize; ++q) {
-                const uint4 r = reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.hist, q))[w];
+                const uint4 r = reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.lvl, q))[w];
                 t.x += r.x, t.y += r.y, t.z += r.z, t.w += r.w;
             }
-            reinterpret_cast<uint4*>(sh.mhist)[w] = t;
+            reinterpret_cast<uint4*>(sh.mlvl)[w] = t;
         }
         cluster.sync();  // every owned word of the sum is complete
-        for (int w = w0 + static_cast<int>(threadIdx.x); w < words; w += kThreads) {
+        for (int w = static_cast<int>(threadIdx.x); w < words; w += kThreads) {
             const int q = w % kClusterSize;
             if (q != rank)
-                reinterpret_cast<uint4*>(sh.mhist)[w] =
-                    reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.mhist, q))[w];
+                reinterpret_cast<uint4*>(sh.mlvl)[w] =
+                    reinterpret_cast<const uint4*>(cluster.map_shared_rank(sh.mlvl, q))[w];
         }
         __syncthreads();
-        return sh.mhist;
+        return sh.mlvl;
     }
     __device__ __forceinline__ uint32_t* counter(const Shared& sh, int i) const {
-        return cg::this_cluster().map_shared_rank(&sh.cnt[i], 0);
+        return cg::this_cluster().map_shared_rank(&sh.cnt()[i], 0);
     }
 };
 
 // ----------------------------------------------------------------------------
-// element sources: registers, the candidate buffer, global memory
+// element sources of the exact path: registers, a candidate list, the
+// per-warp candidate regions, shared memory, global memory. visit(f) calls
+// f(key, position, valid) with a fixed thread-to-element assignment.
 // ----------------------------------------------------------------------------
 
 // Register tile: v[u] holds vector j = u*kThreads + tid of the aligned window.
-template <int NV>
 struct RegSource {
-    const float4 (&v)[NV];
+    const int4 (&v)[kTileVecs];
     int rem, len;
     template <class F>
     __device__ __forceinline__ void visit(F&& f) const {
 #pragma unroll
-        for (int u = 0; u < NV; ++u) {
-            const int j = u * kThreads + static_cast<int>(threadIdx.x);
-            const int p0 = 4 * j - rem;
-            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int u = 0; u < kTileVecs; ++u) {
+            const int p0 = 4 * (u * kThreads + static_cast<int>(threadIdx.x)) - rem;
+            const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int p = p0 + c;
-                f(score_key(e[c]), p, static_cast<unsigned>(p) < static_cast<unsigned>(len));
+                f(bits_key(static_cast<uint32_t>(e[c])), p, static_cast<unsigned>(p) < static_cast<unsigned>(len));
             }
         }
     }
 };
 
+// A contiguous list of n (key, position) entries.
 struct CandSource {
-    const uint32_t* key;
-    const int32_t* pos;
+    const uint2* c;
     uint32_t n;
     template <class F>
     __device__ __forceinline__ void visit(F&& f) const {
         const uint32_t n_round = (n + kThreads - 1) / kThreads * kThreads;
         for (uint32_t i = threadIdx.x; i < n_round; i += kThreads) {
             const bool valid = i < n;
-            f(valid ? key[i] : 0u, valid ? pos[i] : 0, valid);
+            const uint2 e = valid ? c[i] : make_uint2(0u, 0u);
+            f(e.x, static_cast<int32_t>(e.y), valid);
         }
     }
 };
 
-// Global memory: vectors [jb, je) of the aligned window, re-read.
-struct GlobalSource {
+// The per-warp candidate regions of the fast path, (raw bits, position):
+// each warp visits its own region.
+struct RegionSource {
+    const uint2* c;  // region 0; region w at c + w * cap
+    const uint32_t* wcnt;
+    int cap;
+    template <class F>
+    __device__ __forceinline__ void visit(F&& f) const {
+        const int warp = static_cast<int>(threadIdx.x >> 5);
+        const uint2* r = c + warp * cap;
+        const uint32_t n = min(wcnt[warp], static_cast<uint32_t>(cap));
+        const uint32_t n_round = (n + 31u) & ~31u;
+        for (uint32_t i = lane_id(); i < n_round; i += 32) {
+            const bool valid = i < n;
+            const uint2 e = valid ? r[i] : make_uint2(0u, 0u);
+            f(bits_key(e.x), static_cast<int32_t>(e.y), valid);
+        }
+    }
+};
+
+// Vectors [jb, je) of the aligned window from a base (global or shared).
+template <bool kGlobal>
+struct VecSource {
     const float4* vbase;
     int jb, je, rem, len;
     template <class F>
     __device__ __forceinline__ void visit(F&& f) const {
         for (int j0 = jb; j0 < je; j0 += kTileVecs * kThreads) {
-            float4 v[kTileVecs];
+            int4 v[kTileVecs];
 #pragma unroll
             for (int u = 0; u < kTileVecs; ++u) {
                 const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-                v[u] = j < je ? load_stream(vbase + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[u] = j >= je ? make_int4(0, 0, 0, 0)
+                       : kGlobal ? load_stream_bits(vbase + j)
+                                 : reinterpret_cast<const int4*>(vbase)[j];
             }
 #pragma unroll
             for (int u = 0; u < kTileVecs; ++u) {
                 const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
                 const int p0 = 4 * j - rem;
-                const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int p = p0 + c;
-                    f(score_key(e[c]), p, j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len));
+                    f(bits_key(static_cast<uint32_t>(e[c])), p,
+                      j < je && static_cast<unsigned>(p) < static_cast<unsigned>(len));
                 }
             }
         }
     }
 };
+using GlobalSource = VecSource<true>;
 
 // ----------------------------------------------------------------------------
 // selection state and the radix levels
@@ -641,22 +658,25 @@ __device__ __forceinline__ void apply_level(SelState& st, int lvl, const Thresho
     st.exact = (t.count == st.need);
 }
 
-// Levels first..last of the radix descent, stopping once exact. A key level
-// also counts, in the word after its bins, the elements of the current group
-// with any key bit below its digit set; when the merged count is 0 every such
-// bit is 0 throughout the group (scores rounded to bf16 or coarser), so the
-// key is settled and the remaining key levels are skipped.
+// Key levels first..last_key, then (det) the position levels, stopping once
+// exact. A key level also counts, in the word after its bins, the elements
+// of the current group with any key bit below its digit set; when the merged
+// count is 0 every such bit is 0 throughout the group (scores rounded to bf16
+// or coarser), so the key is settled and the remaining key levels are skipped.
 template <class Merge, class Src>
-__device__ void run_levels(SelState& st, int first, int last, const Src& src, const Shared& sh,
+__device__ void run_levels(SelState& st, int first, int last_key, bool det, const Src& src, const Shared& sh,
                            const Merge& mg) {
-    for (int lvl = first; lvl <= last && !st.exact; ++lvl) {
+    int lvl = first;
+    while (!st.exact) {
+        if (lvl > last_key && lvl < kLvlPos) lvl = kLvlPos;
+        if (lvl > kLvlPosLast || (lvl >= kLvlPos && !det)) break;
         const int nb = level_bins(lvl);
         const int shift = level_shift(lvl);
-        uint32_t* hist = sh.hist;
+        uint32_t* hist = sh.lvl;
         const uint32_t digit = static_cast<uint32_t>(nb - 1);
-        const bool key_level = lvl < kKeyLevels;
+        const bool key_level = lvl < kLvlPos;
         const int words = key_level ? nb + 4 : nb;
-        clear_hist(sh.hist, words);
+        clear_words(sh.lvl, words);
         __syncthreads();
         uint32_t below = 0;
         if (key_level) {  // key digits: a 32-bit filter on the resolved key bits
@@ -683,9 +703,11 @@ __device__ void run_levels(SelState& st, int first, int last, const Src& src, co
         const bool settled = key_level && merged[nb] == 0u;  // read before find's barrier
         const Threshold t = find_threshold(merged, nb, st.need, sh);
         apply_level(st, lvl, t);
-        if (settled && lvl < kKeyLevels - 1) {
+        if (settled) {
             st.mask |= static_cast<uint64_t>(below) << 32;  // those bits are 0 in the prefix too
-            lvl = kKeyLevels - 1;
+            lvl = kLvlPos;
+        } else {
+            ++lvl;
         }
     }
 }
@@ -696,49 +718,29 @@ struct Emitter {
     int32_t* out;
     int32_t* out_raw;
     const int32_t* pt_row;     // the row's page-table row (packed rows: its request's)
-    const int32_t* pt_cached;  // the row's page-table entries from pt_first on, in shared memory, or null
+    const int32_t* pt_cached;  // page-table entries from pt_first on, in shared memory, or null
     int32_t token0;            // page-table token of position 0 (0 unless packed)
-    int32_t pt_first;          // first page-table entry the window touches
+    int32_t pt_first;          // first page-table entry held in pt_cached
+    int32_t pt_count;          // entries held in pt_cached
     int32_t page_bits;
     int32_t offset;
     uint32_t k;
     uint32_t* flags;  // device flags word of the workspace
+    __device__ __forceinline__ int32_t value(int32_t pos) const {
+        if (!kPaged) return pos + offset;
+        const int32_t t = pos + token0;
+        const int32_t q = t >> page_bits;
+        const uint32_t c = static_cast<uint32_t>(q - pt_first);
+        const int32_t page = (pt_cached && c < static_cast<uint32_t>(pt_count)) ? pt_cached[c] : __ldg(pt_row + q);
+        return (page << page_bits) | (t & ((1 << page_bits) - 1));
+    }
     __device__ __forceinline__ void write(uint32_t slot, int32_t pos) const {
         if (slot >= k) {  // never taken when the selection is consistent
             atomicOr(flags, TOPK_DEVICE_FLAG_INTERNAL);
             return;
         }
-        int32_t v;
-        if (kPaged) {
-            const int32_t t = pos + token0;
-            const int32_t page = pt_cached ? pt_cached[(t >> page_bits) - pt_first] : __ldg(pt_row + (t >> page_bits));
-            v = (page << page_bits) | (t & ((1 << page_bits) - 1));
-        } else {
-            v = pos + offset;
-        }
-        out[slot] = v;
+        out[slot] = value(pos);
         if (out_raw) out_raw[slot] = pos;
-    }
-    // Straight-line form for loops over candidates: writes when `w` (and the
-    // slot is in range); every load it makes is in bounds whether or not it
-    // writes. The caller reports out-of-range slots (see flag_if).
-    __device__ __forceinline__ void write_if(bool w, uint32_t slot, int32_t pos) const {
-        const bool ok = w && slot < k;
-        int32_t v;
-        if (kPaged) {
-            const int32_t t = pos + token0;
-            const int32_t q = ok ? (t >> page_bits) : pt_first;  // pt_first exists: the row is not empty
-            const int32_t page = pt_cached ? pt_cached[q - pt_first] : __ldg(pt_row + q);
-            v = (page << page_bits) | (t & ((1 << page_bits) - 1));
-        } else {
-            v = pos + offset;
-        }
-        if (ok) out[slot] = v;
-        if (ok && out_raw) out_raw[slot] = pos;
-    }
-    // Reports an out-of-range slot found by a caller that assigns slots itself.
-    __device__ __forceinline__ void flag_if(bool bad) const {
-        if (bad) atomicOr(flags, TOPK_DEVICE_FLAG_INTERNAL);
     }
 };
 
@@ -751,9 +753,6 @@ struct Emitter {
 template <bool kPaged, class Merge, class Src>
 __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, const Shared& sh,
                               const Merge& mg, const Emitter<kPaged>& em) {
-    // this thread's page-table copies have landed; the barrier after the
-    // counting pass publishes them to the CTA
-    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");
     const uint32_t need = st.need;
     const bool exact = st.exact;
     const bool key_only = static_cast<uint32_t>(st.mask) == 0;  // only key levels ran
@@ -763,8 +762,9 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
     // compare against the prefix (exact) or tau
     auto classify = [&](uint32_t key, int32_t pos, bool valid, bool& def, bool& grp) {
         if (key_only) {
-            def = valid && (exact ? key >= pfx : key > pfx);
-            grp = valid && !exact && key == pfx;
+            const uint32_t hk = key & static_cast<uint32_t>(mask >> 32);
+            def = valid && (exact ? hk >= pfx : hk > pfx);
+            grp = valid && !exact && hk == pfx;
         } else {
             const uint64_t hi = composite(key, pos) & mask;
             def = valid && (hi > prefix || (exact && hi == prefix));
@@ -781,14 +781,14 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
     const uint32_t xd = warp_inclusive_scan(nd), xg = warp_inclusive_scan(ng);
     const int warp = static_cast<int>(threadIdx.x >> 5);
     if (lane_id() == 31) {
-        sh.red[warp] = xd;
-        sh.red[kWarps + warp] = xg;
+        sh.red()[warp] = xd;
+        sh.red()[kWarps + warp] = xg;
     }
     __syncthreads();
     uint32_t bd = xd - nd, bg = xg - ng, td = 0, tg = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-        const uint32_t rd = sh.red[w], rg = sh.red[kWarps + w];
+        const uint32_t rd = sh.red()[w], rg = sh.red()[kWarps + w];
         bd += w < warp ? rd : 0u;
         bg += w < warp ? rg : 0u;
         td += rd;
@@ -797,12 +797,12 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
     if (!Merge::kSolo) {  // this CTA's share of the cluster-wide slot ranges
         __syncthreads();
         if (threadIdx.x == 0) {
-            sh.red[0] = td ? atomicAdd(mg.counter(sh, 1), td) : 0u;
-            sh.red[1] = tg ? atomicAdd(mg.counter(sh, 2), tg) : 0u;
+            sh.red()[0] = td ? atomicAdd(mg.counter(sh, 1), td) : 0u;
+            sh.red()[1] = tg ? atomicAdd(mg.counter(sh, 2), tg) : 0u;
         }
         __syncthreads();
-        bd += sh.red[0];
-        bg += sh.red[1];
+        bd += sh.red()[0];
+        bg += sh.red()[1];
     }
     src.visit([&](uint32_t key, int32_t pos, bool valid) {
         bool d, g;
@@ -816,10 +816,6 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
     __syncthreads();  // red is free again
 }
 
-// ----------------------------------------------------------------------------
-// routes
-// ----------------------------------------------------------------------------
-
 template <bool kPaged>
 __device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em) {
     for (uint32_t t = threadIdx.x; t < k; t += kThreads) {
@@ -832,125 +828,18 @@ __device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em) 
     }
 }
 
-
-
-
-
-// Raw bits of one tile: kTileVecs vectors per thread from vector j0 (vectors
-// at or past je read as zero bits and are never in the window).
-__device__ __forceinline__ void load_bits(int4 (&v)[kTileVecs], const float4* vbase, int j0, int je) {
-#pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        v[u] = j < je ? load_stream_bits(vbase + j) : make_int4(0, 0, 0, 0);
-    }
-}
-
-__device__ __forceinline__ int tile_elem(const int4 (&v)[kTileVecs], int e) {
-    const int4 q = v[e / 4];
-    return (e % 4) == 0 ? q.x : (e % 4) == 1 ? q.y : (e % 4) == 2 ? q.z : q.w;
-}
-
-// Bit e set: element e of this thread's tile at vector j0 lies in the window
-// (vector u of the tile holds positions 4j - rem .. 4j - rem + 3 for
-// j = j0 + u * kThreads + tid; vectors at or past je are not in it).
-__device__ __forceinline__ uint32_t tile_valid(int j0, int je, int rem, int len) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int u = 0; u < kTileVecs; ++u) {
-        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
-        const int lo = 4 * j - rem;
-        const int a = max(-lo, 0), b = min(len - lo, 4);  // lanes [a, b) are in the window
-        const uint32_t vm = (j < je && a < b) ? (1u << b) - (1u << a) : 0u;
-        m |= vm << (4 * u);
-    }
-    return m;
-}
-
-// Bit mask of the tile's elements whose key is at least bound_key (tile_ge),
-// by one compare of the raw bits per element: for bound_key >= 2^31 (a
-// non-negative bound) key >= bound_key <=> bits >= bound_key ^ 2^31 as signed
-// integers; below it, key >= bound_key <=> bits <= ~bound_key as unsigned
-// ones. tile_pass keeps the in-window ones: only a tile that reaches past
-// either end of the window is masked.
-__device__ __forceinline__ uint32_t tile_ge(const int4 (&v)[kTileVecs], uint32_t bound_key) {
-    uint32_t pass = 0;
-    if (bound_key >= 0x80000000u) {
-        const int32_t bb = static_cast<int32_t>(bound_key ^ 0x80000000u);
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e) pass |= static_cast<uint32_t>(tile_elem(v, e) >= bb) << e;
-    } else {
-        const uint32_t ub = ~bound_key;
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e)
-            pass |= static_cast<uint32_t>(static_cast<uint32_t>(tile_elem(v, e)) <= ub) << e;
-    }
-    return pass;
-}
-
-__device__ __forceinline__ uint32_t tile_pass(const int4 (&v)[kTileVecs], int j0, int je, int rem, int len,
-                                              uint32_t bound_key) {
-    const uint32_t pass = tile_ge(v, bound_key);
-    const bool interior =
-        4 * j0 - rem >= 0 && 4 * (j0 + kTileVecs * kThreads) - rem <= len && j0 + kTileVecs * kThreads <= je;
-    return interior ? pass : pass & tile_valid(j0, je, rem, len);
-}
-
-// Element e of the tile with e known only at run time: a select tree over the
-// registers (no local-memory copy of the tile).
-__device__ __forceinline__ int tile_elem_at(const int4 (&v)[kTileVecs], int e) {
-    static_assert(kTileVecs == 4, "select tree for four vectors");
-    const int c = e & 3;
-    const bool hi = (e & 8) != 0, odd = (e & 4) != 0;
-    const int4 a = hi ? v[2] : v[0], b = hi ? v[3] : v[1];
-    const int4 q = odd ? b : a;
-    const int lo2 = (c & 1) ? q.y : q.x, hi2 = (c & 1) ? q.w : q.z;
-    return (c & 2) ? hi2 : lo2;
-}
-
-// Appends the tile elements flagged in `pass` to the candidate buffer: one
-// warp scan and one shared atomic per warp reserve the slots, then each
-// thread walks the set bits of its own mask (so a warp's loop runs as many
-// times as its busiest lane has candidates, not once per tile element). With
-// kCountLevel1 each appended element is also counted in the level-1
-// histogram.
-constexpr int kCountNone = 0, kCountLevel1 = 1;
-template <int kCount = kCountNone>
-__device__ __forceinline__ void collect_bits(const int4 (&v)[kTileVecs], uint32_t pass, int j0, int rem,
-                                             const Shared& sh) {
-    const uint32_t c = __popc(pass);
-    const uint32_t incl = warp_inclusive_scan(c);
-    const uint32_t total = __shfl_sync(kFull, incl, 31);
-    if (total == 0) return;
-    uint32_t base = 0;
-    if (lane_id() == 31) base = atomicAdd(&sh.cnt[0], total);
-    base = __shfl_sync(kFull, base, 31);
-    uint32_t idx = base + incl - c;
-    const int p0 = 4 * (j0 + static_cast<int>(threadIdx.x)) - rem;  // element 0's position
-    for (uint32_t rest = pass; rest != 0; rest &= rest - 1u) {
-        const int e = __ffs(static_cast<int>(rest)) - 1;
-        const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem_at(v, e)));
-        if (kCount == kCountLevel1) atomicAdd(&sh.hist[kk >> 20], 1u);
-        if (idx < static_cast<uint32_t>(kCandCap)) {
-            sh.cand_key[idx] = kk;
-            sh.cand_pos[idx] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
-        }
-        ++idx;
-    }
-}
-
-// Ranks the threshold bin's elements, n <= kThreads of them in tkey/tpos
+// Ranks the threshold bin's members, n <= kThreads of them in tkey/tpos
 // (16-byte aligned, room for n rounded up to 4): the rank of an element is
-// the number of bin members whose composite (key, ~position) is larger, and
-// the ones ranked below `need` take slots k - need + rank: put(slot, pos)
-// stores each one. This settles every
-// remaining key and position digit at once (ties go to the lowest position).
-// Up to 32 members are ranked by one warp through shuffles. Longer lists are
-// padded to a multiple of 4 with entries that rank below everything; each
-// element is compared by kThreads / m threads (m = n rounded up to a power of
-// two), each over one segment, and the partial ranks meet in the
-// shared-memory counters `rank` (n words). A caller's barrier must make the
-// lists visible first; the function ends without one.
+// the number of members whose composite (key, ~position) is larger, and the
+// ones ranked below `need` take slots k - need + rank: put(slot, pos) stores
+// each one. This settles every remaining key and position digit at once
+// (ties go to the lowest position). Up to 32 members are ranked by one warp
+// through shuffles. Longer lists are padded to a multiple of 4 with entries
+// that rank below everything; each element is compared by kThreads / m
+// threads (m = n rounded up to a power of two), each over one segment, and the
+// partial ranks meet in the shared-memory counters `rank` (n words). A
+// caller's barrier must make the lists visible first; the function ends
+// without one.
 template <class Put>
 __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32_t* tkey, int32_t* tpos,
                                    uint32_t* rank, const Put& put) {
@@ -1003,338 +892,669 @@ __device__ void rank_threshold_bin(uint32_t n, uint32_t need, uint32_t k, uint32
     }
 }
 
-// Writes the slot-ordered position list (k entries in shared memory) to the
-// output row: thread t takes slots t, t + kThreads, ..., so every warp store
-// covers 32 consecutive slots. Follows a barrier that completes the list.
-template <bool kPaged>
-__device__ __forceinline__ void write_slots(const int32_t* slots, uint32_t k, const Emitter<kPaged>& em) {
-    for (uint32_t s = threadIdx.x; s < k; s += kThreads) em.write(s, slots[s]);
+// The tie list of the threshold bin (a CTA's `ties` area).
+struct TieList {
+    uint32_t* key;
+    int32_t* pos;
+    uint32_t* rank;
+};
+__device__ __forceinline__ TieList tie_list(uint32_t* ties) {
+    constexpr int kPad = kMaxRankTies + 4;
+    return TieList{ties, reinterpret_cast<int32_t*>(ties + kPad), ties + 2 * kPad};
 }
 
-// The finish of a solo streaming row once level 1 is known and every
-// element at or above its threshold bin sits in the candidate buffer (n of
-// them): level 2 is histogrammed over the threshold bin's candidates (unless
-// level 1 is exact); then one counting pass and one writing pass over the
-// buffer send every element above the threshold prefix to its slot (a block
-// scan orders them) and copy the elements equal to it to a tie list (in the
-// histogram's storage), which rank_threshold_bin orders into the last slots. Returns false,
-// having written nothing, when the level-2 threshold bin is too full to rank
-// (many equal scores): the caller continues with the radix levels from
-// level 3 (st then holds levels 1 and 2).
-template <bool kPaged>
-__device__ bool finish_candidates(SelState& st, uint32_t bin1, uint32_t n, uint32_t k, const Shared& sh,
-                                  const Emitter<kPaged>& em) {
-    int shift = 20;
-    uint32_t tau = bin1, n_tie = 0;
-    if (!st.exact) {
-        clear_hist(sh.hist, level_bins(1));
-        __syncthreads();
-        for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-            const uint32_t kk = sh.cand_key[i];
-            if ((kk >> 20) == bin1) atomicAdd(&sh.hist[(kk >> 12) & 0xFFu], 1u);
-        }
-        __syncthreads();
-        const Threshold t2 = find_threshold(sh.hist, level_bins(1), st.need, sh);
-        apply_level(st, 1, t2);
-        shift = 12;
-        tau = (bin1 << 8) | t2.bin;
-        n_tie = t2.count;
-        if (!st.exact && n_tie > static_cast<uint32_t>(kThreads)) return false;
+// ----------------------------------------------------------------------------
+// fast path: register tiles, the filter, the sample bound
+// ----------------------------------------------------------------------------
+
+// Raw bits of one tile: kTileVecs vectors per thread from vector j0 (vectors
+// at or past je read as zero bits and are never in the window).
+__device__ __forceinline__ void load_bits(int4 (&v)[kTileVecs], const float4* vbase, int j0, int je) {
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < je ? load_stream_bits(vbase + j) : make_int4(0, 0, 0, 0);
     }
-    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
-    const bool exact = st.exact;
-    uint32_t c = 0;  // selected in the low half, ties in the high half (n <= kCandCap < 2^16)
-    for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t pf = sh.cand_key[i] >> shift;
-        c += (exact ? pf >= tau : pf > tau) ? 1u : (!exact && pf == tau) ? 0x10000u : 0u;
+}
+
+// The same from a shared-memory chunk: vectors [0, n) of `chunk`.
+__device__ __forceinline__ void load_bits_smem(int4 (&v)[kTileVecs], const float4* chunk, int n) {
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = j < n ? reinterpret_cast<const int4*>(chunk)[j] : make_int4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ int tile_elem(const int4 (&v)[kTileVecs], int e) {
+    const int4 q = v[e / 4];
+    return (e % 4) == 0 ? q.x : (e % 4) == 1 ? q.y : (e % 4) == 2 ? q.z : q.w;
+}
+
+// Bit e set: element e of this thread's tile at vector j0 lies in the window
+// (vector u of the tile holds positions 4j - rem .. 4j - rem + 3 for
+// j = j0 + u * kThreads + tid; vectors at or past je are not in it).
+__device__ __forceinline__ uint32_t tile_valid(int j0, int je, int rem, int len) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = j0 + u * kThreads + static_cast<int>(threadIdx.x);
+        const int lo = 4 * j - rem;
+        const int a = max(-lo, 0), b = min(len - lo, 4);  // lanes [a, b) are in the window
+        const uint32_t vm = (j < je && a < b) ? (1u << b) - (1u << a) : 0u;
+        m |= vm << (4 * u);
+    }
+    return m;
+}
+
+// Whether every element of the tile at vector j0 lies in the window.
+__device__ __forceinline__ bool tile_interior(int j0, int je, int rem, int len) {
+    constexpr int T = kTileVecs * kThreads;
+    return 4 * j0 - rem >= 0 && 4 * (j0 + T) - rem <= len && j0 + T <= je;
+}
+
+// key >= bound_key as one compare of the raw bits: for a non-negative bound
+// (bound_key >= 2^31) key >= bound_key <=> bits >= bound_key ^ 2^31 as signed
+// integers; below it, key >= bound_key <=> bits <= ~bound_key as unsigned
+// ones. thr is that right-hand side.
+template <bool kNonNeg>
+__device__ __forceinline__ bool passes(int32_t b, uint32_t thr) {
+    return kNonNeg ? b >= static_cast<int32_t>(thr) : static_cast<uint32_t>(b) <= thr;
+}
+__device__ __forceinline__ uint32_t pass_threshold(uint32_t bound_key) {
+    return bound_key >= 0x80000000u ? (bound_key ^ 0x80000000u) : ~bound_key;
+}
+
+// Stores (bits, p0 + kOff) at shared address a and advances a by one entry
+// when bits pass the bound (thr: see passes); with kMasked only when bit kBit
+// of `valid` is set too. One compare, one predicated store, one predicated
+// add; the position is formed inside, so no position is kept in a register.
+template <bool kNonNeg, bool kMasked, int kOff, int kBit>
+__device__ __forceinline__ void append_if(uint32_t& a, int32_t bits, uint32_t thr, int32_t p0, uint32_t valid) {
+    if (kMasked) {
+        if (kNonNeg)
+            asm volatile(
+                "{\n\t.reg .pred v, q;\n\t.reg .b32 t;\n\tand.b32 t, %4, %6;\n\tsetp.ne.b32 v, t, 0;\n\t"
+                "setp.ge.and.s32 q, %1, %2, v;\n\tadd.s32 t, %3, %5;\n\t"
+                "@q st.shared.v2.b32 [%0], {%1, t};\n\t@q add.u32 %0, %0, 8;\n\t}"
+                : "+r"(a)
+                : "r"(bits), "r"(thr), "r"(p0), "r"(valid), "n"(kOff), "n"(1 << kBit)
+                : "memory");
+        else
+            asm volatile(
+                "{\n\t.reg .pred v, q;\n\t.reg .b32 t;\n\tand.b32 t, %4, %6;\n\tsetp.ne.b32 v, t, 0;\n\t"
+                "setp.le.and.u32 q, %1, %2, v;\n\tadd.s32 t, %3, %5;\n\t"
+                "@q st.shared.v2.b32 [%0], {%1, t};\n\t@q add.u32 %0, %0, 8;\n\t}"
+                : "+r"(a)
+                : "r"(bits), "r"(thr), "r"(p0), "r"(valid), "n"(kOff), "n"(1 << kBit)
+                : "memory");
+    } else {
+        if (kNonNeg)
+            asm volatile(
+                "{\n\t.reg .pred q;\n\t.reg .b32 t;\n\tsetp.ge.s32 q, %1, %2;\n\tadd.s32 t, %3, %4;\n\t"
+                "@q st.shared.v2.b32 [%0], {%1, t};\n\t@q add.u32 %0, %0, 8;\n\t}"
+                : "+r"(a)
+                : "r"(bits), "r"(thr), "r"(p0), "n"(kOff)
+                : "memory");
+        else
+            asm volatile(
+                "{\n\t.reg .pred q;\n\t.reg .b32 t;\n\tsetp.le.u32 q, %1, %2;\n\tadd.s32 t, %3, %4;\n\t"
+                "@q st.shared.v2.b32 [%0], {%1, t};\n\t@q add.u32 %0, %0, 8;\n\t}"
+                : "+r"(a)
+                : "r"(bits), "r"(thr), "r"(p0), "n"(kOff)
+                : "memory");
+    }
+}
+
+// Adds 1 to c when bits pass the bound (and, with kMasked, bit kBit of valid
+// is set).
+template <bool kNonNeg, bool kMasked, int kBit>
+__device__ __forceinline__ void count_if(uint32_t& c, int32_t bits, uint32_t thr, uint32_t valid) {
+    if (kMasked) {
+        if (kNonNeg)
+            asm("{\n\t.reg .pred v, q;\n\t.reg .b32 t;\n\tand.b32 t, %2, %4;\n\tsetp.ne.b32 v, t, 0;\n\t"
+                "setp.ge.and.s32 q, %1, %3, v;\n\t@q add.u32 %0, %0, 1;\n\t}"
+                : "+r"(c) : "r"(bits), "r"(valid), "r"(thr), "n"(1 << kBit));
+        else
+            asm("{\n\t.reg .pred v, q;\n\t.reg .b32 t;\n\tand.b32 t, %2, %4;\n\tsetp.ne.b32 v, t, 0;\n\t"
+                "setp.le.and.u32 q, %1, %3, v;\n\t@q add.u32 %0, %0, 1;\n\t}"
+                : "+r"(c) : "r"(bits), "r"(valid), "r"(thr), "n"(1 << kBit));
+    } else {
+        if (kNonNeg)
+            asm("{\n\t.reg .pred q;\n\tsetp.ge.s32 q, %1, %2;\n\t@q add.u32 %0, %0, 1;\n\t}"
+                : "+r"(c) : "r"(bits), "r"(thr));
+        else
+            asm("{\n\t.reg .pred q;\n\tsetp.le.u32 q, %1, %2;\n\t@q add.u32 %0, %0, 1;\n\t}"
+                : "+r"(c) : "r"(bits), "r"(thr));
+    }
+}
+
+// Compile-time loop over the tile's elements: f(integral_constant<e>).
+template <int E, class F>
+__device__ __forceinline__ void for_each_elem(F&& f) {
+    if constexpr (E < kTileElems) {
+        f(std::integral_constant<int, E>{});
+        for_each_elem<E + 1>(f);
+    }
+}
+
+// The filter: appends the tile's in-window elements whose key is at least
+// the bound to this warp's candidate region (shared address `region`) as
+// (raw bits, position). Straight-line code: every element is compared, one
+// warp scan of the per-thread counts gives each thread its first slot, the
+// stores are predicated (no branch per element, no shared atomic). `wcount`
+// is the warp's running count (warp-uniform); a region that would overflow
+// takes no more entries and sets `ovf` (the row then finishes on the exact
+// path). Element e of the tile sits at position p0 + (e / 4) * 4 * kThreads
+// + e % 4.
+template <bool kNonNeg, bool kMasked>
+__device__ __forceinline__ void filter_tile(const int4 (&v)[kTileVecs], uint32_t thr, uint32_t valid, int p0,
+                                            uint32_t region, uint32_t& wcount, uint32_t cap, bool& ovf) {
+    uint32_t c = 0;
+    for_each_elem<0>([&](auto ec) {
+        constexpr int e = decltype(ec)::value;
+        count_if<kNonNeg, kMasked, e>(c, tile_elem(v, e), thr, valid);
+    });
     const uint32_t incl = warp_inclusive_scan(c);
-    const int warp = static_cast<int>(threadIdx.x >> 5);
-    if (lane_id() == 31) sh.red[warp] = incl;
-    __syncthreads();
-    uint32_t base = incl - c;
-    for (int w = 0; w < warp; ++w) base += sh.red[w];
-    uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
-    uint32_t* tkey = sh.hist;                                  // tie list: kThreads + 4 entries each
-    int32_t* tpos = reinterpret_cast<int32_t*>(sh.hist + 2 * kThreads);
-    for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t kk = sh.cand_key[i];
-        const uint32_t pf = kk >> shift;
-        const bool w = exact ? pf >= tau : pf > tau;
-        const bool t = !exact && pf == tau;
-        const int32_t pos = sh.cand_pos[i];
-        em.write_if(w, slot, pos);
-        if (t) {
-            tkey[tslot] = kk;
-            tpos[tslot] = pos;
-        }
-        slot += w;
-        tslot += t;
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    uint32_t a = region + (wcount + incl - c) * 8u;
+    wcount += total;
+    if (wcount > cap) {  // warp-uniform
+        ovf = true;
+        return;
     }
-    em.flag_if(slot > k - (exact ? 0u : st.need));
+    for_each_elem<0>([&](auto ec) {
+        constexpr int e = decltype(ec)::value;
+        append_if<kNonNeg, kMasked, (e >> 2) * (4 * kThreads) + (e & 3), e>(a, tile_elem(v, e), thr, p0, valid);
+    });
+}
+
+// filter_tile for the tile at vector j0 of a window of vectors [.., je).
+template <bool kNonNeg>
+__device__ __forceinline__ void filter_at(const int4 (&v)[kTileVecs], uint32_t thr, int j0, int je, int rem, int len,
+                                          uint32_t region, uint32_t& wcount, uint32_t cap, bool& ovf) {
+    const int p0 = 4 * (j0 + static_cast<int>(threadIdx.x)) - rem;
+    if (tile_interior(j0, je, rem, len))
+        filter_tile<kNonNeg, false>(v, thr, 0xFFFFu, p0, region, wcount, cap, ovf);
+    else
+        filter_tile<kNonNeg, true>(v, thr, tile_valid(j0, je, rem, len), p0, region, wcount, cap, ovf);
+}
+
+// Lower bound on the threshold from a sample of n_s of the window's len keys
+// (this thread's in skey[j] where bit j of vmask is set): the 16-bit key
+// prefix at which the count from the top first reaches the sample's expected
+// share of the top-k plus four standard deviations plus 2, found by two
+// 256-bin levels (the top 8 key bits, then the next 8) in the two halves of
+// shist (zero on entry; every thread calls this). Returns the prefix's lowest
+// key. Four barriers; warp 0 searches.
+template <int N>
+__device__ uint32_t sample_bound(const uint32_t (&skey)[N], uint32_t vmask, uint32_t n_s, int len, uint32_t k,
+                                 const Shared& sh) {
+    const float expect = static_cast<float>(k) * static_cast<float>(n_s) / static_cast<float>(len);
+    const float tgt = fminf(ceilf(expect + 4.0f * sqrtf(expect) + 2.0f), static_cast<float>(n_s));
+    const uint32_t target = max(static_cast<uint32_t>(tgt), 1u);
+    const uint32_t h1 = saddr(sh.shist()), h2 = saddr(sh.shist() + kSmallWords);
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        if ((vmask >> j) & 1u) red_add_shared(h1 + (skey[j] >> 24) * 4u, 1u);
+    __syncthreads();
+    const Threshold t1 = find_threshold(sh.shist(), kSmall, target, sh);
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+        if (((vmask >> j) & 1u) && (skey[j] >> 24) == t1.bin) red_add_shared(h2 + ((skey[j] >> 16) & 255u) * 4u, 1u);
+    __syncthreads();
+    const Threshold t2 = find_threshold(sh.shist() + kSmallWords, kSmall, target - t1.above, sh);
+    return ((t1.bin << 8) | t2.bin) << 16;
+}
+
+// The sample of a window read from global memory: one 16-byte vector per
+// thread, vector (tid * nv) >> 9 of the aligned window, so 512 vectors
+// spread evenly over it (nv > 512); it is loaded before anything else of the
+// row so that it heads the memory queue.
+__device__ __forceinline__ int4 sample_load(const float4* vbase, int nv) {
+    return load_stream_bits(vbase + ((static_cast<uint64_t>(threadIdx.x) * static_cast<uint32_t>(nv)) >> 9));
+}
+
+// sample_bound over those vectors: every in-window lane (all but the head
+// vector's `rem` leading lanes, since the tail vector is never sampled when
+// nv > 512), 2048 - rem elements in all.
+__device__ uint32_t sample_bound_vec(const int4& sv, int nv, int rem, int len, uint32_t k, const Shared& sh) {
+    const int p0 = 4 * static_cast<int>((static_cast<uint64_t>(threadIdx.x) * static_cast<uint32_t>(nv)) >> 9) - rem;
+    const uint32_t skey[4] = {bits_key(static_cast<uint32_t>(sv.x)), bits_key(static_cast<uint32_t>(sv.y)),
+                              bits_key(static_cast<uint32_t>(sv.z)), bits_key(static_cast<uint32_t>(sv.w))};
+    uint32_t vmask = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) vmask |= (p0 + c >= 0 && p0 + c < len ? 1u : 0u) << c;
+    return sample_bound<4>(skey, vmask, static_cast<uint32_t>(4 * kThreads - rem), len, k, sh);
+}
+
+// ----------------------------------------------------------------------------
+// fast path: the finish over the candidates
+// ----------------------------------------------------------------------------
+
+// Bin of a candidate key in the 256-bin histogram of 16-bit key prefixes
+// based at base16 (the bound's prefix); keys 255 or more prefixes above share
+// the top bin.
+__device__ __forceinline__ uint32_t fine_bin(uint32_t key, uint32_t base16) {
+    return min((key >> 16) - base16, static_cast<uint32_t>(kSmall - 1));
+}
+
+// Counts this warp's n candidates (region at shared address `region`) into
+// its own histogram at shared address `whist`.
+__device__ __forceinline__ void count_candidates(uint32_t region, uint32_t n, uint32_t base16, uint32_t whist) {
+    for (uint32_t i = lane_id(); i < n; i += 32)
+        red_add_shared(whist + fine_bin(bits_key(ld_shared_u32(region + i * 8u)), base16) * 4u, 1u);
+}
+
+// Thread t < kSmall: bin t summed over the warps' histograms (after a barrier
+// that completes them).
+__device__ __forceinline__ uint32_t sum_warp_bins(const Shared& sh) {
+    uint32_t c = 0;
+    const uint32_t* w = sh.whist() + threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) c += w[q * kSmall];
+    return c;
+}
+
+// This warp's count of definite candidates (bins above tau, and tau itself
+// when exact) and of threshold-bin members, from its own histogram; every
+// lane gets both.
+__device__ __forceinline__ void warp_counts(const Shared& sh, uint32_t tau, bool exact, uint32_t& def, uint32_t& tie) {
+    const uint32_t* h = sh.whist() + (threadIdx.x >> 5) * kSmall + 8 * lane_id();
+    const uint4 a = *reinterpret_cast<const uint4*>(h), b = *reinterpret_cast<const uint4*>(h + 4);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t d = 0, t = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t bin = 8 * lane_id() + static_cast<uint32_t>(i);
+        d += (bin > tau || (exact && bin == tau)) ? v[i] : 0u;
+        t += (!exact && bin == tau) ? v[i] : 0u;
+    }
+    def = __reduce_add_sync(kFull, d);
+    tie = __reduce_add_sync(kFull, t);
+}
+
+// The classify-and-write pass over this warp's n candidates once the
+// threshold bin tau is known: candidates above it (at or above it when
+// exact) take output slots def_base, def_base + 1, ... in order; members of
+// the bin take tie-list entries tie_base, ... for ranking (the list may be
+// another CTA's). The bases come from the warps' counts, so the pass needs
+// no atomics.
+template <bool kPaged>
+__device__ __forceinline__ void classify_write(uint32_t region, uint32_t n, uint32_t base16, uint32_t tau,
+                                               bool exact, uint32_t def_base, uint32_t tie_base,
+                                               const TieList& ties, const Emitter<kPaged>& em) {
+    const uint32_t n_round = (n + 31u) & ~31u;
+    const uint32_t lt = lanemask_lt();
+    for (uint32_t i = lane_id(); i < n_round; i += 32) {
+        const bool valid = i < n;
+        const uint2 e = valid ? ld_shared_v2(region + i * 8u) : make_uint2(0u, 0u);
+        const uint32_t key = bits_key(e.x);
+        const uint32_t bin = fine_bin(key, base16);
+        const bool def = valid && (bin > tau || (exact && bin == tau));
+        const uint32_t m = __ballot_sync(kFull, def);
+        if (def) em.write(def_base + static_cast<uint32_t>(__popc(m & lt)), static_cast<int32_t>(e.y));
+        def_base += static_cast<uint32_t>(__popc(m));
+        if (!exact) {
+            const bool tie = valid && bin == tau;
+            const uint32_t mt = __ballot_sync(kFull, tie);
+            if (tie) {
+                const uint32_t t = tie_base + static_cast<uint32_t>(__popc(mt & lt));
+                if (t < static_cast<uint32_t>(kMaxRankTies)) {
+                    ties.key[t] = key;
+                    ties.pos[t] = static_cast<int32_t>(e.y);
+                }
+            }
+            tie_base += static_cast<uint32_t>(__popc(mt));
+        }
+    }
+}
+
+// Outcome of the fast finish.
+enum FinishResult { kFinished = 0, kNeedLevels = 1, kNeedExact = 2 };
+
+// The fast finish of a single-CTA row (every candidate of the row in this
+// CTA's regions, `ovf` this warp's overflow flag). kNeedExact: nothing was
+// written, the caller runs the exact path from scratch. kNeedLevels: the
+// threshold bin is too full to rank; st then holds its 16-bit prefix and the
+// caller continues with the low-16-bit radix levels over the regions.
+template <bool kPaged>
+__device__ FinishResult finish_solo(uint32_t bound_key, uint32_t wcount, bool ovf, uint32_t k, SelState& st,
+                                    uint32_t cap, const Shared& sh, const Emitter<kPaged>& em) {
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const uint32_t region = saddr(sh.cand) + static_cast<uint32_t>(warp) * cap * 8u;
+    const uint32_t n = min(wcount, cap);
+    const uint32_t base16 = bound_key >> 16;
+    if (lane_id() == 0) {
+        sh.wcnt()[warp] = n;
+        if (ovf) atomicOr(&sh.cnt()[3], 1u);
+    }
+    if (!ovf) count_candidates(region, n, base16, saddr(sh.whist() + warp * kSmall));
+    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // page-table entries, published below
+    __syncthreads();
+    if (sh.cnt()[3] != 0u) return kNeedExact;
+    if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
+    __syncthreads();
+    const Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    if (!t.found || t.bin == static_cast<uint32_t>(kSmall - 1)) return kNeedExact;
+    const uint32_t need = k - t.above;
+    const bool exact = t.count == need;
+    if (!exact && t.count > static_cast<uint32_t>(kMaxRankTies)) {
+        st = SelState{static_cast<uint64_t>(base16 + t.bin) << 48, 0xFFFFull << 48, need, false};
+        return kNeedLevels;
+    }
+    uint32_t def, tie;
+    warp_counts(sh, t.bin, exact, def, tie);
+    if (lane_id() == 0) {
+        sh.red()[warp] = def;
+        sh.red()[kWarps + warp] = tie;
+    }
+    __syncthreads();
+    uint32_t def_base = 0, tie_base = 0;
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+        def_base += q < warp ? sh.red()[q] : 0u;
+        tie_base += q < warp ? sh.red()[kWarps + q] : 0u;
+    }
+    const TieList ties = tie_list(sh.ties());
+    classify_write<kPaged>(region, n, base16, t.bin, exact, def_base, tie_base, ties, em);
     if (!exact) {
         __syncthreads();
-        rank_threshold_bin(n_tie, st.need, k, tkey, tpos, sh.cand_key,
+        rank_threshold_bin(t.count, need, k, ties.key, ties.pos, ties.rank,
                            [&](uint32_t s, int32_t pos) { em.write(s, pos); });
     }
-    return true;
+    return kFinished;
 }
 
-// The register route's finish once the selection prefix is known: every
-// tile element whose prefix (key >> shift) is above tau (at least tau when
-// exact) is selected and goes to its slot in a slot-ordered list (one block
-// scan of both counts orders the slots), the elements equal to it (not
-// exact) go to a tie list in the candidate buffer, which rank_threshold_bin
-// orders into the last `need` slots, and the list is written out coalesced.
-template <bool kPaged>
-__device__ void finish_registers(const int4 (&v)[kTileVecs], uint32_t valid, int rem, int shift, uint32_t tau,
-                                 bool exact, uint32_t need, uint32_t n_tie, uint32_t k, const Shared& sh,
-                                 const Emitter<kPaged>& em) {
-    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // published by the barrier below
-    // prefix >= tau and prefix > tau as raw-bit compares against the
-    // smallest keys with prefix tau and tau + 1
-    const uint32_t ge_tau = tile_ge(v, tau << shift);
-    const bool top_bin = tau + 1u == (1u << (32 - shift));
-    const uint32_t gt_tau = (exact || top_bin) ? 0u : tile_ge(v, (tau + 1u) << shift);
-    const uint32_t def = (exact ? ge_tau : gt_tau) & valid;
-    const uint32_t tie = exact ? 0u : (ge_tau & ~gt_tau & valid);
-    // both counts in one scan: selected in the low half, ties in the high
-    // half (a CTA holds at most 8192 elements)
-    const uint32_t c = static_cast<uint32_t>(__popc(def)) | (static_cast<uint32_t>(__popc(tie)) << 16);
+// ----------------------------------------------------------------------------
+// exact paths (used when the fast path's self-check fails)
+// ----------------------------------------------------------------------------
+
+// Appends every in-window element of the tile whose key is at least the bound
+// (thr = pass_threshold(bound)) to the contiguous list of (key, position)
+// `list`, counted in sh.cnt()[0] (one shared atomic per warp); entries past
+// `cap` are dropped (callers count first).
+template <bool kNonNeg>
+__device__ void collect_tile(const int4 (&v)[kTileVecs], uint32_t thr, int j0, int je, int rem, int len,
+                             const Shared& sh, uint2* list, int cap) {
+    const uint32_t valid = tile_valid(j0, je, rem, len);
+    uint32_t c = 0;
+#pragma unroll
+    for (int e = 0; e < kTileElems; ++e) c += (passes<kNonNeg>(tile_elem(v, e), thr) && ((valid >> e) & 1u)) ? 1u : 0u;
     const uint32_t incl = warp_inclusive_scan(c);
-    const int warp = static_cast<int>(threadIdx.x >> 5);
-    if (lane_id() == 31) sh.red[warp] = incl;
-    __syncthreads();
-    uint32_t base = incl - c;
-    for (int w = 0; w < warp; ++w) base += sh.red[w];
-    uint32_t slot = base & 0xFFFFu, tslot = base >> 16;
-    int32_t* slots = reinterpret_cast<int32_t*>(sh.hist + kBins - TOPK_MAX_K);  // slot-ordered positions
-    const int32_t p0 = 4 * static_cast<int32_t>(threadIdx.x) - rem;  // position of element 0
-    // walk the set bits only (a warp loops as often as its busiest lane)
-    for (uint32_t rest = def; rest != 0; rest &= rest - 1u) {
-        const int e = __ffs(static_cast<int>(rest)) - 1;
-        if (slot < k) slots[slot] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
-        ++slot;
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    if (total == 0) return;
+    uint32_t base = 0;
+    if (lane_id() == 31) base = atomicAdd(&sh.cnt()[0], total);
+    uint32_t idx = __shfl_sync(kFull, base, 31) + incl - c;
+    const int p0 = 4 * (j0 + static_cast<int>(threadIdx.x)) - rem;
+#pragma unroll
+    for (int e = 0; e < kTileElems; ++e) {
+        const int32_t b = tile_elem(v, e);
+        if (passes<kNonNeg>(b, thr) && ((valid >> e) & 1u)) {
+            if (idx < static_cast<uint32_t>(cap))
+                list[idx] = make_uint2(bits_key(static_cast<uint32_t>(b)),
+                                          static_cast<uint32_t>(p0 + (e >> 2) * (4 * kThreads) + (e & 3)));
+            ++idx;
+        }
     }
-    for (uint32_t rest = tie; rest != 0; rest &= rest - 1u) {
-        const int e = __ffs(static_cast<int>(rest)) - 1;
-        sh.cand_key[tslot] = bits_key(static_cast<uint32_t>(tile_elem_at(v, e)));
-        sh.cand_pos[tslot] = p0 + (e >> 2) * (4 * kThreads) + (e & 3);
-        ++tslot;
-    }
-    em.flag_if(slot > k - (exact ? 0u : need));
+}
+
+// The exact path of a single-CTA row read from global memory: a full level-1
+// histogram pass; then, when the elements at or above its threshold bin fit
+// the candidate buffer, one more pass collects them and the remaining levels
+// run on the buffer, else the levels re-read the row.
+template <bool kPaged>
+__device__ __noinline__ void exact_row_global(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
+                                 const Shared& sh0, const Emitter<kPaged>& em) {
+    constexpr int T = kTileVecs * kThreads;
+    const Shared sh = exact_view(sh0, false);
+    uint2* list = exact_list(sh);
+    const SoloMerge mg;
+    const GlobalSource all{vbase, 0, nv, rem, len};
+    clear_words(sh.lvl, kBins);
     __syncthreads();
-    if (!exact) {
-        rank_threshold_bin(n_tie, need, k, sh.cand_key, sh.cand_pos, sh.hist,
-                           [&](uint32_t s, int32_t pos) { slots[s] = pos; });
+    uint32_t* hist = sh.lvl;
+    all.visit([&](uint32_t kk, int32_t, bool valid) {
+        if (valid) atomicAdd(&hist[kk >> 20], 1u);
+    });
+    const Threshold t1 = find_threshold(mg.merge(sh, kBins), kBins, k, sh);
+    SelState st{0ull, 0ull, k, false};
+    apply_level(st, kLvlKey12, t1);
+    if (!st.exact && count_from(sh.lvl, kBins, t1.bin, sh) <= static_cast<uint32_t>(kXListCap)) {
+        if (threadIdx.x == 0) sh.cnt()[0] = 0;
         __syncthreads();
+        const uint32_t bound = t1.bin << 20, thr = pass_threshold(bound);
+        for (int j0 = 0; j0 < nv; j0 += T) {
+            int4 v[kTileVecs];
+            load_bits(v, vbase, j0, nv);
+            if (bound >= 0x80000000u) collect_tile<true>(v, thr, j0, nv, rem, len, sh, list, kXListCap);
+            else collect_tile<false>(v, thr, j0, nv, rem, len, sh, list, kXListCap);
+        }
+        __syncthreads();
+        const CandSource src{list, min(sh.cnt()[0], static_cast<uint32_t>(kXListCap))};
+        run_levels(st, kLvlKey12 + 1, kLvlKeyLast, det, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    } else {
+        run_levels(st, kLvlKey12 + 1, kLvlKeyLast, det, all, sh, mg);
+        emit_selected<kPaged>(st, k, all, sh, mg, em);
     }
-    write_slots<kPaged>(slots, k, em);
+}
+
+// ----------------------------------------------------------------------------
+// routes of a single-CTA row
+// ----------------------------------------------------------------------------
+
+// Per-row inputs, after the data-error checks.
+struct RowInfo {
+    int32_t len, start, offset, table_row, token0;
+};
+
+__device__ __forceinline__ void park_row(const RowInfo& r, const Shared& sh) {
+    if (threadIdx.x == 0) {
+        int32_t* d = sh.row();
+        d[0] = r.len, d[1] = r.start, d[2] = r.offset, d[3] = r.table_row, d[4] = r.token0;
+    }
+}
+__device__ __forceinline__ RowInfo load_row(const Shared& sh) {
+    const int32_t* d = sh.row();
+    return RowInfo{d[0], d[1], d[2], d[3], d[4]};
+}
+
+// The page-table entries [first, first + n) of a row's table that window
+// positions [p_lo, p_hi) map to (tokens token0 + p).
+struct PageSpan {
+    int32_t first;
+    int n;
+};
+__device__ __forceinline__ PageSpan page_span(int32_t token0, int32_t page_bits, int32_t p_lo, int32_t p_hi) {
+    const int32_t first = (token0 + p_lo) >> page_bits;
+    return PageSpan{first, ((token0 + p_hi - 1) >> page_bits) - first + 1};
+}
+
+// PAGED: starts asynchronous copies into shared memory of the page-table
+// entries that positions [p_lo, p_hi) map to, when they fit `cap` entries;
+// the finish waits for them (cp.async.wait_all, then a barrier). Other
+// lookups read global memory.
+template <bool kPaged>
+__device__ __forceinline__ void prefetch_pages(const Params& p, const RowInfo& r, int32_t p_lo, int32_t p_hi, int cap,
+                                               const Shared& sh) {
+    if (!kPaged || p_hi <= p_lo) return;
+    const PageSpan ps = page_span(r.token0, p.page_bits, p_lo, p_hi);
+    if (ps.n > cap) return;
+    const int32_t* pt_row = p.page_table + static_cast<int64_t>(r.table_row) * p.page_table_stride + ps.first;
+    for (int i = threadIdx.x; i < ps.n; i += kThreads) {
+        const uint32_t dst = saddr(sh.pages + i);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(pt_row + i) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <bool kPaged>
+__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, const RowInfo& r) {
+    Emitter<kPaged> em;
+    em.out = p.out + static_cast<int64_t>(b) * p.k;
+    em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
+    em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(r.table_row) * p.page_table_stride : nullptr;
+    em.pt_cached = nullptr;
+    em.token0 = r.token0;
+    em.pt_first = 0;
+    em.pt_count = 0;
+    em.page_bits = p.page_bits;
+    em.offset = r.offset;
+    em.k = static_cast<uint32_t>(p.k);
+    em.flags = &p.hdr->flags;
+    return em;
+}
+
+// The emitter of a row whose page-table entries for positions [p_lo, p_hi)
+// were prefetched (prefetch_pages with the same arguments). Built after the
+// filter, so none of it is live during the score pass.
+template <bool kPaged>
+__device__ __forceinline__ Emitter<kPaged> row_emitter(const Params& p, int b, const RowInfo& r, int32_t p_lo,
+                                                       int32_t p_hi, int cap, const Shared& sh) {
+    Emitter<kPaged> em = make_emitter<kPaged>(p, b, r);
+    if (kPaged && p_hi > p_lo) {
+        const PageSpan ps = page_span(r.token0, p.page_bits, p_lo, p_hi);
+        if (ps.n <= cap) {
+            em.pt_cached = sh.pages;
+            em.pt_first = ps.first;
+            em.pt_count = ps.n;
+        }
+    }
+    return em;
+}
+
+// The rest of a row after the fast finish declined to rank its threshold
+// bin (see finish_solo): the low-16-bit radix levels over the regions.
+template <bool kPaged>
+__device__ __noinline__ void finish_levels(SelState st, uint32_t k, bool det, const Shared sh,
+                                           const Emitter<kPaged> em) {
+    const RegionSource src{sh.cand, sh.wcnt(), kWarpCap};
+    run_levels(st, kLvlLow16, kLvlLow16Last, det, src, sh, SoloMerge{});
+    emit_selected<kPaged>(st, k, src, sh, SoloMerge{}, em);
+}
+
+// The exact path of a register-route row, from its registers.
+template <bool kPaged>
+__device__ __noinline__ void exact_row_registers(const int4 (&v)[kTileVecs], int rem, int len, uint32_t k, bool det,
+                                                 const Shared sh0, const Emitter<kPaged> em) {
+    const Shared sh = exact_view(sh0, false);
+    SelState st{0ull, 0ull, k, false};
+    const RegSource src{v, rem, len};
+    run_levels(st, kLvlKey12, kLvlKeyLast, det, src, sh, SoloMerge{});
+    emit_selected<kPaged>(st, k, src, sh, SoloMerge{}, em);
 }
 
 // Register route: the whole aligned window (nv <= kTileVecs * kThreads
-// vectors) is one register tile.
-//  * The first digit is 14 bits wide: 16384 16-bit counters (two per word,
-//    in the candidate buffer's storage), one shared atomic per element. When
-//    its threshold bin holds at most kThreads elements (the usual case; about
-//    40 for a row of 8192 normal scores), finish_registers writes every
-//    element above it to its slot and ranks the bin's members for the rest.
-//  * Otherwise (many equal scores) the 12-bit levels run: level 1 from the
-//    tile, level 2 over its threshold bin from the registers, the same finish
-//    when that bin is small, else the radix levels on the candidate buffer
-//    (or on the registers when the bins do not fit it).
-template <bool kPaged>
-__device__ void register_row(const float4* vbase, int nv, int rem, int len, uint32_t k, bool det,
-                             const Shared& sh, const Emitter<kPaged>& em) {
+// vectors) is one register tile. The sample is every fourth position
+// (positions 4j: lane `rem` of vector j), read from the registers.
+template <bool kPaged, int kLay>
+__device__ void register_row(const Params& p, int b, const float4* vbase, int nv, int rem, int len) {
+    const uint32_t k = static_cast<uint32_t>(p.k);
     int4 v[kTileVecs];
-    load_bits(v, vbase, 0, nv);  // in flight while the histogram is cleared
-    static_assert(kFineWords <= 2 * kCandCap, "the fine histogram lives in the candidate buffer");
-    uint32_t* fine = sh.cand_key;
-    clear_hist(fine, kFineWords);
-    __syncthreads();
+    load_bits(v, vbase, 0, nv);
+    uint32_t skey[kTileVecs];
+    uint32_t vmask = 0;
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int j = u * kThreads + static_cast<int>(threadIdx.x);
+        const int32_t b = rem == 0 ? v[u].x : rem == 1 ? v[u].y : rem == 2 ? v[u].z : v[u].w;
+        skey[u] = bits_key(static_cast<uint32_t>(b));
+        vmask |= (4 * j < len ? 1u : 0u) << u;
+    }
+    const uint32_t bound_key =
+        sample_bound<kTileVecs>(skey, vmask, static_cast<uint32_t>((len + 3) / 4), len, k, layout<kLay>());
+    const uint32_t thr = pass_threshold(bound_key);
     const uint32_t valid = tile_valid(0, nv, rem, len);
-#pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e) {
-        const uint32_t d = bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> kFineShift;
-        if ((valid >> e) & 1u) atomicAdd(&fine[d >> 1], (d & 1u) ? 0x10000u : 1u);
-    }
-    __syncthreads();
-    {
-        const uint32_t total = find_fine_publish(fine, k, sh);
-        __syncthreads();  // the fine bins are read: the candidate buffer is free again
-        const Threshold tf = find_wide_result(total, k, sh);
-        const uint32_t need = k - tf.above;
-        const bool exact = tf.count == need;
-        if (exact || tf.count <= static_cast<uint32_t>(kThreads)) {
-            finish_registers<kPaged>(v, valid, rem, kFineShift, tf.bin, exact, need, tf.count, k, sh, em);
-            return;
-        }
-    }
-    clear_hist(sh.hist, kBins);
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < 4 * kTileVecs; ++e)
-        if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(v, e))) >> 20], 1u);
-    __syncthreads();
-    // Level 1; its bins are free once the search has read them, so the
-    // level-2 bins are cleared before the barrier that publishes the result.
-    const uint32_t total1 = find_wide_publish(sh.hist, k, sh);
-    clear_hist(sh.hist, level_bins(1));
-    __syncthreads();
-    const Threshold t1 = find_wide_result(total1, k, sh);
-    SoloMerge mg;
-    SelState st{0ull, 0ull, k, false};
-    apply_level(st, 0, t1);
-    const int last = (det ? kAllLevels : kKeyLevels) - 1;
-    // Level 2 inside the threshold bin, histogrammed from the registers.
-    int shift = 20;           // the selection prefix is key >> shift ...
-    uint32_t tau = t1.bin;    // ... compared with tau
-    uint32_t n_tie = 0;
-    if (!st.exact) {
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e) {
-            const uint32_t kk = bits_key(static_cast<uint32_t>(tile_elem(v, e)));
-            if (((valid >> e) & 1u) && (kk >> 20) == t1.bin) atomicAdd(&sh.hist[(kk >> 12) & 0xFFu], 1u);
-        }
-        __syncthreads();
-        const Threshold t2 = find_threshold(sh.hist, level_bins(1), st.need, sh);
-        apply_level(st, 1, t2);
-        shift = 12;
-        tau = (t1.bin << 8) | t2.bin;
-        n_tie = t2.count;
-    }
-    if (st.exact || n_tie <= static_cast<uint32_t>(kThreads)) {
-        finish_registers<kPaged>(v, valid, rem, shift, tau, st.exact, st.need, n_tie, k, sh, em);
+    const int p0 = 4 * static_cast<int>(threadIdx.x) - rem;
+    const uint32_t region = saddr(layout<kLay>().cand) + (threadIdx.x >> 5) * (kWarpCap * 8u);
+    uint32_t wcount = 0;
+    bool ovf = false;
+    if (bound_key >= 0x80000000u) filter_tile<true, true>(v, thr, valid, p0, region, wcount, kWarpCap, ovf);
+    else filter_tile<false, true>(v, thr, valid, p0, region, wcount, kWarpCap, ovf);
+    const Shared sh = layout<kLay>();
+    const RowInfo ri = load_row(sh);
+    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
+    const Emitter<kPaged> em = row_emitter<kPaged>(p, b, ri, 0, len, kPageCache, sh);
+    SelState st;
+    const FinishResult r = finish_solo<kPaged>(bound_key, wcount, ovf, k, st, kWarpCap, sh, em);
+    if (r == kFinished) return;
+    if (r == kNeedLevels) {
+        finish_levels<kPaged>(st, k, det, sh, em);
         return;
     }
-    // A threshold bin too full to rank (many equal scores): the radix levels
-    // continue from level 3 on the candidate buffer, or on the registers when
-    // the bins at or above the level-1 threshold do not fit it.
-    if (t1.above + t1.count <= static_cast<uint32_t>(kCandCap)) {
-        __syncthreads();
-        collect_bits(v, tile_pass(v, 0, nv, rem, len, t1.bin << 20), 0, rem, sh);
-        __syncthreads();
-        const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
-        run_levels(st, 2, last, src, sh, mg);
-        emit_selected<kPaged>(st, k, src, sh, mg, em);
-    } else {
-        float4 f[kTileVecs];
-#pragma unroll
-        for (int u = 0; u < kTileVecs; ++u)
-            f[u] = make_float4(__int_as_float(v[u].x), __int_as_float(v[u].y), __int_as_float(v[u].z),
-                               __int_as_float(v[u].w));
-        const RegSource<kTileVecs> src{f, rem, len};
-        run_levels(st, 2, last, src, sh, mg);
-        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    exact_row_registers<kPaged>(v, rem, len, k, det, sh, em);
+}
+
+// Asks the memory system to bring tile t of the window (vectors
+// [t * T, min((t + 1) * T, nv))) into L2 ahead of its loads: one 1-D bulk
+// prefetch (16-byte aligned start and size), issued by one thread, costing
+// no registers while the bytes are in flight.
+__device__ __forceinline__ void prefetch_tile_l2(const float4* vbase, int t, int nv) {
+    constexpr int T = kTileVecs * kThreads;
+    const int j = t * T;
+    if (j >= nv) return;
+    const uint32_t bytes = static_cast<uint32_t>(min(T, nv - j)) * 16u;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vbase + j), "r"(bytes) : "memory");
+}
+constexpr int kPrefetchTiles = 4;  // tiles requested ahead of the one being filtered
+
+// Streaming route (nv > kTileVecs * kThreads vectors): two register tiles in
+// turn, one loading while the other is filtered, and the kPrefetchTiles
+// tiles after those on their way into L2; the sample is read from global
+// memory (spread over the whole window).
+template <bool kNonNeg>
+__device__ __forceinline__ void stream_filter(int4 (&cur)[kTileVecs], int4 (&nxt)[kTileVecs], const float4* vbase,
+                                              int nv, int rem, int len, uint32_t thr, uint32_t region,
+                                              uint32_t& wcount, bool& ovf) {
+    constexpr int T = kTileVecs * kThreads;
+    int j0 = 0;
+    for (int t = 0;; t += 2) {
+        if (threadIdx.x == 0) {  // tiles t + 2 + kPrefetchTiles, t + 3 + kPrefetchTiles into L2
+            prefetch_tile_l2(vbase, t + 2 + kPrefetchTiles, nv);
+            prefetch_tile_l2(vbase, t + 3 + kPrefetchTiles, nv);
+        }
+        filter_at<kNonNeg>(cur, thr, j0, nv, rem, len, region, wcount, kWarpCap, ovf);
+        j0 += T;
+        if (j0 >= nv) break;
+        if (j0 + T < nv) load_bits(cur, vbase, j0 + T, nv);
+        filter_at<kNonNeg>(nxt, thr, j0, nv, rem, len, region, wcount, kWarpCap, ovf);
+        j0 += T;
+        if (j0 >= nv) break;
+        if (j0 + T < nv) load_bits(nxt, vbase, j0 + T, nv);
     }
 }
 
-// Number of window positions p in [4*ja - rem, 4*jb - rem) (vectors [ja, jb)).
-__device__ __forceinline__ int window_count(int ja, int jb, int rem, int len) {
-    const int lo = max(4 * ja - rem, 0), hi = min(4 * jb - rem, len);
-    return max(hi - lo, 0);
-}
-
-
-// Streaming route over vectors [jb, je) of the aligned window: the whole row
-// on one CTA, or this CTA's slice of a row cut over a thread-block cluster.
-//  1. The slice's head tile gets a full level-1 histogram, which sets the
-//     slice's own lower bound on the threshold bin, aiming about 4 sigma
-//     above the slice head's expected share of the top-k (no cluster
-//     exchange).
-//  2. One pass over the rest collects every element at or above the bound.
-//  3. Level 1 comes from the merged histograms (on a cluster, merged only
-//     over the bins the slices' candidates occupy). It is exact when its
-//     threshold bin clears every slice's bound (each slice's counts are
-//     exact from its bound up); otherwise, or if a buffer overflowed, a full
-//     histogram pass and a re-collection run (always exact, only slower).
-//  4. Solo rows finish with finish_candidates; cluster rows run the radix
-//     levels and emit_selected over the slices' candidate buffers.
-template <bool kPaged, class Merge>
-__device__ void streaming_row(const float4* vbase, int jb, int je, int rem, int len, uint32_t k, bool det,
-                              const Shared& sh, const Merge& mg, const Emitter<kPaged>& em) {
+template <bool kPaged, int kLay>
+__device__ void stream_row(const Params& p, int b, const float* w, const float4* vbase, int nv, int rem, int len) {
+    const uint32_t k = static_cast<uint32_t>(p.k);
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
-    load_bits(cur, vbase, jb, je);                   // the head tile
-    if (jb + T < je) load_bits(nxt, vbase, jb + T, je);  // the next tile is in flight meanwhile
-    {
-        const uint32_t valid = tile_valid(jb, je, rem, len);
-#pragma unroll
-        for (int e = 0; e < 4 * kTileVecs; ++e)
-            if ((valid >> e) & 1u) atomicAdd(&sh.hist[bits_key(static_cast<uint32_t>(tile_elem(cur, e))) >> 20], 1u);
+    const int4 sv = sample_load(vbase, nv);  // nv > T > 512
+    load_bits(cur, vbase, 0, nv);
+    load_bits(nxt, vbase, T, nv);
+    if (threadIdx.x == 0)
+        for (int t = 2; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
+    const uint32_t bound_key = sample_bound_vec(sv, nv, rem, len, k, layout<kLay>());
+    const uint32_t thr = pass_threshold(bound_key);
+    const uint32_t region = saddr(layout<kLay>().cand) + (threadIdx.x >> 5) * (kWarpCap * 8u);
+    uint32_t wcount = 0;
+    bool ovf = false;
+    if (bound_key >= 0x80000000u) stream_filter<true>(cur, nxt, vbase, nv, rem, len, thr, region, wcount, ovf);
+    else stream_filter<false>(cur, nxt, vbase, nv, rem, len, thr, region, wcount, ovf);
+    const Shared sh = layout<kLay>();
+    const RowInfo ri = load_row(sh);
+    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
+    const Emitter<kPaged> em = row_emitter<kPaged>(p, b, ri, 0, len, kPageCache, sh);
+    SelState st;
+    const FinishResult r = finish_solo<kPaged>(bound_key, wcount, ovf, k, st, kWarpCap, sh, em);
+    if (r == kFinished) return;
+    if (r == kNeedLevels) {
+        finish_levels<kPaged>(st, k, det, sh, em);
+        return;
     }
-    __syncthreads();  // the head histogram is complete
-    // this part's lower bound, from its own head tile
-    const int n_head = window_count(jb, min(je, jb + T), rem, len);
-    uint32_t bound_bin = 0;
-    if (n_head > 0) {
-        const float expect = static_cast<float>(k) * static_cast<float>(n_head) / static_cast<float>(len);
-        const float tgt = fminf(expect + 4.0f * sqrtf(expect) + 16.0f, static_cast<float>(n_head));
-        bound_bin = find_threshold(sh.hist, kBins, max(static_cast<uint32_t>(tgt), 1u), sh).bin;
-    }
-    const uint32_t bound_key = bound_bin << 20;
-    collect_bits(cur, tile_pass(cur, jb, je, rem, len, bound_key), jb, rem, sh);
-    // two register tiles in turn: one is collected while the next loads
-    for (int j0 = jb + T; j0 < je;) {
-        if (j0 + T < je) load_bits(cur, vbase, j0 + T, je);
-        collect_bits<kCountLevel1>(nxt, tile_pass(nxt, j0, je, rem, len, bound_key), j0, rem, sh);
-        j0 += T;
-        if (j0 >= je) break;
-        if (j0 + T < je) load_bits(nxt, vbase, j0 + T, je);
-        collect_bits<kCountLevel1>(cur, tile_pass(cur, j0, je, rem, len, bound_key), j0, rem, sh);
-        j0 += T;
-    }
-    __syncthreads();
-    // Each part's histogram holds every head-tile element and every candidate
-    // after it, so its counts are exact for every bin at or above its bound;
-    // the merged level 1 is exact when its threshold bin clears every part's
-    // bound.
-    uint32_t max_bound = 0;
-    bool overflow = false;
-    const uint32_t* merged =
-        mg.merge_level1(sh, bound_bin, sh.cnt[0] > static_cast<uint32_t>(kCandCap), max_bound, overflow);
-    Threshold t1 = find_threshold(merged, kBins, k, sh);
-    bool cands_ok = true;
-    if (overflow || !t1.found || t1.bin < max_bound) {  // uniform over a cluster
-        // full level-1 histogram of this CTA's elements, then re-collect
-        clear_hist(sh.hist, kBins);
-        __syncthreads();
-        uint32_t* hist = sh.hist;
-        const GlobalSource all{vbase, jb, je, rem, len};
-        all.visit([&](uint32_t kk, int32_t, bool valid) {
-            if (valid) atomicAdd(&hist[kk >> 20], 1u);
-        });
-        merged = mg.merge(sh, kBins);
-        t1 = find_threshold(merged, kBins, k, sh);
-        cands_ok = false;
-        if (count_from(sh.hist, kBins, t1.bin, sh) <= static_cast<uint32_t>(kCandCap)) {
-            if (threadIdx.x == 0) sh.cnt[0] = 0;
-            __syncthreads();
-            for (int j0 = jb; j0 < je; j0 += T) {
-                load_bits(cur, vbase, j0, je);
-                collect_bits(cur, tile_pass(cur, j0, je, rem, len, t1.bin << 20), j0, rem, sh);
-            }
-            __syncthreads();
-            cands_ok = true;
-        }
-    }
-    SelState st{0ull, 0ull, k, false};
-    apply_level(st, 0, t1);
-    const int last = (det ? kAllLevels : kKeyLevels) - 1;
-    if (cands_ok) {
-        const CandSource src{sh.cand_key, sh.cand_pos, min(sh.cnt[0], static_cast<uint32_t>(kCandCap))};
-        int first = 1;
-        if (Merge::kSolo) {
-            if (finish_candidates<kPaged>(st, t1.bin, src.n, k, sh, em)) return;
-            first = 2;
-        }
-        run_levels(st, first, last, src, sh, mg);
-        emit_selected<kPaged>(st, k, src, sh, mg, em);
-    } else {
-        const GlobalSource src{vbase, jb, je, rem, len};
-        run_levels(st, 1, last, src, sh, mg);
-        emit_selected<kPaged>(st, k, src, sh, mg, em);
-    }
+    exact_row_global<kPaged>(vbase, nv, rem, len, k, det, sh, em);
 }
 
 // ----------------------------------------------------------------------------
@@ -1351,44 +1571,52 @@ __device__ void streaming_row(const float4* vbase, int jb, int je, int rem, int 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ bool plan_matches(const Params& p) {
-    const PlanHeader* h = p.hdr;
-    return h->magic == kPlanMagic && h->batch == p.batch && h->k == p.k;
+// Reads row b's inputs; a negative length, start or packed page-table start
+// makes the row empty and is counted (seq_len < 0 already by the plan when
+// `planned`).
+__device__ __forceinline__ RowInfo row_info(const Params& p, int b, bool kPagedMode) {
+    RowInfo r;
+    r.len = p.seq_lens[b];
+    r.start = p.row_starts ? p.row_starts[b] : 0;
+    r.offset = kPagedMode ? 0 : p.out_offsets[b];
+    r.table_row = (kPagedMode && p.row_to_batch) ? p.row_to_batch[b] : b;
+    r.token0 = (kPagedMode && p.pt_row_starts) ? p.pt_row_starts[b] : 0;
+    return r;
 }
 
-template <bool kPaged>
-__device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, int32_t offset, int32_t table_row,
-                                                        int32_t token0) {
-    Emitter<kPaged> em;
-    em.out = p.out + static_cast<int64_t>(b) * p.k;
-    em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
-    em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(table_row) * p.page_table_stride : nullptr;
-    em.pt_cached = nullptr;
-    em.token0 = token0;
-    em.pt_first = kPaged ? (token0 >> p.page_bits) : 0;
-    em.page_bits = p.page_bits;
-    em.offset = offset;
-    em.k = static_cast<uint32_t>(p.k);
-    em.flags = &p.hdr->flags;
-    return em;
-}
-
-// PAGED, non-trivial row: starts asynchronous copies of the page-table
-// entries its window's tokens token0 .. token0 + len - 1 map to (each one a
-// page some window position maps to) into shared memory when they fit; the
-// emit waits for them.
-template <bool kPaged>
-__device__ __forceinline__ void prefetch_pages(Emitter<kPaged>& em, int32_t len, const Shared& sh) {
-    if (!kPaged) return;
-    const int n = ((em.token0 + len - 1) >> em.page_bits) - em.pt_first + 1;
-    if (n > kPageCache) return;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sh.pages + i));
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(em.pt_row + em.pt_first + i)
-                     : "memory");
+__device__ __forceinline__ void check_row(RowInfo& r, bool planned, bool counter_thread, const Params& p) {
+    if (r.len < 0 || r.start < 0 || r.token0 < 0) {
+        if (counter_thread && (!planned || r.len >= 0)) atomicAdd(&p.hdr->error_rows, 1u);
+        r.len = 0;
+        r.token0 = 0;
+        r.start = 0;
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    em.pt_cached = sh.pages;
+}
+
+// One row on one CTA (trivial, register or streaming route); the shared
+// counters and histograms must be zero.
+template <bool kPaged, int kLay>
+__device__ void solo_row(const Params& p, int b, const RowInfo& r) {
+    const uint32_t k = static_cast<uint32_t>(p.k);
+    if (r.len <= p.k) {
+        trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r));
+        return;
+    }
+    prefetch_pages<kPaged>(p, r, 0, r.len, kPageCache, layout<kLay>());
+    park_row(r, layout<kLay>());  // read back after the score pass (published by its barriers)
+    const int rem = r.start & 3;
+    const float* w = p.scores + static_cast<int64_t>(b) * p.score_stride + r.start;
+    const float4* vbase = reinterpret_cast<const float4*>(w - rem);
+    const int nv = (r.len + rem + 3) >> 2;
+    if (nv <= kTileVecs * kThreads) register_row<kPaged, kLay>(p, b, vbase, nv, rem, r.len);
+    else stream_row<kPaged, kLay>(p, b, w, vbase, nv, rem, r.len);
+}
+
+// Zeroes the shared state one row needs (histograms, counters). No barrier.
+__device__ __forceinline__ void clear_row_state(const Shared& sh) {
+    clear_words(sh.shist(), 2 * kSmallWords);
+    clear_words(sh.hist(), 2 * kSmallWords + kWarps * kSmall);  // hist, mhist, whist
+    if (threadIdx.x < 48) sh.res()[threadIdx.x] = 0;  // res, cnt, wcnt (not the parked row)
 }
 
 // One CTA per row; rows come from the plan's order (longest first), rows the
@@ -1398,8 +1626,7 @@ __device__ __forceinline__ void prefetch_pages(Emitter<kPaged>& em, int32_t len,
 // registers.
 template <bool kPaged, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const Shared sh = carve(smem, false);
+    clear_row_state(layout<kLayRows>());  // shared memory only: before the grid dependency
     grid_dependency_wait();
     allow_dependents();
     // The header, this CTA's order entry and the row data of row blockIdx.x
@@ -1411,13 +1638,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const _
     const uint32_t magic = hdr->magic;
     const int32_t h_batch = hdr->batch, h_k = hdr->k, n_order = hdr->n_order;
     const int32_t ord = p.order[b0];
-    const int32_t len0 = p.seq_lens[b0];
-    const int32_t start0 = p.row_starts ? p.row_starts[b0] : 0;
-    const int32_t off0 = kPaged ? 0 : p.out_offsets[b0];
-    const int32_t table0 = (kPaged && p.row_to_batch) ? p.row_to_batch[b0] : b0;
-    const int32_t token00 = (kPaged && p.pt_row_starts) ? p.pt_row_starts[b0] : 0;
+    const RowInfo r0 = row_info(p, b0, kPaged);
     const bool planned = magic == kPlanMagic && h_batch == p.batch && h_k == p.k;
-    if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
     int b = b0;
     if (planned) {
         if (b0 >= n_order) return;
@@ -1425,93 +1647,281 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const _
     } else if (blockIdx.x == 0 && threadIdx.x == 0) {
         atomicOr(&p.hdr->flags, TOPK_DEVICE_FLAG_PLAN_MISMATCH);
     }
-    const bool same = b == b0;
-    int32_t len = same ? len0 : p.seq_lens[b];
-    const int32_t start = same ? start0 : (p.row_starts ? p.row_starts[b] : 0);
-    const int32_t offset = kPaged ? 0 : (same ? off0 : p.out_offsets[b]);
-    const int32_t table_row = same ? table0 : ((kPaged && p.row_to_batch) ? p.row_to_batch[b] : b);
-    const int32_t token0 = same ? token00 : ((kPaged && p.pt_row_starts) ? p.pt_row_starts[b] : 0);
-    if (len < 0 || start < 0 || token0 < 0) {
-        // seq_len < 0 was counted by the plan; count the rest here
-        if (threadIdx.x == 0 && (!planned || len >= 0)) atomicAdd(&p.hdr->error_rows, 1u);
-        len = 0;
-    }
-    const uint32_t k = static_cast<uint32_t>(p.k);
-    Emitter<kPaged> em = make_emitter<kPaged>(p, b, offset, table_row, token0 < 0 ? 0 : token0);
-    if (len <= p.k) {
-        trivial_row<kPaged>(len, k, em);
-        return;
-    }
-    prefetch_pages<kPaged>(em, len, sh);
-    if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
-    const int rem = start & 3;
-    const float4* vbase = reinterpret_cast<const float4*>(
-        p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
-    const int nv = (len + rem + 3) >> 2;
-    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
-    if (nv <= kTileVecs * kThreads) {
-        register_row<kPaged>(vbase, nv, rem, len, k, det, sh, em);
-    } else {
-        clear_hist(sh.hist, kBins);
-        __syncthreads();
-        streaming_row<kPaged>(vbase, 0, nv, rem, len, k, det, sh, SoloMerge{}, em);
+    RowInfo r = b == b0 ? r0 : row_info(p, b, kPaged);
+    check_row(r, planned, threadIdx.x == 0, p);
+    __syncthreads();  // the cleared state is visible
+    solo_row<kPaged, kLayRows>(p, b, r);
+}
+
+// ----------------------------------------------------------------------------
+// cluster route: bulk-copy staging, the cluster finish
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(m)), "r"(count) : "memory");
+}
+
+// One arrival plus the byte count the bulk copies completing on `m` will bring.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(m)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(m)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Waits for phase `parity` of `m` to complete, at most kWaitCycles; past that
+// it flags TOPK_DEVICE_FLAG_TIMEOUT and returns (the caller goes on, so no
+// barrier is left unmatched; the result is then flagged as unreliable).
+__device__ void mbar_wait(uint64_t* m, uint32_t parity, uint32_t* flags) {
+    if (mbar_try_wait(m, parity)) return;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(m, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+            if (lane_id() == 0) atomicOr(flags, TOPK_DEVICE_FLAG_TIMEOUT);
+            return;
+        }
     }
 }
 
-// One thread-block cluster per long row (looping over the plan's cluster list).
-// As for the rows kernel, kMinBlocks = 1 (no 64-register cap) serves launches
-// whose clusters all fit one CTA per SM.
-template <bool kPaged, int kMinBlocks>
-__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads, kMinBlocks)
-    topk_cluster_kernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const Shared sh = carve(smem, true);
-    grid_dependency_wait();
-    allow_dependents();
-    if (threadIdx.x < 4) sh.res[threadIdx.x] = 0;
-    if (!plan_matches(p)) return;  // uniform over the cluster: no barrier is skipped
+// Chunk c of this CTA's slice, vectors [jb + c * kStageVecs, ...) of the
+// aligned window, into stage c % kStages by one 1-D bulk copy (16-byte
+// aligned source, destination and size), completing on that stage's
+// mbarrier. One thread issues it.
+__device__ __forceinline__ void issue_chunk(const Shared& sh, const float4* vbase, int jb, int je, int c) {
+    const int s = c % kStages;
+    const int j = jb + c * kStageVecs;
+    const uint32_t bytes = static_cast<uint32_t>(min(kStageVecs, je - j)) * 16u;
+    mbar_expect_tx(&sh.mbar()[s], bytes);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(sh.stage + s * kStageVecs)),
+                 "l"(vbase + j), "r"(bytes), "r"(smem_addr(&sh.mbar()[s]))
+                 : "memory");
+}
+
+// The exact radix path over this CTA's slice (levels merged over the
+// cluster), from the staged copy when it is whole, else from global memory.
+// Ends with a cluster barrier (no CTA reads another's histograms after it).
+template <bool kPaged>
+__device__ __noinline__ void exact_slice(const float4* vbase, const float4* staged, int jb, int je, int rem, int len, uint32_t k,
+                            bool det, const Shared& sh0, const Emitter<kPaged>& em) {
+    const Shared sh = exact_view(sh0, true);
+    SelState st{0ull, 0ull, k, false};
+    const ClusterMerge mg;
+    if (staged) {
+        const VecSource<false> src{staged - jb, jb, je, rem, len};
+        run_levels(st, kLvlKey12, kLvlKeyLast, det, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    } else {
+        const GlobalSource src{vbase, jb, je, rem, len};
+        run_levels(st, kLvlKey12, kLvlKeyLast, det, src, sh, mg);
+        emit_selected<kPaged>(st, k, src, sh, mg, em);
+    }
+    cg::this_cluster().sync();
+}
+
+// One long row on the cluster: CTA `rank` takes the slice of vectors
+// [jb, je) of the aligned window. Every CTA draws the same sample of the
+// whole row, so every CTA computes the same bound; each filters its staged
+// slice into its candidate regions and counts them in its own 256-bin
+// histogram, which it then adds into every CTA's `mhist` with
+// distributed-shared-memory reductions (so each CTA searches an identical
+// copy); definite slots come from the leader's counter, and the threshold
+// bin's members are gathered in the leader's tie list and ranked there.
+// Ends with a cluster barrier after which the CTA's state is clean again
+// (the leader resets its counters after it).
+template <bool kPaged>
+__device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& phase) {
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
-    const int n_slots = static_cast<int>(gridDim.x) / kClusterSize;
-    const int slot = static_cast<int>(blockIdx.x) / kClusterSize;
-    const int n_rows = p.hdr->n_cluster;
-    const ClusterMerge mg;
-    const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
     const uint32_t k = static_cast<uint32_t>(p.k);
-    for (int i = slot; i < n_rows; i += n_slots) {
-        const int b = p.cluster_rows[i];
-        int32_t len = p.seq_lens[b];
-        const int32_t start = p.row_starts ? p.row_starts[b] : 0;
-        const int32_t table_row = (kPaged && p.row_to_batch) ? p.row_to_batch[b] : b;
-        const int32_t token0 = (kPaged && p.pt_row_starts) ? p.pt_row_starts[b] : 0;
-        if (len < 0 || start < 0 || token0 < 0) {
-            // seq_len < 0 was counted by the plan (cluster rows have seq_len > 32768)
-            if (rank == 0 && threadIdx.x == 0 && len >= 0) atomicAdd(&p.hdr->error_rows, 1u);
-            len = 0;
-        }
-        Emitter<kPaged> em =
-            make_emitter<kPaged>(p, b, kPaged ? 0 : p.out_offsets[b], table_row, token0 < 0 ? 0 : token0);
-        if (len <= p.k) {
-            if (rank == 0) trivial_row<kPaged>(len, k, em);
-            cluster.sync();
-            continue;
-        }
-        prefetch_pages<kPaged>(em, len, sh);
-        if (threadIdx.x < 8) sh.cnt[threadIdx.x] = 0;
-        clear_hist(sh.hist, kBins);
-        clear_hist(sh.mhist, kBins);
-        const int rem = start & 3;
-        const float4* vbase = reinterpret_cast<const float4*>(
-            p.scores + static_cast<int64_t>(b) * p.score_stride + (start - rem));
-        const int nv = (len + rem + 3) >> 2;
+    RowInfo r = row_info(p, b, kPaged);
+    check_row(r, true, rank == 0 && threadIdx.x == 0, p);
+    if (r.len <= p.k) {  // only a data error (an emptied row) makes a cluster row this short
+        if (rank == 0) trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r));
+    } else {
+        const int rem = r.start & 3;
+        const float* w = p.scores + static_cast<int64_t>(b) * p.score_stride + r.start;
+        const float4* vbase = reinterpret_cast<const float4*>(w - rem);
+        const int nv = (r.len + rem + 3) >> 2;
         const int per = (nv + kClusterSize - 1) / kClusterSize;
         const int jb = min(nv, rank * per);
         const int je = min(nv, jb + per);
-        // counters of the leader CTA must be zero before any CTA emits: the
-        // merges below pass several cluster barriers first
+        const int n_chunks = (je - jb + kStageVecs - 1) / kStageVecs;
+        const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
+        const int4 sv = sample_load(vbase, nv);  // the same sample of the whole row in every CTA
+        if (threadIdx.x == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the stages come first
+            for (int c = 0; c < min(n_chunks, kStages); ++c) issue_chunk(sh, vbase, jb, je, c);
+        }
+        const int32_t p_lo = max(4 * jb - rem, 0), p_hi = min(4 * je - rem, r.len);
+        prefetch_pages<kPaged>(p, r, p_lo, p_hi, kClusterPageCache, sh);
+        const uint32_t bound_key = sample_bound_vec(sv, nv, rem, r.len, k, sh);
+        const uint32_t thr = pass_threshold(bound_key);
+        const int warp = static_cast<int>(threadIdx.x >> 5);
+        const uint32_t region = saddr(sh.cand) + static_cast<uint32_t>(warp) * (kClusterWarpCap * 8u);
+        uint32_t wcount = 0;
+        bool ovf = false;
+        auto filter_slice = [&](auto nonneg) {
+            constexpr bool kNN = decltype(nonneg)::value;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int s = c % kStages;
+                mbar_wait(&sh.mbar()[s], (phase >> s) & 1u, &p.hdr->flags);
+                phase ^= 1u << s;
+                const int j0 = jb + c * kStageVecs;
+                int4 v[kTileVecs];
+                load_bits_smem(v, sh.stage + s * kStageVecs, min(kStageVecs, je - j0));
+                filter_at<kNN>(v, thr, j0, je, rem, r.len, region, wcount, kClusterWarpCap, ovf);
+                if (c + kStages < n_chunks) {
+                    __syncthreads();  // every thread is done with stage s
+                    if (threadIdx.x == 0) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue_chunk(sh, vbase, jb, je, c + kStages);
+                    }
+                }
+            }
+        };
+        if (bound_key >= 0x80000000u) filter_slice(std::true_type{});
+        else filter_slice(std::false_type{});
+
+        // the cluster finish
+        const Emitter<kPaged> em = row_emitter<kPaged>(p, b, r, p_lo, p_hi, kClusterPageCache, sh);
+        const uint32_t n = min(wcount, static_cast<uint32_t>(kClusterWarpCap));
+        const uint32_t base16 = bound_key >> 16;
+        if (lane_id() == 0) {
+            sh.wcnt()[warp] = n;
+            if (ovf)
+                for (int q = 0; q < kClusterSize; ++q) atomicOr(cluster.map_shared_rank(&sh.cnt()[3], q), 1u);
+        }
+        if (!ovf) count_candidates(region, n, base16, saddr(sh.whist() + warp * kSmall));
+        __syncthreads();  // this CTA's warp histograms are complete
+        if (threadIdx.x < kSmall) {
+            const uint32_t c = sum_warp_bins(sh);
+            if (c != 0u)
+                for (int q = 0; q < kClusterSize; ++q) atomicAdd(cluster.map_shared_rank(sh.mhist(), q) + threadIdx.x, c);
+        }
+        if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");
+        cluster.sync();  // every CTA's counts are in every CTA's mhist, every flag is set
+        bool done = false;
+        if (sh.cnt()[3] == 0u) {  // the same in every CTA, like mhist
+            const Threshold t = find_threshold(sh.mhist(), kSmall, k, sh);
+            if (t.found && t.bin != static_cast<uint32_t>(kSmall - 1)) {
+                const uint32_t need = k - t.above;
+                const bool exact = t.count == need;
+                if (!exact && t.count > static_cast<uint32_t>(kMaxRankTies)) {
+                    SelState st{static_cast<uint64_t>(base16 + t.bin) << 48, 0xFFFFull << 48, need, false};
+                    const RegionSource src{sh.cand, sh.wcnt(), kClusterWarpCap};
+                    run_levels(st, kLvlLow16, kLvlLow16Last, det, src, sh, ClusterMerge{});
+                    emit_selected<kPaged>(st, k, src, sh, ClusterMerge{}, em);
+                    cluster.sync();  // no CTA reads another's level bins after this
+                } else {
+                    // slot bases: this warp's place in the CTA, the CTA's in the row (one
+                    // atomic per CTA on the leader's counters)
+                    uint32_t def, tie;
+                    warp_counts(sh, t.bin, exact, def, tie);
+                    if (lane_id() == 0) {
+                        sh.red()[warp] = def;
+                        sh.red()[kWarps + warp] = tie;
+                    }
+                    __syncthreads();
+                    uint32_t def_base = 0, tie_base = 0, cta_def = 0, cta_tie = 0;
+#pragma unroll
+                    for (int q = 0; q < kWarps; ++q) {
+                        const uint32_t dq = sh.red()[q], tq = sh.red()[kWarps + q];
+                        def_base += q < warp ? dq : 0u;
+                        tie_base += q < warp ? tq : 0u;
+                        cta_def += dq;
+                        cta_tie += tq;
+                    }
+                    if (threadIdx.x == 0) {
+                        sh.res()[8] = cta_def ? atomicAdd(cluster.map_shared_rank(&sh.cnt()[1], 0), cta_def) : 0u;
+                        sh.res()[9] = cta_tie ? atomicAdd(cluster.map_shared_rank(&sh.cnt()[2], 0), cta_tie) : 0u;
+                    }
+                    __syncthreads();
+                    def_base += sh.res()[8];
+                    tie_base += sh.res()[9];
+                    const TieList leader_ties = tie_list(cluster.map_shared_rank(sh.ties(), 0));
+                    classify_write<kPaged>(region, n, base16, t.bin, exact, def_base, tie_base, leader_ties, em);
+                    if (!exact) {
+                        cluster.sync();  // the tie list is complete
+                        if (rank == 0) {
+                            const TieList ties = tie_list(sh.ties());
+                            rank_threshold_bin(t.count, need, k, ties.key, ties.pos, ties.rank,
+                                               [&](uint32_t s, int32_t pos) { em.write(s, pos); });
+                        }
+                    }
+                }
+                done = true;
+            }
+        }
+        if (!done)
+            exact_slice<kPaged>(vbase, n_chunks <= kStages ? sh.stage : nullptr, jb, je, rem, r.len, k, det, sh, em);
+    }
+    __syncthreads();  // every local use of this row's state is done
+    if (threadIdx.x == 0) sh.cnt()[3] = 0;
+    clear_words(sh.hist(), 2 * kSmallWords + kWarps * kSmall);  // hist, mhist, whist
+    clear_words(sh.shist(), 2 * kSmallWords);
+    cluster.sync();  // the row is done in every CTA; no CTA touches another's state for it any more
+    if (rank == 0 && threadIdx.x == 0) {
+        sh.cnt()[1] = 0;
+        sh.cnt()[2] = 0;
+    }
+}
+
+
+// One thread-block cluster per long row, looping over the plan's cluster list.
+// With all_rows set the same launch also takes every other row of the batch
+// (after the cluster rows of its slot): rank 0 of a cluster runs it as a
+// single-CTA row and the other CTAs of that cluster are done.
+template <bool kPaged>
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kThreads, 1)
+    topk_cluster_kernel(const __grid_constant__ Params p, int all_rows) {
+    const Shared sh = layout<kLayCluster>();
+    clear_row_state(sh);  // shared memory only: before the grid dependency
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&sh.mbar()[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    grid_dependency_wait();
+    allow_dependents();
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const PlanHeader* hdr = p.hdr;
+    const bool planned = hdr->magic == kPlanMagic && hdr->batch == p.batch && hdr->k == p.k;
+    const int n_cluster = planned ? hdr->n_cluster : 0;
+    const int n_rest = !all_rows ? 0 : planned ? hdr->n_order : p.batch;
+    if (all_rows && !planned && blockIdx.x == 0 && threadIdx.x == 0)
+        atomicOr(&p.hdr->flags, TOPK_DEVICE_FLAG_PLAN_MISMATCH);
+    const int n_slots = static_cast<int>(gridDim.x) / kClusterSize;
+    const int slot = static_cast<int>(blockIdx.x) / kClusterSize;
+    __syncthreads();  // the cleared state and the mbarriers are ready
+    if (slot < n_cluster) cluster.sync();  // every CTA of the cluster runs before any reaches into another
+    uint32_t phase = 0;
+    for (int i = slot; i < n_cluster + n_rest; i += n_slots) {
+        if (i < n_cluster) {
+            cluster_row<kPaged>(p, p.cluster_rows[i], sh, phase);
+            continue;
+        }
+        if (rank != 0) return;  // rows of the rest come after every cluster row of this slot
+        const int b = planned ? p.order[i - n_cluster] : i - n_cluster;
+        RowInfo r = row_info(p, b, kPaged);
+        check_row(r, planned, threadIdx.x == 0, p);
         __syncthreads();
-        streaming_row<kPaged>(vbase, jb, je, rem, len, k, det, sh, mg, em);
-        cluster.sync();  // all emits done before the leader's counters are reset
+        clear_row_state(sh);
+        __syncthreads();
+        solo_row<kPaged, kLayClusterSolo>(p, b, r);
     }
 }
 
@@ -1600,27 +2010,26 @@ __global__ void __launch_bounds__(kPlanThreads) topk_plan_kernel(const int32_t* 
     }
 }
 
+
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
 
 struct DeviceState {
     bool ready = false;
-    cudaError_t err = cudaSuccess;
-    int max_clusters = 0;       // co-resident clusters of the two-CTA-per-SM cluster build
-    int max_clusters_wide = 0;  // ... of the one-CTA-per-SM build
-    int sms = 0;                // streaming multiprocessors
+    int max_clusters = 0;  // co-resident clusters of the cluster kernel (one CTA per SM)
+    int sms = 0;           // streaming multiprocessors
 };
 
 constexpr int kMaxDevices = 64;
 DeviceState g_devices[kMaxDevices];
 std::mutex g_mutex;
 
-// Shared-memory size and co-resident cluster count of one cluster-kernel build.
-template <bool kPaged, int kMinBlocks>
+// Shared-memory size and co-resident cluster count of the cluster kernel.
+template <bool kPaged>
 cudaError_t prepare_cluster_kernel(int& max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged, kMinBlocks>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemCluster));
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemCluster));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterSize, 1, 1);
@@ -1634,7 +2043,7 @@ cudaError_t prepare_cluster_kernel(int& max_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kPaged, kMinBlocks>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, topk_cluster_kernel<kPaged>, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();  // the query is advisory: fall back to a conservative count
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
@@ -1646,16 +2055,14 @@ cudaError_t prepare_cluster_kernel(int& max_clusters) {
 }
 
 template <bool kPaged>
-cudaError_t prepare_kernels(int& max_clusters, int& max_clusters_wide) {
+cudaError_t prepare_kernels(int& max_clusters) {
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemRows));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_rows_kernel<kPaged, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemRows));
     if (e != cudaSuccess) return e;
-    e = prepare_cluster_kernel<kPaged, 2>(max_clusters);
-    if (e != cudaSuccess) return e;
-    return prepare_cluster_kernel<kPaged, 1>(max_clusters_wide);
+    return prepare_cluster_kernel<kPaged>(max_clusters);
 }
 
 cudaError_t device_state(DeviceState** out) {
@@ -1666,12 +2073,11 @@ cudaError_t device_state(DeviceState** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
     if (!st.ready) {
-        int mc = 0, mcw = 0;
-        e = prepare_kernels<true>(mc, mcw);
-        if (e == cudaSuccess) e = prepare_kernels<false>(mc, mcw);
+        int mc = 0;
+        e = prepare_kernels<true>(mc);
+        if (e == cudaSuccess) e = prepare_kernels<false>(mc);
         if (e != cudaSuccess) return e;
         st.max_clusters = mc > 0 ? mc : 1;
-        st.max_clusters_wide = mcw > 0 ? mcw : 1;
         e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         st.ready = true;
@@ -1700,22 +2106,34 @@ cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Kernels one transform of `batch` rows launches: a batch whose every row can
+// have a cluster of its own runs in the cluster kernel alone (its cluster rows
+// split, the others on one CTA each); a larger batch of at most
+// kClusterMaxBatch rows adds the cluster kernel to the rows kernel; above that
+// the rows kernel alone.
+int transform_launches(const DeviceState& ds, int32_t batch) {
+    if (batch <= 0) return 0;
+    if (batch <= kClusterMaxBatch && batch <= ds.max_clusters) return 1;
+    return batch <= kClusterMaxBatch ? 2 : 1;
+}
+
 template <bool kPaged>
 int launch_transform(const Params& prm, cudaStream_t stream) {
     DeviceState* ds = nullptr;
     if (device_state(&ds) != cudaSuccess) return TOPK_ERR_CUDA;
-    const cudaError_t le =
-        prm.batch <= ds->sms ? launch_pdl(topk_rows_kernel<kPaged, 1>, prm.batch, kThreads, kSmemRows, stream, prm)
-                             : launch_pdl(topk_rows_kernel<kPaged, 2>, prm.batch, kThreads, kSmemRows, stream, prm);
-    if (le != cudaSuccess) return TOPK_ERR_CUDA;
-    if (prm.batch <= kClusterMaxBatch) {
-        // every row's cluster resident at once with one CTA per SM: the wide build
+    const int B = prm.batch;
+    if (B <= kClusterMaxBatch && B <= ds->max_clusters) {
         const cudaError_t ce =
-            prm.batch <= ds->max_clusters_wide
-                ? launch_pdl(topk_cluster_kernel<kPaged, 1>, kClusterSize * prm.batch, kThreads, kSmemCluster, stream,
-                             prm)
-                : launch_pdl(topk_cluster_kernel<kPaged, 2>, kClusterSize * min(prm.batch, ds->max_clusters),
-                             kThreads, kSmemCluster, stream, prm);
+            launch_pdl(topk_cluster_kernel<kPaged>, kClusterSize * B, kThreads, kSmemCluster, stream, prm, 1);
+        return ce == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+    }
+    const cudaError_t le = B <= ds->sms
+                               ? launch_pdl(topk_rows_kernel<kPaged, 1>, B, kThreads, kSmemRows, stream, prm)
+                               : launch_pdl(topk_rows_kernel<kPaged, 2>, B, kThreads, kSmemRows, stream, prm);
+    if (le != cudaSuccess) return TOPK_ERR_CUDA;
+    if (B <= kClusterMaxBatch) {
+        const cudaError_t ce = launch_pdl(topk_cluster_kernel<kPaged>, kClusterSize * min(B, ds->max_clusters),
+                                          kThreads, kSmemCluster, stream, prm, 0);
         if (ce != cudaSuccess) return TOPK_ERR_CUDA;
     }
     return TOPK_OK;
@@ -1827,6 +2245,13 @@ int topk_read_device_errors(const void* workspace, int32_t* host_error_rows, uin
     *host_error_rows = static_cast<int32_t>(h.error_rows);
     if (host_flags) *host_flags = h.flags;
     return TOPK_OK;
+}
+
+int topk_transform_launches(int32_t batch) {
+    if (batch <= 0) return 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != cudaSuccess) return -1;
+    return transform_launches(*ds, batch);
 }
 
 const char* topk_status_string(int status) {

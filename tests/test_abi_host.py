@@ -38,6 +38,10 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_transform_launches_of_an_empty_batch(lib):
+    assert lib.topk_transform_launches(0) == 0 and lib.topk_transform_launches(-3) == 0
+
+
 def test_workspace_bytes(lib):
     assert lib.topk_workspace_bytes(-1) == 0
     assert lib.topk_workspace_bytes(0) == 256

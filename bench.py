@@ -52,7 +52,8 @@ L2_BYTES = 126 * 1024 * 1024
 HEADLINE = "ragged_extend"
 REF_BUDGET_S = 120.0     # the whole reference-arm run, warm-up included
 MAX_ROTATION_BYTES = 6 << 30   # device memory a rotation of small input sets may take
-KERNEL_SRC = os.path.join(ROOT, "sparse_attention_top_row_gb300", "csrc", "topk.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "sparse_attention_top_row_gb300", "csrc", f)
+               for f in ("topk.cu", "topk_common.cuh", "topk_select.cuh", "topk_select512.cu", "topk_select256.cu")]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -67,8 +68,12 @@ def measured_peaks():
 
 
 def kernel_source_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of the kernel sources, concatenated."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel, workload):

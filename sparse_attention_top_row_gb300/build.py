@@ -1,7 +1,9 @@
 """Builds the CUDA library in-tree (``_build/libtopk.so``) for sm_103a.
 
-One translation unit, one ``-gencode``, shared cudart (the same runtime
-PyTorch loads). nvcc cross-compiles without a GPU.
+Three translation units (the plan and C ABI, and the selection kernels
+compiled for 512 and for 256 threads per row), compiled in parallel to
+objects and linked into one shared library; one ``-gencode``, shared cudart
+(the same runtime PyTorch loads). nvcc cross-compiles without a GPU.
 """
 
 from __future__ import annotations
@@ -12,7 +14,9 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SRC = os.path.join(HERE, "csrc", "topk.cu")
+CSRC = os.path.join(HERE, "csrc")
+SOURCES = [os.path.join(CSRC, f) for f in ("topk.cu", "topk_select512.cu", "topk_select256.cu")]
+HEADERS = [os.path.join(CSRC, f) for f in ("topk_common.cuh", "topk_select.cuh")]
 HEADER = os.path.join(ROOT, "include", "topk.h")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libtopk.so")
@@ -37,23 +41,39 @@ def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in (SRC, HEADER, __file__))
+    return any(os.path.getmtime(f) > t for f in (*SOURCES, *HEADERS, HEADER, __file__))
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if not force and not needs_build():
         return LIB
+    from concurrent.futures import ThreadPoolExecutor
+
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = nvcc_path()
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-cudart", "shared", f"-I{os.path.join(ROOT, 'include')}", SRC, "-o", tmp]
+    tag = f".tmp{os.getpid()}"
+    common = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{os.path.join(ROOT, 'include')}",
+              f"-I{CSRC}", *extra_flags]
+    objs = [os.path.join(BUILD_DIR, os.path.basename(src) + tag + ".o") for src in SOURCES]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        cmd = common + ["-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        subprocess.run(cmd, check=True)
+
+    with ThreadPoolExecutor(len(SOURCES)) as ex:
+        list(ex.map(compile_one, zip(SOURCES, objs)))
+    tmp = LIB + tag
+    link = [nvcc, ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp]
     for d in cuda_lib_dirs(nvcc):
-        cmd += ["-Xlinker", f"-rpath,{d}"]
-    cmd += list(extra_flags)
+        link += ["-Xlinker", f"-rpath,{d}"]
     if verbose:
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
+        print(" ".join(link), flush=True)
+    subprocess.run(link, check=True)
+    for obj in objs:
+        os.remove(obj)
     os.replace(tmp, LIB)
     return LIB
 

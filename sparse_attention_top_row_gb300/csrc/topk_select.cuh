@@ -90,6 +90,12 @@
 #ifndef TOPK_PAGE_CACHE
 #define TOPK_PAGE_CACHE 4096  // page-table entries of a single-CTA row held in shared memory
 #endif
+#ifndef TOPK_PRESAMPLED
+#define TOPK_PRESAMPLED 0  // 1: streamed rows take their bound from Params::bounds (bound kernel)
+#endif
+#ifndef TOPK_COMPACT_LISTS
+#define TOPK_COMPACT_LISTS 1  // 1: streamed rows collect candidates in per-thread compact lists
+#endif
 
 namespace topk_impl {
 namespace TOPK_NS {
@@ -266,6 +272,9 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
     return v;
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t a) {
     uint2 v;
@@ -1507,18 +1516,258 @@ __device__ __forceinline__ void stream_filter(int4 (&cur)[kTileVecs], int4 (&nxt
     }
 }
 
+// ----------------------------------------------------------------------------
+// streamed rows: compact per-thread candidate lists
+// ----------------------------------------------------------------------------
+//
+// Each thread appends its candidates to a list of its own: entry s of thread
+// t is word s * kThreads + t of the candidate buffer (interleaved, so a
+// warp's lanes storing their s-th entries hit 32 different banks). An entry
+// packs the top 16 bits of the score's fp32 pattern (all the finish's
+// histogram needs) with the element's 16-bit index l in the thread's share of
+// the row: l = 16 * tile + 4 * u + c for lane c of the thread's vector u of a
+// tile, so position = 4 * (tile * T + u * kThreads + t) + c - rem. The filter
+// then needs no per-tile count and no warp scan: per element one compare, one
+// add, one byte permute, one predicated store and one predicated add. The
+// few members of the threshold bin, which need their full keys, are read
+// again from global memory (L2).
+
+constexpr int kListCap = kCandBytes / (kThreads * 4);  // entries per thread
+constexpr uint32_t kListStride = kThreads * 4u;        // bytes between a thread's entries
+constexpr int kListMaxTiles = 4096;                    // tiles a 16-bit index covers
+static_assert(kTileVecs == 4 && kListCap >= 24, "list layout");
+
+#define TOPK_LA_HEAD "{\n\t.reg .pred q, v, r;\n\t.reg .b32 t;\n\t"
+#define TOPK_LA_GE "setp.ge.s32 q, %1, %2;\n\t"
+#define TOPK_LA_LE "setp.le.u32 q, %1, %2;\n\t"
+#define TOPK_LA_MASK "and.b32 t, %4, %7;\n\tsetp.ne.b32 v, t, 0;\n\t"
+#define TOPK_LA_GE_M "setp.ge.and.s32 q, %1, %2, v;\n\t"
+#define TOPK_LA_LE_M "setp.le.and.u32 q, %1, %2, v;\n\t"
+#define TOPK_LA_ENTRY "add.u32 t, %3, %6;\n\tprmt.b32 t, t, %1, 0x7610;\n\t"
+#define TOPK_LA_STORE "@q st.shared.u32 [%0], t;\n\t@q add.u32 %0, %0, %8;\n\t}"
+#define TOPK_LA_STORE_CHK "setp.lt.and.u32 r, %0, %5, q;\n\t@r st.shared.u32 [%0], t;\n\t@q add.u32 %0, %0, %8;\n\t}"
+#define TOPK_LA_ARGS                                                                                       \
+    : "+r"(a) : "r"(bits), "r"(thr), "r"(lb), "r"(valid), "r"(lim), "n"(kOff), "n"(1 << kBit), "n"(kListStride) \
+    : "memory"
+
+// Appends the entry of element kOff of the tile (bits, index lb + kOff) at
+// shared address a and advances a by one list stride when the bits pass the
+// bound (thr: see passes); kMasked: only if bit kBit of `valid` is set;
+// kChecked: the store is skipped at or past `lim` (a still advances, so a
+// final a > lim reports the overflow).
+template <bool kNonNeg, bool kMasked, bool kChecked, int kOff, int kBit>
+__device__ __forceinline__ void list_append(uint32_t& a, int32_t bits, uint32_t thr, uint32_t lb, uint32_t valid,
+                                            uint32_t lim) {
+    if constexpr (!kMasked && !kChecked) {
+        if constexpr (kNonNeg) asm volatile(TOPK_LA_HEAD TOPK_LA_GE TOPK_LA_ENTRY TOPK_LA_STORE TOPK_LA_ARGS);
+        else asm volatile(TOPK_LA_HEAD TOPK_LA_LE TOPK_LA_ENTRY TOPK_LA_STORE TOPK_LA_ARGS);
+    } else if constexpr (!kMasked) {
+        if constexpr (kNonNeg) asm volatile(TOPK_LA_HEAD TOPK_LA_GE TOPK_LA_ENTRY TOPK_LA_STORE_CHK TOPK_LA_ARGS);
+        else asm volatile(TOPK_LA_HEAD TOPK_LA_LE TOPK_LA_ENTRY TOPK_LA_STORE_CHK TOPK_LA_ARGS);
+    } else {
+        static_assert(kChecked, "masked tiles are always checked");
+        if constexpr (kNonNeg)
+            asm volatile(TOPK_LA_HEAD TOPK_LA_MASK TOPK_LA_GE_M TOPK_LA_ENTRY TOPK_LA_STORE_CHK TOPK_LA_ARGS);
+        else asm volatile(TOPK_LA_HEAD TOPK_LA_MASK TOPK_LA_LE_M TOPK_LA_ENTRY TOPK_LA_STORE_CHK TOPK_LA_ARGS);
+    }
+}
+#undef TOPK_LA_HEAD
+#undef TOPK_LA_GE
+#undef TOPK_LA_LE
+#undef TOPK_LA_MASK
+#undef TOPK_LA_GE_M
+#undef TOPK_LA_LE_M
+#undef TOPK_LA_ENTRY
+#undef TOPK_LA_STORE
+#undef TOPK_LA_STORE_CHK
+#undef TOPK_LA_ARGS
+
+template <bool kNonNeg, bool kMasked, bool kChecked>
+__device__ __forceinline__ void list_tile(const int4 (&v)[kTileVecs], uint32_t thr, uint32_t lb, uint32_t valid,
+                                          uint32_t& a, uint32_t lim) {
+    for_each_elem<0>([&](auto ec) {
+        constexpr int e = decltype(ec)::value;
+        list_append<kNonNeg, kMasked, kChecked, e, e>(a, tile_elem(v, e), thr, lb, valid, lim);
+    });
+}
+
+// The tile at vector j0 (index base lb = 16 * tile): tiles at the window's
+// edges are masked; a warp with a lane within one tile of its list's end
+// takes the checked appends, every other warp the plain ones.
+template <bool kNonNeg>
+__device__ __forceinline__ void list_at(const int4 (&v)[kTileVecs], uint32_t thr, int j0, int je, int rem, int len,
+                                        uint32_t lb, uint32_t& a, uint32_t lim) {
+    if (!tile_interior(j0, je, rem, len))
+        list_tile<kNonNeg, true, true>(v, thr, lb, tile_valid(j0, je, rem, len), a, lim);
+    else if (__any_sync(kFull, a + static_cast<uint32_t>(kTileElems) * kListStride > lim))
+        list_tile<kNonNeg, false, true>(v, thr, lb, 0xFFFFu, a, lim);
+    else
+        list_tile<kNonNeg, false, false>(v, thr, lb, 0xFFFFu, a, lim);
+}
+
+// The streamed window (nv <= kListMaxTiles tiles) into the lists: two register
+// tiles in turn, as stream_filter. a: this thread's list cursor (shared
+// address), lim: its end.
+template <bool kNonNeg>
+__device__ __forceinline__ void stream_list(int4 (&cur)[kTileVecs], int4 (&nxt)[kTileVecs], const float4* vbase,
+                                            int nv, int rem, int len, uint32_t thr, uint32_t& a, uint32_t lim) {
+    constexpr int T = kTileVecs * kThreads;
+    int j0 = 0;
+    uint32_t lb = 0;
+    for (int t = 0;; t += 2) {
+        if (threadIdx.x == 0) {
+            prefetch_tile_l2(vbase, t + 2 + kPrefetchTiles, nv);
+            prefetch_tile_l2(vbase, t + 3 + kPrefetchTiles, nv);
+        }
+        list_at<kNonNeg>(cur, thr, j0, nv, rem, len, lb, a, lim);
+        j0 += T;
+        lb += kTileElems;
+        if (j0 >= nv) break;
+        if (j0 + T < nv) load_bits(cur, vbase, j0 + T, nv);
+        list_at<kNonNeg>(nxt, thr, j0, nv, rem, len, lb, a, lim);
+        j0 += T;
+        lb += kTileElems;
+        if (j0 >= nv) break;
+        if (j0 + T < nv) load_bits(nxt, vbase, j0 + T, nv);
+    }
+}
+
+// Bits 31..16 of an entry's key (the order-preserving map of its top 16 bits).
+__device__ __forceinline__ uint32_t entry_key16(uint32_t e) {
+    return (e >> 16) ^ ((static_cast<uint32_t>(static_cast<int32_t>(e) >> 31) & 0x7FFFu) | 0x8000u);
+}
+// The window position of this thread's entry e: with l its low 16 bits,
+// 4 * (tile * T + u * kThreads + t) + c - rem = ((l & ~3) << log2(kThreads))
+// + (l & 3) + tbase, tbase = 4 * t - rem.
+constexpr int kLogThreads = kThreads == 512 ? 9 : kThreads == 256 ? 8 : kThreads == 128 ? 7 : -1;
+static_assert(kLogThreads > 0 && (1 << kLogThreads) == kThreads, "power-of-two teams");
+__device__ __forceinline__ int32_t entry_pos(uint32_t e, int32_t tbase) {
+    const uint32_t l = e & 0xFFFFu;
+    return static_cast<int32_t>(((l & ~3u) << kLogThreads) + (l & 3u)) + tbase;
+}
+__device__ __forceinline__ uint32_t fine_bin16(uint32_t key16, uint32_t base16) {
+    return min(key16 - base16, static_cast<uint32_t>(kSmall - 1));
+}
+
+// The fast finish over the compact lists (n_raw: this thread's appends, more
+// than kListCap meaning its list overflowed); w: the window's scores, for
+// the threshold bin's full keys. As finish_solo, except that a threshold bin
+// too full to rank also sends the row to the exact path, that the count pass
+// writes each entry's bin over its top 16 bits for the classify pass, and
+// that the selected positions are first gathered in shared memory (the
+// per-warp histograms' space, free by then; a warp's definite entries of one
+// list depth take consecutive slots, threshold-bin members go to the tie list
+// through a shared counter) and then written out slot by slot, so that every
+// global store is coalesced. kNeedExact: nothing was written.
+template <bool kPaged>
+__device__ __forceinline__ FinishResult finish_list(uint32_t bound_key, uint32_t n_raw, uint32_t k, int rem, const float* w,
+                                    const Shared& sh, const Emitter<kPaged>& em) {
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const bool ovf = n_raw > static_cast<uint32_t>(kListCap);
+    const uint32_t n = min(n_raw, static_cast<uint32_t>(kListCap));
+    const uint32_t nmax = __reduce_max_sync(kFull, n);
+    const uint32_t base16 = bound_key >> 16;
+    uint32_t* const lp = reinterpret_cast<uint32_t*>(sh.cand) + threadIdx.x;  // entry s at lp[s * kThreads]
+    uint32_t* const whw = sh.whist() + warp * kSmall;
+#pragma unroll 2
+    for (uint32_t s = 0; s < nmax; ++s) {
+        if (s < n) {
+            const uint32_t e = lp[s * kThreads];
+            const uint32_t bin = fine_bin16(entry_key16(e), base16);
+            atomicAdd(&whw[bin], 1u);
+            lp[s * kThreads] = (bin << 16) | (e & 0xFFFFu);
+        }
+    }
+    if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // page-table entries, published below
+    if (__syncthreads_or(ovf)) return kNeedExact;
+    if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
+    __syncthreads();
+    const Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    if (!t.found || t.bin == static_cast<uint32_t>(kSmall - 1)) return kNeedExact;
+    const uint32_t need = k - t.above;
+    const bool exact = t.count == need;
+    if (!exact && t.count > static_cast<uint32_t>(kMaxRankTies)) return kNeedExact;
+    uint32_t def, tie;
+    warp_counts(sh, t.bin, exact, def, tie);
+    if (lane_id() == 0) sh.red()[warp] = def;
+    const uint32_t tau = t.bin;
+    // bins above the threshold bin, and the threshold bin itself when exact
+    const uint32_t lowest = exact ? tau : tau + 1u;
+    const int32_t tbase = 4 * static_cast<int32_t>(threadIdx.x) - rem;
+    const TieList ties = tie_list(sh.ties());
+    __syncthreads();  // the warps' counts
+    uint32_t slot = 0;
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) slot += q < warp ? sh.red()[q] : 0u;
+    const uint32_t lt = lanemask_lt();
+    static_assert(kWarps * kSmall >= TOPK_MAX_K, "the gathered slots fit the per-warp histograms");
+    int32_t* const stage = reinterpret_cast<int32_t*>(sh.whist());  // slot -> position
+    uint32_t* const n_ties = &sh.cnt()[2];
+#pragma unroll 2
+    for (uint32_t s = 0; s < nmax; ++s) {
+        const bool valid = s < n;
+        const uint32_t e = valid ? lp[s * kThreads] : 0u;
+        const uint32_t bin = e >> 16;
+        const bool d = valid && bin >= lowest;
+        const uint32_t m = __ballot_sync(kFull, d);
+        const uint32_t sl = slot + static_cast<uint32_t>(__popc(m & lt));
+        if (d && sl < k) stage[sl] = entry_pos(e, tbase);  // (sl < k always holds when consistent)
+        slot += static_cast<uint32_t>(__popc(m));
+        if (!exact && valid && bin == tau)  // a threshold-bin member (few per row)
+            ties.pos[atomicAdd(n_ties, 1u)] = entry_pos(e, tbase);
+    }
+    if (!exact) {
+        __syncthreads();  // the members' positions; their keys are read in one round trip
+        if (threadIdx.x < t.count)
+            ties.key[threadIdx.x] = bits_key(__ldg(reinterpret_cast<const uint32_t*>(w) + ties.pos[threadIdx.x]));
+        __syncthreads();
+        rank_threshold_bin(t.count, need, k, ties.key, ties.pos, ties.rank, [&](uint32_t s, int32_t pos) {
+            if (s < k) stage[s] = pos;
+        });
+    }
+    __syncthreads();  // every slot gathered
+    for (uint32_t i = threadIdx.x; i < k; i += kThreads) em.write(i, stage[i]);
+    return kFinished;
+}
+
+// The bound comes from the row's own sample, or (TOPK_PRESAMPLED) from the
+// bound kernel that ran before this one (Params::bounds; the rows kernel is
+// then free to start streaming at once).
 template <bool kPaged, int kLay>
 __device__ void stream_row(const Params& p, int b, const float* w, const float4* vbase, int nv, int rem, int len) {
     const uint32_t k = static_cast<uint32_t>(p.k);
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
+#if TOPK_PRESAMPLED
+    const uint32_t bound_key = p.bounds[b];
+    load_bits(cur, vbase, 0, nv);
+    load_bits(nxt, vbase, T, nv);
+    if (threadIdx.x == 0)
+        for (int t = 2; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
+#else
     const SampleVecs sv = sample_load(vbase, nv);  // nv > T >= 1024
     load_bits(cur, vbase, 0, nv);
     load_bits(nxt, vbase, T, nv);
     if (threadIdx.x == 0)
         for (int t = 2; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
     const uint32_t bound_key = sample_bound_vec(sv, nv, rem, len, k, layout<kLay>());
+#endif
     const uint32_t thr = pass_threshold(bound_key);
+#if TOPK_COMPACT_LISTS
+    if (nv <= kListMaxTiles * T) {
+        const uint32_t a0 = saddr(layout<kLay>().cand) + threadIdx.x * 4u;
+        const uint32_t lim = a0 + static_cast<uint32_t>(kListCap) * kListStride;
+        uint32_t a = a0;
+        if (bound_key >= 0x80000000u) stream_list<true>(cur, nxt, vbase, nv, rem, len, thr, a, lim);
+        else stream_list<false>(cur, nxt, vbase, nv, rem, len, thr, a, lim);
+        const Shared sh = layout<kLay>();
+        const RowInfo ri = load_row(sh);
+        const Emitter<kPaged> em = row_emitter<kPaged>(p, b, ri, 0, len, kPageCache, sh);
+        if (finish_list<kPaged>(bound_key, (a - a0) / kListStride, k, rem, w, sh, em) == kFinished) return;
+        exact_row_global<kPaged>(vbase, nv, rem, len, k, (p.flags & TOPK_DETERMINISTIC) != 0, sh, em);
+        return;
+    }
+#endif
     const uint32_t region = saddr(layout<kLay>().cand) + (threadIdx.x >> 5) * (kWarpCap * 8u);
     uint32_t wcount = 0;
     bool ovf = false;
@@ -1593,9 +1842,7 @@ __device__ __forceinline__ void clear_row_state(const Shared& sh) {
 
 // One CTA per row; rows come from the plan's order (longest first), rows the
 // plan gave to the cluster path are skipped (their CTAs exit at once).
-// kMinBlocks = 2 keeps two CTAs per SM (64 registers a thread); batches that
-// fit one CTA per SM use kMinBlocks = 1, which lets the code keep more in
-// registers.
+// kMinBlocks: CTAs per SM the register budget is sized for.
 template <bool kPaged, int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) topk_rows_kernel(const __grid_constant__ Params p) {
     clear_row_state(layout<kLayRows>());  // shared memory only: before the grid dependency

@@ -1,7 +1,8 @@
 // The 256-thread build of the selection kernels: the rows kernel for large
 // batches (more rows than SMs), four CTAs of 256 threads per SM, so that four
-// rows are in flight on every SM and one row's latency-bound phases (the
-// sample, the finish) overlap the others' score streams.
+// rows are in flight on every SM and one row's latency-bound finish overlaps
+// the others' score streams. Its streamed rows take their threshold bounds
+// from the bound kernel, which runs first.
 #define TOPK_THREADS 256
 #define TOPK_NS t256
 #define TOPK_WITH_CLUSTER 0
@@ -9,15 +10,18 @@
 #define TOPK_CTAS_PER_SM 4
 #endif
 #ifndef TOPK_WARP_CAP
-#define TOPK_WARP_CAP 480
+#define TOPK_WARP_CAP 512
 #endif
 #ifndef TOPK_PAGE_CACHE
 #define TOPK_PAGE_CACHE 1024
 #endif
+#define TOPK_PRESAMPLED 1
 #include "topk_select.cuh"
 
 namespace topk_impl {
 namespace t256 {
+
+static_assert(kStreamVecs == kTileVecs * kThreads, "rows streamed by this build are the rows given bounds");
 
 cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<true, TOPK_CTAS_PER_SM>, cudaFuncAttributeMaxDynamicSharedMemorySize,

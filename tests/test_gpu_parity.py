@@ -511,3 +511,17 @@ def test_full_mixed_boundary_single_rows(cuda_lib, bi):
     for mode in ("paged", "ragged"):
         w = wl.mixed("cuda", mode=mode, k=2048, batch=1, boundary_index=bi, sub_id=50 + bi)
         _sample_and_check(cuda_lib, w, [0])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["extend", "decode"])
+def test_fast_path_takes_every_row(cuda_lib, name):
+    """The sample bounds hold on the benchmark's workloads: no row of a full
+    extend chunk (bound kernel, then the 256-thread rows kernel) or of the
+    decode batch (in-kernel sample) falls back to the exact path, going by the
+    plan header's count of exact-path rows."""
+    w = wl.ragged_extend("cuda", chunk=3) if name == "extend" else wl.paged_decode("cuda")
+    _, _, ws = cuda_lib.run_workload(w)
+    torch.cuda.synchronize()
+    hdr = ws[:64].cpu().numpy().view(np.uint32)
+    assert hdr[7] == 0, f"{hdr[7]} rows took the exact path"

@@ -53,8 +53,7 @@ HEADLINE = "ragged_extend"
 REF_BUDGET_S = 120.0     # the whole reference-arm run, warm-up included
 MAX_ROTATION_BYTES = 6 << 30   # device memory a rotation of small input sets may take
 KERNEL_SRCS = [os.path.join(ROOT, "sparse_attention_top_row_gb300", "csrc", f)
-               for f in ("topk.cu", "topk_common.cuh", "topk_select.cuh", "topk_select512.cu", "topk_select256.cu",
-                         "topk_bound.cu")]
+               for f in ("topk.cu", "topk_common.cuh", "topk_select.cuh", "topk_select512.cu", "topk_select256.cu")]
 
 
 # ----------------------------------------------------------------------------- helpers

@@ -87,9 +87,7 @@ typedef enum {
 
 /*
  * Bytes of device workspace that topk_plan and the transforms need for
- * `batch` rows (a small header plus three 32-bit lists of `batch` entries:
- * two the plan writes, one the transforms of batches larger than the SM
- * count write and read: per-row threshold bounds).
+ * `batch` rows (a small header plus two int32 lists of `batch` entries).
  * Host only, pure. Returns 0 for batch < 0.
  */
 TOPK_API size_t topk_workspace_bytes(int32_t batch);
@@ -115,11 +113,7 @@ TOPK_API size_t topk_workspace_bytes(int32_t batch);
  * consumes the plan; one plan serves any number of transforms with the same
  * seq_lens, batch and k (e.g. every layer of a decode step). A transform whose
  * (batch, k) does not match the plan sets TOPK_DEVICE_FLAG_PLAN_MISMATCH and
- * still computes the right result, without the cluster path. Transforms of
- * more rows than SMs also write per-row threshold bounds into the workspace
- * and read them back: transforms that share one workspace should be ordered
- * (one stream); overlapping ones still compute the right result (a bound is
- * only a hint, checked before use) but may take the slower exact path.
+ * still computes the right result, without the cluster path.
  */
 TOPK_API int topk_plan(const int32_t* seq_lens, int32_t batch, int32_t k, void* workspace,
                        size_t workspace_bytes, topk_stream_t stream);
@@ -234,7 +228,7 @@ TOPK_API int topk_read_device_errors(const void* workspace, int32_t* host_error_
  *   batch must be at most TOPK_NOALLOC_MAX_BATCH; a larger batch returns
  *   TOPK_ERR_WORKSPACE and enqueues nothing.
  *
- * The built-in workspace is about 192 KB, held by every GPU that loads the
+ * The built-in workspace is about 128 KB, held by every GPU that loads the
  * library until the process exits. The first call on a device looks up its
  * address (no allocation); make that first call before any stream capture.
  * Every call on a device shares the one array and rewrites it: calls whose
@@ -254,9 +248,7 @@ TOPK_API int topk_transform_ragged_noalloc(const float* scores, int64_t score_st
  * device (after the plan's one): 1 or 2 (0 for batch <= 0; -1 if the device
  * cannot be queried). A batch whose every row can own a thread-block cluster
  * runs in one kernel; batches of up to 64 rows beyond that add the cluster
- * kernel for their long rows to the per-row kernel; batches of more rows than
- * the device has SMs run a bound kernel (a threshold bound per long row,
- * from a sample) before the per-row kernel. Host only; the first call
+ * kernel for their long rows to the per-row kernel. Host only; the first call
  * on a device sets up the kernels' attributes, like the first transform.
  */
 TOPK_API int topk_transform_launches(int32_t batch);

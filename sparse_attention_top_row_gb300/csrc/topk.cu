@@ -32,11 +32,10 @@ constexpr int kBandCluster = 33;
 constexpr int kBands = 34;
 
 
-// Workspace: the plan header, order[batch] and cluster_rows[batch] (written
-// by the plan), bounds[batch] (written by a transform's bound kernel).
+// Workspace: the plan header, order[batch] and cluster_rows[batch].
 size_t workspace_bytes_for(int32_t batch) {
     if (batch < 0) return 0;
-    size_t bytes = sizeof(PlanHeader) + 3 * sizeof(int32_t) * static_cast<size_t>(batch);
+    size_t bytes = sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(batch);
     return (bytes + 255) / 256 * 256;
 }
 
@@ -167,14 +166,12 @@ bool valid_k(int32_t k) { return k >= 1 && k <= TOPK_MAX_K; }
 // Kernels one transform of `batch` rows launches: a batch whose every row can
 // have a cluster of its own runs in the cluster kernel alone (its cluster rows
 // split, the others on one CTA each); a larger batch of at most
-// kClusterMaxBatch rows adds the cluster kernel to the rows kernel; up to one
-// row per SM the rows kernel alone; above that the bound kernel and the rows
-// kernel.
+// kClusterMaxBatch rows adds the cluster kernel to the rows kernel; above that
+// the rows kernel alone.
 int transform_launches(const DeviceState& ds, int32_t batch) {
     if (batch <= 0) return 0;
     if (batch <= kClusterMaxBatch && batch <= ds.max_clusters) return 1;
-    if (batch <= kClusterMaxBatch) return 2;
-    return batch <= ds.sms ? 1 : 2;
+    return batch <= kClusterMaxBatch ? 2 : 1;
 }
 
 // The launch plan of a transform:
@@ -182,8 +179,7 @@ int transform_launches(const DeviceState& ds, int32_t batch) {
 //     kernel alone (512 threads per CTA);
 //   batch <= SMs: the 512-thread rows kernel, one CTA per SM (plus the
 //     cluster kernel for the long rows of batches up to kClusterMaxBatch);
-//   larger batches: the bound kernel (a threshold bound for every row the
-//     next kernel streams), then the 256-thread rows kernel, four CTAs per SM.
+//   larger batches: the 256-thread rows kernel, four CTAs per SM.
 template <bool kPaged>
 int launch_transform(const Params& prm, cudaStream_t stream) {
     DeviceState* ds = nullptr;
@@ -191,16 +187,8 @@ int launch_transform(const Params& prm, cudaStream_t stream) {
     const int B = prm.batch;
     if (B <= kClusterMaxBatch && B <= ds->max_clusters)
         return t512::launch_cluster(kPaged, B, 1, prm, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
-    cudaError_t le;
-    if (B <= ds->sms) {
-        le = t512::launch_rows(kPaged, true, prm, stream);
-    } else {
-        Params p = prm;
-        uint32_t* bounds = reinterpret_cast<uint32_t*>(const_cast<int32_t*>(prm.cluster_rows) + B);
-        p.bounds = bounds;
-        le = bound::launch(p, bounds, t256::kStreamVecs, stream);
-        if (le == cudaSuccess) le = t256::launch_rows(kPaged, p, stream);
-    }
+    const cudaError_t le = B <= ds->sms ? t512::launch_rows(kPaged, true, prm, stream)
+                                        : t256::launch_rows(kPaged, prm, stream);
     if (le != cudaSuccess) return TOPK_ERR_CUDA;
     if (B <= kClusterMaxBatch &&
         t512::launch_cluster(kPaged, min(B, ds->max_clusters), 0, prm, stream) != cudaSuccess)
@@ -347,7 +335,7 @@ const char* topk_status_string(int status) {
 namespace {
 
 constexpr size_t kNoAllocWorkspaceBytes =
-    (sizeof(PlanHeader) + 3 * sizeof(int32_t) * static_cast<size_t>(TOPK_NOALLOC_MAX_BATCH) + 255) / 256 * 256;
+    (sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(TOPK_NOALLOC_MAX_BATCH) + 255) / 256 * 256;
 
 }  // namespace
 
@@ -402,9 +390,8 @@ extern "C" int topk_transform_ragged_noalloc(const float* scores, int64_t score_
     if (batch == 0) return TOPK_OK;
     void* ws = nullptr;
     if (noalloc_workspace(&ws) != cudaSuccess) return TOPK_ERR_CUDA;
-    // the plan rewrites the whole header and both row lists, and the bound
-    // kernel every bound the rows kernel reads, so nothing left by an earlier
-    // call is read
+    // the plan rewrites the whole header and both row lists, so nothing left
+    // by an earlier call is read
     const int ps = topk_plan(seq_lens, batch, k, ws, kNoAllocWorkspaceBytes, stream);
     if (ps != TOPK_OK) return ps;
     return topk_transform_ragged(scores, score_stride, row_starts, seq_lens, out_offsets, batch, k, ws,

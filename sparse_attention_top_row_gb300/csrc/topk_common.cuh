@@ -51,7 +51,6 @@ struct Params {
     const int32_t* cluster_rows;
     const int32_t* pt_row_starts;  // packed PAGED: request-local token of each row's position 0, or null
     const int32_t* row_to_batch;   // packed PAGED: each row's page-table row, or null
-    const uint32_t* bounds;        // per-row threshold bounds from the bound kernel (256-thread rows kernel)
 };
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
@@ -108,19 +107,10 @@ cudaError_t launch_rows(bool paged, bool one_per_sm, const Params& p, cudaStream
 cudaError_t launch_cluster(bool paged, int clusters, int all_rows, const Params& p, cudaStream_t stream);
 }  // namespace t512
 
-// The 256-thread build (topk_select256.cu): the rows kernel, four CTAs per SM,
-// whose streamed rows (more than kStreamVecs 16-byte vectors) take their
-// bounds from p.bounds.
+// The 256-thread build (topk_select256.cu): the rows kernel, four CTAs per SM.
 namespace t256 {
-constexpr int kStreamVecs = 4 * 256;
 cudaError_t prepare();
 cudaError_t launch_rows(bool paged, const Params& p, cudaStream_t stream);
 }  // namespace t256
-
-// The bound kernel (topk_bound.cu): one CTA per row writes bounds[b] for the
-// rows of more than min_nv vectors (and seq_len > k).
-namespace bound {
-cudaError_t launch(const Params& p, uint32_t* bounds, int min_nv, cudaStream_t stream);
-}  // namespace bound
 
 }  // namespace topk_impl

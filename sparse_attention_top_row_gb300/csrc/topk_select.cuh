@@ -90,9 +90,6 @@
 #ifndef TOPK_PAGE_CACHE
 #define TOPK_PAGE_CACHE 4096  // page-table entries of a single-CTA row held in shared memory
 #endif
-#ifndef TOPK_PRESAMPLED
-#define TOPK_PRESAMPLED 0  // 1: streamed rows take their bound from Params::bounds (bound kernel)
-#endif
 #ifndef TOPK_COMPACT_LISTS
 #define TOPK_COMPACT_LISTS 1  // 1: streamed rows collect candidates in per-thread compact lists
 #endif
@@ -1069,50 +1066,95 @@ __device__ uint32_t sample_bound(const uint32_t (&skey)[N], uint32_t vmask, uint
     return ((t1.bin << 8) | t2.bin) << 16;
 }
 
-// The sample of a window read from global memory: kSampleVecs 16-byte
-// vectors spread evenly over the aligned window, vector (i * nv) >> 10 for
-// i < 1024 (nv > 1024), kSampleVecs / kThreads of them per thread (i = tid,
-// tid + kThreads, ...). They are loaded before anything else of the row so
-// that they head the memory queue.
-constexpr int kSampleVecs = 1024;
-constexpr int kSamplePerThread = kSampleVecs / kThreads;
-static_assert(kSamplePerThread * kThreads == kSampleVecs, "whole sample vectors per thread");
+// The spread sample of a streamed window: 256 pieces of 4 consecutive
+// 16-byte vectors, each a whole 64-byte-aligned block of memory. With v0 the
+// first vector of the aligned span on such a boundary and nq the whole blocks
+// from there inside the span, piece i is the block v0 + 4 * floor(i * nq /
+// 256), so the pieces cover the whole row; 4 consecutive threads load a piece,
+// one vector each (kSpreadLoads vectors per thread). 4096 elements in all,
+// less the few lanes outside the window.
+constexpr int kSpreadPieces = 256;
+constexpr int kSpreadLoads = kSpreadPieces * 4 / kThreads;
+static_assert(kSpreadLoads * kThreads == 4 * kSpreadPieces && 4 * kSpreadLoads <= 32, "spread sample shape");
+constexpr int kSpreadBins1 = 2048;  // level 1: key bits 31..21
+constexpr int kSpreadBins2 = 256;   // level 2: key bits 20..13 inside the level-1 bin
+static_assert(kWarps * kSmall >= kSpreadBins1, "level 1 fits the per-warp histograms");
 
-__device__ __forceinline__ int sample_vec(int q, int nv) {
-    const uint32_t i = threadIdx.x + static_cast<uint32_t>(q) * kThreads;
-    return static_cast<int>((static_cast<uint64_t>(i) * static_cast<uint32_t>(nv)) >> 10);
-}
-
-struct SampleVecs {
-    int4 v[kSamplePerThread];
+struct SpreadSample {
+    int4 v[kSpreadLoads];
+    uint32_t valid;  // bit 4u + c: lane c of vector u lies in the window
 };
 
-__device__ __forceinline__ SampleVecs sample_load(const float4* vbase, int nv) {
-    SampleVecs s;
+__device__ __forceinline__ int spread_v0(const float4* vbase) {
+    return static_cast<int>((4u - ((static_cast<uint32_t>(reinterpret_cast<uintptr_t>(vbase)) >> 4) & 3u)) & 3u);
+}
+__device__ __forceinline__ int spread_vec(int u, int v0, uint64_t nq) {
+    const uint64_t piece = static_cast<uint64_t>(u * (kThreads / 4) + static_cast<int>(threadIdx.x >> 2));
+    return v0 + 4 * static_cast<int>((piece * nq) >> 8) + static_cast<int>(threadIdx.x & 3u);
+}
+
+// Loads this thread's share of the spread sample (nv > 1024).
+__device__ __forceinline__ SpreadSample spread_load(const float4* vbase, int nv, int rem, int len) {
+    SpreadSample s;
+    const int v0 = spread_v0(vbase);
+    const uint64_t nq = static_cast<uint32_t>(nv - v0) >> 2;  // >= 255
+    s.valid = 0;
 #pragma unroll
-    for (int q = 0; q < kSamplePerThread; ++q) s.v[q] = load_stream_bits(vbase + sample_vec(q, nv));
+    for (int u = 0; u < kSpreadLoads; ++u) {
+        const int j = spread_vec(u, v0, nq);  // < v0 + 4 * nq <= nv
+        s.v[u] = load_stream_bits(vbase + j);
+        const int p0 = 4 * j - rem;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s.valid |= (p0 + c >= 0 && p0 + c < len ? 1u : 0u) << (4 * u + c);
+    }
     return s;
 }
 
-// sample_bound over those vectors: every in-window lane, which is all but the
-// head vector's `rem` leading lanes (the tail vector is never sampled when
-// nv > 1024): 4 * kSampleVecs - rem elements in all.
-__device__ uint32_t sample_bound_vec(const SampleVecs& sv, int nv, int rem, int len, uint32_t k, const Shared& sh) {
-    constexpr int N = 4 * kSamplePerThread;
-    uint32_t skey[N];
-    uint32_t vmask = 0;
+// The elements of the spread sample: every sampled lane but the `rem`
+// before the window (vector 0 is sampled exactly when v0 = 0) and those after
+// it (in vector nv - 1, when sampled).
+__device__ __forceinline__ uint32_t spread_count(const float4* vbase, int nv, int rem, int len) {
+    const int v0 = spread_v0(vbase);
+    const uint64_t nq = static_cast<uint32_t>(nv - v0) >> 2;
+    const int last = v0 + 4 * static_cast<int>((static_cast<uint64_t>(kSpreadPieces - 1) * nq) >> 8) + 3;
+    return static_cast<uint32_t>(16 * kSpreadPieces - (v0 == 0 ? rem : 0) - (last == nv - 1 ? 4 * nv - rem - len : 0));
+}
+
+// The threshold bound from the spread sample (every thread calls): the
+// sample's expected share of the top k plus four standard deviations plus 2,
+// located in a 2048-bin histogram of the top 11 key bits (sh.whist()) and
+// then a 256-bin one of the next 8 (sh.hist()); both zero on entry and on
+// return. Returns a key whose 13 low bits are zero.
+__device__ uint32_t spread_bound(const SpreadSample& s, uint32_t n_s, int len, uint32_t k, const Shared& sh) {
+    uint32_t* h1 = sh.whist();
+    uint32_t* h2 = sh.hist();
 #pragma unroll
-    for (int q = 0; q < kSamplePerThread; ++q) {
-        const int p0 = 4 * sample_vec(q, nv) - rem;
-        const int4 v = sv.v[q];
-        const int32_t e[4] = {v.x, v.y, v.z, v.w};
+    for (int u = 0; u < kSpreadLoads; ++u) {
+        const int32_t e[4] = {s.v[u].x, s.v[u].y, s.v[u].z, s.v[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if ((s.valid >> (4 * u + c)) & 1u) atomicAdd(&h1[bits_key(static_cast<uint32_t>(e[c])) >> 21], 1u);
+    }
+    const float expect = static_cast<float>(k) * static_cast<float>(n_s) / static_cast<float>(len);
+    const float tgt = fminf(ceilf(expect + 4.0f * sqrtf(expect) + 2.0f), static_cast<float>(n_s));
+    const uint32_t target = max(static_cast<uint32_t>(tgt), 1u);
+    __syncthreads();
+    const Threshold t1 = find_threshold(h1, kSpreadBins1, target, sh);
+#pragma unroll
+    for (int u = 0; u < kSpreadLoads; ++u) {
+        const int32_t e[4] = {s.v[u].x, s.v[u].y, s.v[u].z, s.v[u].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            skey[4 * q + c] = bits_key(static_cast<uint32_t>(e[c]));
-            vmask |= (p0 + c >= 0 && p0 + c < len ? 1u : 0u) << (4 * q + c);
+            const uint32_t key = bits_key(static_cast<uint32_t>(e[c]));
+            if (((s.valid >> (4 * u + c)) & 1u) && (key >> 21) == t1.bin) atomicAdd(&h2[(key >> 13) & 255u], 1u);
         }
     }
-    return sample_bound<N>(skey, vmask, static_cast<uint32_t>(4 * kSampleVecs - rem), len, k, sh);
+    __syncthreads();
+    const Threshold t2 = find_threshold(h2, kSpreadBins2, target - t1.above, sh);
+    clear_words(h1, kSpreadBins1);  // (the searches' last barrier is behind every read of the bins)
+    clear_words(h2, kSpreadBins2);
+    __syncthreads();
+    return t1.found && t2.found ? (t1.bin << 21) | (t2.bin << 13) : 0u;
 }
 
 // ----------------------------------------------------------------------------
@@ -1591,44 +1633,57 @@ __device__ __forceinline__ void list_tile(const int4 (&v)[kTileVecs], uint32_t t
     });
 }
 
-// The tile at vector j0 (index base lb = 16 * tile): tiles at the window's
-// edges are masked; a warp with a lane within one tile of its list's end
-// takes the checked appends, every other warp the plain ones.
+// Loads tile j0 (vectors j0 + u * kThreads + t) without bounds checks: for
+// tiles wholly inside the aligned span.
+__device__ __forceinline__ void load_bits_full(int4 (&v)[kTileVecs], const float4* vbase, int j0) {
+    const float4* q = vbase + j0 + static_cast<int>(threadIdx.x);
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) v[u] = load_stream_bits(q + u * kThreads);
+}
+
+// One step of the streamed filter: tile tt (in v) into the lists, then the
+// load of tile tt + 2 into v. Tiles [t_lo, t_hi) lie wholly inside the window
+// (no masks, unchecked loads); a warp with a lane within one tile of its
+// list's end takes the checked appends.
 template <bool kNonNeg>
-__device__ __forceinline__ void list_at(const int4 (&v)[kTileVecs], uint32_t thr, int j0, int je, int rem, int len,
-                                        uint32_t lb, uint32_t& a, uint32_t lim) {
-    if (!tile_interior(j0, je, rem, len))
-        list_tile<kNonNeg, true, true>(v, thr, lb, tile_valid(j0, je, rem, len), a, lim);
-    else if (__any_sync(kFull, a + static_cast<uint32_t>(kTileElems) * kListStride > lim))
-        list_tile<kNonNeg, false, true>(v, thr, lb, 0xFFFFu, a, lim);
-    else
-        list_tile<kNonNeg, false, false>(v, thr, lb, 0xFFFFu, a, lim);
+__device__ __forceinline__ void list_step(int4 (&v)[kTileVecs], int tt, int t_lo, int t_hi, int n_tiles,
+                                          const float4* vbase, int nv, int rem, int len, uint32_t thr,
+                                          uint32_t& a, uint32_t lim) {
+    constexpr int T = kTileVecs * kThreads;
+    const uint32_t lb = static_cast<uint32_t>(tt) * kTileElems;
+    if (tt >= t_lo && tt < t_hi) {
+        if (__any_sync(kFull, a + static_cast<uint32_t>(kTileElems) * kListStride > lim))
+            list_tile<kNonNeg, false, true>(v, thr, lb, 0xFFFFu, a, lim);
+        else
+            list_tile<kNonNeg, false, false>(v, thr, lb, 0xFFFFu, a, lim);
+    } else {
+        list_tile<kNonNeg, true, true>(v, thr, lb, tile_valid(tt * T, nv, rem, len), a, lim);
+    }
+    const int tn = tt + 2;
+    if (tn < t_hi) load_bits_full(v, vbase, tn * T);
+    else if (tn < n_tiles) load_bits(v, vbase, tn * T, nv);
 }
 
 // The streamed window (nv <= kListMaxTiles tiles) into the lists: two register
-// tiles in turn, as stream_filter. a: this thread's list cursor (shared
-// address), lim: its end.
+// tiles in turn (tiles 0 and 1 loaded by the caller), one loading while the
+// other is filtered, the kPrefetchTiles tiles after those on their way into
+// L2. a: this thread's list cursor (shared address), lim: its end.
 template <bool kNonNeg>
 __device__ __forceinline__ void stream_list(int4 (&cur)[kTileVecs], int4 (&nxt)[kTileVecs], const float4* vbase,
                                             int nv, int rem, int len, uint32_t thr, uint32_t& a, uint32_t lim) {
     constexpr int T = kTileVecs * kThreads;
-    int j0 = 0;
-    uint32_t lb = 0;
+    const int n_tiles = (nv + T - 1) / T;
+    const int t_lo = rem == 0 ? 0 : 1;     // tile 0 holds the rem lanes before the window
+    const int t_hi = (len + rem) / (4 * T);  // tiles below it end inside the window
     for (int t = 0;; t += 2) {
         if (threadIdx.x == 0) {
             prefetch_tile_l2(vbase, t + 2 + kPrefetchTiles, nv);
             prefetch_tile_l2(vbase, t + 3 + kPrefetchTiles, nv);
         }
-        list_at<kNonNeg>(cur, thr, j0, nv, rem, len, lb, a, lim);
-        j0 += T;
-        lb += kTileElems;
-        if (j0 >= nv) break;
-        if (j0 + T < nv) load_bits(cur, vbase, j0 + T, nv);
-        list_at<kNonNeg>(nxt, thr, j0, nv, rem, len, lb, a, lim);
-        j0 += T;
-        lb += kTileElems;
-        if (j0 >= nv) break;
-        if (j0 + T < nv) load_bits(nxt, vbase, j0 + T, nv);
+        list_step<kNonNeg>(cur, t, t_lo, t_hi, n_tiles, vbase, nv, rem, len, thr, a, lim);
+        if (t + 1 >= n_tiles) break;
+        list_step<kNonNeg>(nxt, t + 1, t_lo, t_hi, n_tiles, vbase, nv, rem, len, thr, a, lim);
+        if (t + 2 >= n_tiles) break;
     }
 }
 
@@ -1726,32 +1781,34 @@ __device__ __forceinline__ FinishResult finish_list(uint32_t bound_key, uint32_t
         });
     }
     __syncthreads();  // every slot gathered
-    for (uint32_t i = threadIdx.x; i < k; i += kThreads) em.write(i, stage[i]);
+    const bool vec = (k & 3u) == 0u && ((reinterpret_cast<uintptr_t>(em.out) | reinterpret_cast<uintptr_t>(em.out_raw)) & 15u) == 0u;
+    if (vec) {  // 16-byte rows: four slots per store
+        const int4* st4 = reinterpret_cast<const int4*>(stage);
+        for (uint32_t i = threadIdx.x; i < k / 4u; i += kThreads) {
+            const int4 q = st4[i];
+            reinterpret_cast<int4*>(em.out)[i] = make_int4(em.value(q.x), em.value(q.y), em.value(q.z), em.value(q.w));
+            if (em.out_raw) reinterpret_cast<int4*>(em.out_raw)[i] = q;
+        }
+    } else {
+        for (uint32_t i = threadIdx.x; i < k; i += kThreads) em.write(i, stage[i]);
+    }
     return kFinished;
 }
 
-// The bound comes from the row's own sample, or (TOPK_PRESAMPLED) from the
-// bound kernel that ran before this one (Params::bounds; the rows kernel is
-// then free to start streaming at once).
+// Streaming route (nv > kTileVecs * kThreads vectors): the bound comes from
+// the row's spread sample, taken first while the head tiles travel into L2.
 template <bool kPaged, int kLay>
 __device__ void stream_row(const Params& p, int b, const float* w, const float4* vbase, int nv, int rem, int len) {
     const uint32_t k = static_cast<uint32_t>(p.k);
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
-#if TOPK_PRESAMPLED
-    const uint32_t bound_key = p.bounds[b];
+    // the spread sample first, the head tiles on their way into L2 meanwhile
+    const SpreadSample ss = spread_load(vbase, nv, rem, len);  // nv > T >= 1024
+    if (threadIdx.x == 0)
+        for (int t = 0; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
+    const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, len), len, k, layout<kLay>());
     load_bits(cur, vbase, 0, nv);
     load_bits(nxt, vbase, T, nv);
-    if (threadIdx.x == 0)
-        for (int t = 2; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
-#else
-    const SampleVecs sv = sample_load(vbase, nv);  // nv > T >= 1024
-    load_bits(cur, vbase, 0, nv);
-    load_bits(nxt, vbase, T, nv);
-    if (threadIdx.x == 0)
-        for (int t = 2; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
-    const uint32_t bound_key = sample_bound_vec(sv, nv, rem, len, k, layout<kLay>());
-#endif
     const uint32_t thr = pass_threshold(bound_key);
 #if TOPK_COMPACT_LISTS
     if (nv <= kListMaxTiles * T) {
@@ -1982,14 +2039,14 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
         const int je = min(nv, jb + per);
         const int n_chunks = (je - jb + kStageVecs - 1) / kStageVecs;
         const bool det = (p.flags & TOPK_DETERMINISTIC) != 0;
-        const SampleVecs sv = sample_load(vbase, nv);  // the same sample of the whole row in every CTA
+        const SpreadSample ss = spread_load(vbase, nv, rem, r.len);  // the same sample of the whole row in every CTA
         if (threadIdx.x == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the stages come first
             for (int c = 0; c < min(n_chunks, kStages); ++c) issue_chunk(sh, vbase, jb, je, c);
         }
         const int32_t p_lo = max(4 * jb - rem, 0), p_hi = min(4 * je - rem, r.len);
         prefetch_pages<kPaged>(p, r, p_lo, p_hi, kClusterPageCache, sh);
-        const uint32_t bound_key = sample_bound_vec(sv, nv, rem, r.len, k, sh);
+        const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, r.len), r.len, k, sh);
         const uint32_t thr = pass_threshold(bound_key);
         const int warp = static_cast<int>(threadIdx.x >> 5);
         const uint32_t region = saddr(sh.cand) + static_cast<uint32_t>(warp) * (kClusterWarpCap * 8u);

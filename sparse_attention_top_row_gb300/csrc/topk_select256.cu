@@ -10,18 +10,15 @@
 #define TOPK_CTAS_PER_SM 4
 #endif
 #ifndef TOPK_WARP_CAP
-#define TOPK_WARP_CAP 512
+#define TOPK_WARP_CAP 576
 #endif
 #ifndef TOPK_PAGE_CACHE
 #define TOPK_PAGE_CACHE 1024
 #endif
-#define TOPK_PRESAMPLED 1
 #include "topk_select.cuh"
 
 namespace topk_impl {
 namespace t256 {
-
-static_assert(kStreamVecs == kTileVecs * kThreads, "rows streamed by this build are the rows given bounds");
 
 cudaError_t prepare() {
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<true, TOPK_CTAS_PER_SM>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -45,9 +45,9 @@ def test_transform_launches_of_an_empty_batch(lib):
 def test_workspace_bytes(lib):
     assert lib.topk_workspace_bytes(-1) == 0
     assert lib.topk_workspace_bytes(0) == 256
-    assert lib.topk_workspace_bytes(48) == 768          # 64 + 3*4*48 = 640 -> 768
+    assert lib.topk_workspace_bytes(48) == 512          # 64 + 2*4*48 = 448 -> 512
     assert lib.topk_workspace_bytes(16384) % 256 == 0
-    assert lib.topk_workspace_bytes(16384) >= 64 + 12 * 16384
+    assert lib.topk_workspace_bytes(16384) >= 64 + 8 * 16384
 
 
 FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails first

@@ -517,9 +517,9 @@ def test_full_mixed_boundary_single_rows(cuda_lib, bi):
 @pytest.mark.parametrize("name", ["extend", "decode"])
 def test_fast_path_takes_every_row(cuda_lib, name):
     """The sample bounds hold on the benchmark's workloads: no row of a full
-    extend chunk (bound kernel, then the 256-thread rows kernel) or of the
-    decode batch (in-kernel sample) falls back to the exact path, going by the
-    plan header's count of exact-path rows."""
+    extend chunk (256-thread rows kernel, spread sample) or of the decode batch
+    (512-thread rows kernel, register sample) falls back to the exact path,
+    going by the plan header's count of exact-path rows."""
     w = wl.ragged_extend("cuda", chunk=3) if name == "extend" else wl.paged_decode("cuda")
     _, _, ws = cuda_lib.run_workload(w)
     torch.cuda.synchronize()

@@ -1124,8 +1124,11 @@ __device__ __forceinline__ uint32_t spread_count(const float4* vbase, int nv, in
 // sample's expected share of the top k plus four standard deviations plus 2,
 // located in a 2048-bin histogram of the top 11 key bits (sh.whist()) and
 // then a 256-bin one of the next 8 (sh.hist()); both zero on entry and on
-// return. Returns a key whose 13 low bits are zero.
-__device__ uint32_t spread_bound(const SpreadSample& s, uint32_t n_s, int len, uint32_t k, const Shared& sh) {
+// return. Returns a key whose 13 low bits are zero. arrived() runs once this
+// thread's sample is in (so that traffic it starts queues behind the sample).
+template <class Arrived>
+__device__ uint32_t spread_bound(const SpreadSample& s, uint32_t n_s, int len, uint32_t k, const Shared& sh,
+                                 Arrived&& arrived) {
     uint32_t* h1 = sh.whist();
     uint32_t* h2 = sh.hist();
 #pragma unroll
@@ -1135,6 +1138,7 @@ __device__ uint32_t spread_bound(const SpreadSample& s, uint32_t n_s, int len, u
         for (int c = 0; c < 4; ++c)
             if ((s.valid >> (4 * u + c)) & 1u) atomicAdd(&h1[bits_key(static_cast<uint32_t>(e[c])) >> 21], 1u);
     }
+    arrived();
     const float expect = static_cast<float>(k) * static_cast<float>(n_s) / static_cast<float>(len);
     const float tgt = fminf(ceilf(expect + 4.0f * sqrtf(expect) + 2.0f), static_cast<float>(n_s));
     const uint32_t target = max(static_cast<uint32_t>(tgt), 1u);
@@ -1530,7 +1534,15 @@ __device__ __forceinline__ void prefetch_tile_l2(const float4* vbase, int t, int
     const uint32_t bytes = static_cast<uint32_t>(min(T, nv - j)) * 16u;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vbase + j), "r"(bytes) : "memory");
 }
-constexpr int kPrefetchTiles = 4;  // tiles requested ahead of the one being filtered
+// Tiles requested into L2 beyond the two register tiles. 0: each register
+// tile's bytes are asked for by one bulk prefetch a step before its loads
+// (one 16 KB request instead of thousands of 16-byte ones), and no further;
+// deeper prefetching was slower on the 1024-row extend chunk, where about
+// 600 rows stream at once and L2 is no larger than the bytes in flight.
+#ifndef TOPK_PREFETCH_TILES
+#define TOPK_PREFETCH_TILES 0
+#endif
+constexpr int kPrefetchTiles = TOPK_PREFETCH_TILES;
 
 // Streaming route (nv > kTileVecs * kThreads vectors): two register tiles in
 // turn, one loading while the other is filtered, and the kPrefetchTiles
@@ -1802,11 +1814,13 @@ __device__ void stream_row(const Params& p, int b, const float* w, const float4*
     const uint32_t k = static_cast<uint32_t>(p.k);
     constexpr int T = kTileVecs * kThreads;
     int4 cur[kTileVecs], nxt[kTileVecs];
-    // the spread sample first, the head tiles on their way into L2 meanwhile
+    // the spread sample first; once it is in, the head tiles travel into L2
+    // while the bound is searched
     const SpreadSample ss = spread_load(vbase, nv, rem, len);  // nv > T >= 1024
-    if (threadIdx.x == 0)
-        for (int t = 0; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
-    const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, len), len, k, layout<kLay>());
+    const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, len), len, k, layout<kLay>(), [&] {
+        if (threadIdx.x == 0)
+            for (int t = 0; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
+    });
     load_bits(cur, vbase, 0, nv);
     load_bits(nxt, vbase, T, nv);
     const uint32_t thr = pass_threshold(bound_key);
@@ -2046,7 +2060,7 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
         }
         const int32_t p_lo = max(4 * jb - rem, 0), p_hi = min(4 * je - rem, r.len);
         prefetch_pages<kPaged>(p, r, p_lo, p_hi, kClusterPageCache, sh);
-        const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, r.len), r.len, k, sh);
+        const uint32_t bound_key = spread_bound(ss, spread_count(vbase, nv, rem, r.len), r.len, k, sh, [] {});
         const uint32_t thr = pass_threshold(bound_key);
         const int warp = static_cast<int>(threadIdx.x >> 5);
         const uint32_t region = saddr(sh.cand) + static_cast<uint32_t>(warp) * (kClusterWarpCap * 8u);

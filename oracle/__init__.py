@@ -155,6 +155,26 @@ def run_workload(w, rows=None, mutant: int = 0):
     return np.concatenate(outs), np.concatenate(raws), errs
 
 
+def swa_combine(out, out_raw, positions, window_size: int, swa_offsets, width: int, mutant: int = 0):
+    """The SWA combine of the transform's rows (see topk_oracle.cpp): out,
+    out_raw [B, k] int32 (numpy), positions [B], swa_offsets [B] or None;
+    returns [B, width] int32."""
+    lib = _load(mutant)
+    fn = lib.oracle_swa_combine
+    fn.restype = None
+    fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+    out = _i32(out)
+    out_raw = _i32(out_raw)
+    B, k = out.shape
+    assert out_raw.shape == (B, k) and width >= k + window_size and window_size >= 0
+    pos = _i32(positions)
+    offs = None if swa_offsets is None else _i32(swa_offsets)
+    res = np.empty((B, width), dtype=np.int32)
+    fn(B, k, _ptr(out), _ptr(out_raw), _ptr(pos), int(window_size), _ptr(offs), int(width), _ptr(res))
+    return res
+
+
 def host_cores() -> int:
     """Host cores this process may run on."""
     try:

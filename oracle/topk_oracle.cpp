@@ -45,6 +45,19 @@
 //     treated as an empty row (all -1) and counted in the return value (the
 //     PR #35175 page states seq_lens must be non-negative).
 //
+//   * SWA combine (oracle_swa_combine; the PR #30255 page, "sparse_prefill_
+//     utils.py": _combine_topk_swa_indices_kernel and combine_topk_swa_indices
+//     merge the top-k indices with the sliding-window indices, topk_len =
+//     min((pos + 1) // COMPRESS_RATIO, top_k); the page elides the kernel's
+//     body, so this is the plainest reading of its signature): row b of width
+//     `width` holds the row's selected entries (as the transform emitted them,
+//     topk_len of them: with seq_len = (pos + 1) // COMPRESS_RATIO that is the
+//     page's min((pos + 1) // COMPRESS_RATIO, top_k)), then the window's
+//     tokens pos - w + 1 .. pos in ascending order, w = min(WINDOW_SIZE,
+//     pos + 1) (none for pos < 0), each plus swa_offsets[b] (0 when null),
+//     then -1 up to the width (the page's PADDED_TOP_K, at least top_k +
+//     WINDOW_SIZE).
+//
 // Parity pins (tests/test_oracle_pins.py): brute-force rank counting on tiny
 // rows, an exhaustive sweep over short vectors with ties and signed zeros,
 // invariants on every workload shape, numpy's partition on the tie-free
@@ -188,6 +201,37 @@ int64_t oracle_topk_transform(int32_t mode, const float* scores, int64_t score_s
     return oracle_topk_transform_packed(mode, scores, score_stride, row_starts, seq_lens, out_offsets,
                                         page_table, page_table_stride, page_size, nullptr, nullptr, batch, k,
                                         out, out_raw);
+}
+
+// SWA combine (see the header): out / out_raw are the transform's [batch, k]
+// rows (out_raw's -1 padding marks where the selected entries end),
+// positions[b] the row's query position, result [batch, width].
+void oracle_swa_combine(int32_t batch, int32_t k, const int32_t* out, const int32_t* out_raw,
+                        const int32_t* positions, int32_t window_size, const int32_t* swa_offsets,
+                        int32_t width, int32_t* result) {
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t* o = out + (int64_t)b * k;
+        const int32_t* r = out_raw + (int64_t)b * k;
+        int32_t* res = result + (int64_t)b * width;
+        int32_t n = 0;
+        while (n < k && r[n] >= 0) ++n;  // the selected entries lead the row
+        int32_t t = 0;
+        for (int32_t i = 0; i < n; ++i) res[t++] = o[i];
+#if ORACLE_MUTANT == 9
+        for (int32_t i = 0; i < n; ++i) res[i] = r[i];  // mutant: untransformed positions
+#endif
+        const int32_t pos = positions[b];
+        const int32_t w = pos < 0 ? 0 : std::min(window_size, pos + 1);
+        const int32_t off = swa_offsets ? swa_offsets[b] : 0;
+        for (int32_t i = 0; i < w; ++i) {
+#if ORACLE_MUTANT == 8
+            res[t++] = pos - w + i + off;  // mutant: the window ends one token early
+#else
+            res[t++] = pos - w + 1 + i + off;
+#endif
+        }
+        while (t < width) res[t++] = -1;
+    }
 }
 
 }  // extern "C"

@@ -127,6 +127,38 @@ def ragged_extend(device="cpu", chunk=0, rows_per_chunk=1024, n_req=4, prefix=28
                 page_table_stride=0, page_size=1, batch=rows_per_chunk)
 
 
+def ragged_swa(device="cpu", sub_id=0, n_req=2, prefix=28672, new=512, ratio=4, window=128, k=512):
+    """Compressed-KV top-k rows with the sliding-window combine (the PR #30255
+    page's SWA combine; the reading is the library's topk_transform_ragged_swa).
+
+    Query i of request r sits at raw token position pos = prefix + i; its
+    compressed window holds L = (pos + 1) // ratio entries starting at
+    row_start = r * C in a compressed row space of C = (prefix + new) // ratio
+    columns per request; out_offsets = row_start, and the window tokens map
+    through swa_offsets = r * (prefix + new) (the raw token space). Scores are
+    N(0,1) inside the windows and the 1e3 sentinel elsewhere. The combined
+    rows are k + window wide.
+    """
+    g = _gen(device, seed_for(8, sub_id))
+    per_req = (prefix + new) // ratio
+    stride = n_req * per_req
+    rows = torch.arange(n_req * new, device=device)
+    req = rows // new
+    pos = prefix + rows % new
+    seq_lens = (pos + 1) // ratio
+    starts = req * per_req
+    cols = torch.arange(stride, device=device)
+    inside = (cols[None, :] >= starts[:, None]) & (cols[None, :] < (starts + seq_lens)[:, None])
+    vals = torch.randn(n_req * new, stride, generator=g, device=device)
+    scores = torch.where(inside, vals, torch.full_like(vals, SENTINEL))
+    del vals, inside
+    return dict(name=f"ragged swa req={n_req} prefix={prefix} new={new} ratio={ratio} window={window} k={k}",
+                mode="ragged", k=k, scores=scores, score_stride=stride, row_starts=_i32(starts),
+                seq_lens=_i32(seq_lens), out_offsets=_i32(starts), page_table=None, page_table_stride=0,
+                page_size=1, batch=n_req * new, positions=_i32(pos), window_size=window,
+                swa_offsets=_i32(req * (prefix + new)), out_width=k + window)
+
+
 def paged_long(device="cpu", sub_id=0, batch=1, seq_len=131072, k=2048, page_size=64, scale=0.1):
     """Few long PAGED rows whose scores are 0.1*N(0,1) rounded to
     bf16-representable values (heavy exact ties near the threshold)."""

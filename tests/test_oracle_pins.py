@@ -194,6 +194,56 @@ PINS = [pin_golden, pin_bruteforce, pin_exhaustive, pin_partition, pin_paged_exp
         pin_invariants]
 
 
+SWA_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "swa_examples.json")
+
+
+def pin_swa_golden(mutant=0):
+    """The SWA combine's hand-built examples (tests/golden/swa_examples.json)."""
+    with open(SWA_GOLDEN) as f:
+        g = json.load(f)
+    w = wl.custom("ragged", g["k"], g["rows"], out_offsets=g["out_offsets"])
+    w["seq_lens"] = torch.tensor(g["seq_lens"], dtype=torch.int32)
+    out, raw, _ = oracle.run_workload(w, mutant=mutant)
+    res = oracle.swa_combine(out, raw, g["positions"], g["window_size"], g["swa_offsets"], g["width"],
+                             mutant=mutant)
+    for case in g["cases"]:
+        row = res[case["row"]]
+        n = len(case["topk_sorted"])
+        assert sorted(row[:n].tolist()) == case["topk_sorted"], case["why"]
+        assert row[n:].tolist() == case["tail"], case["why"]
+
+
+def pin_swa_formula(mutant=0, seed=11):
+    """On compressed rows of L = (pos + 1) // ratio entries, the combined row
+    carries min((pos + 1) // ratio, k) selected entries (the page's topk_len),
+    exactly the row's top-k selection; its window part is the set of tokens t
+    with 0 <= t <= pos and pos - t < window (a brute-force filter of 0..pos),
+    plus the row's SWA offset, in ascending order; the rest is -1."""
+    rng = np.random.default_rng(seed)
+    for ratio, window, k in ((4, 8, 5), (1, 3, 16), (128, 16, 2)):
+        B = 12
+        pos = rng.integers(-1, 300, B).astype(np.int32)
+        lens = np.where(pos >= 0, (pos + 1) // ratio, 0).astype(np.int32)
+        stride = int(lens.max()) + 1
+        rows = [rng.standard_normal(stride).astype(np.float32).tolist() for _ in range(B)]
+        offs = rng.integers(0, 1000, B).astype(np.int32)
+        swa = rng.integers(0, 100000, B).astype(np.int32)
+        w = wl.custom("ragged", k, rows, out_offsets=offs.tolist())
+        w["seq_lens"] = torch.from_numpy(lens)
+        out, raw, _ = oracle.run_workload(w, mutant=mutant)
+        width = k + window + 3
+        res = oracle.swa_combine(out, raw, pos, window, swa, width, mutant=mutant)
+        for b in range(B):
+            topk_len = min(int(pos[b] + 1) // ratio, k) if pos[b] >= 0 else 0
+            assert sorted(res[b, :topk_len].tolist()) == sorted(out[b, :topk_len].tolist())
+            win = [t + int(swa[b]) for t in range(0, int(pos[b]) + 1) if int(pos[b]) - t < window]
+            assert res[b, topk_len:topk_len + len(win)].tolist() == win
+            assert (res[b, topk_len + len(win):] == -1).all()
+
+
+PINS += [pin_swa_golden, pin_swa_formula]
+
+
 # ------------------------------------------------------------------ tests
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -214,7 +264,7 @@ def test_error_rows_are_empty_and_counted():
 
 def test_planted_mistakes_are_caught():
     """Each planted mistake in the oracle fails at least one pin family."""
-    for mutant in range(1, 8):
+    for mutant in range(1, 10):
         caught = []
         for pin in PINS:
             try:

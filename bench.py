@@ -188,7 +188,7 @@ DESCRIPTIONS = {
              "L log-uniform in [256, 131072] plus boundary rows (24 launches)",
 }
 EXTRA = ("ragged_tiny", "paged_decode", "paged_long_b1", "paged_long_b30", "paged_long_b31", "paged_packed",
-         "mixed")
+         "mixed", "ragged_swa")
 
 
 def make_workload(name, device, rank=0):
@@ -199,6 +199,8 @@ def make_workload(name, device, rank=0):
         return [wl.ragged_tiny(device, sub_id=rank)]
     if name == "ragged_extend":
         return [wl.ragged_extend(device, chunk=c, sub_id=c + 16 * rank) for c in range(16)]
+    if name == "ragged_swa":  # compressed-KV top-k fused with the sliding-window combine
+        return [wl.ragged_swa(device, sub_id=rank, n_req=4, new=1024, prefix=28672, ratio=4, window=128, k=512)]
     if name == "ragged_extend_chunk":  # one 1024-row chunk (profiling size)
         return [wl.ragged_extend(device, chunk=0)]
     if name == "paged_packed":  # packed PAGED extend rows: 8 requests x 16 queries, sliding window 16384
@@ -231,8 +233,11 @@ def algorithmic_bytes(w, out_raw):
     lens = w["seq_lens"].to(torch.int64).clamp(min=0)
     nontrivial = lens > k
     scores = int((4 * lens[nontrivial]).sum().item())
-    out = 4 * k * int(w["batch"])
+    swa = w.get("positions") is not None  # the fused SWA combine writes rows of out_width
+    out = 4 * (int(w["out_width"]) if swa else k) * int(w["batch"])
     packed = [w.get(key) for key in ("page_table_row_starts", "row_to_batch")]
+    if swa:
+        packed += [w["positions"], w.get("swa_offsets")]
     meta = 4 * int(w["batch"]) * (1 + (w.get("row_starts") is not None) + (w["mode"] == "ragged") +
                                   sum(a is not None for a in packed))
     pages = 0
@@ -264,7 +269,9 @@ class Launch:
     def __init__(self, w, flags=0):
         self.w = w
         self.B, self.k = int(w["batch"]), int(w["k"])
-        self.out = torch.empty((self.B, self.k), dtype=torch.int32, device=w["scores"].device)
+        self.swa = w.get("positions") is not None  # the fused SWA combine: rows of out_width
+        width = int(w["out_width"]) if self.swa else self.k
+        self.out = torch.empty((self.B, width), dtype=torch.int32, device=w["scores"].device)
         self.ws = topk.new_workspace(self.B, w["scores"].device)
         self.flags = flags
 
@@ -282,6 +289,11 @@ class Launch:
             topk.topk_transform_paged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                                       w["page_table"], w["page_table_stride"], w["page_size"], self.k,
                                       self.ws, self.out, out_raw, self.flags, stream=stream)
+        elif self.swa:
+            topk.topk_transform_ragged_swa(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                                           w["out_offsets"], self.k, self.ws, w["positions"], w["window_size"],
+                                           w.get("swa_offsets"), w["out_width"], self.out, out_raw, self.flags,
+                                           stream=stream)
         else:
             topk.topk_transform_ragged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                                        w["out_offsets"], self.k, self.ws, self.out, out_raw, self.flags,

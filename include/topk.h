@@ -204,6 +204,47 @@ TOPK_API int topk_transform_ragged(const float* scores, int64_t score_stride,
                                    int32_t* out_raw, uint32_t flags, topk_stream_t stream);
 
 /*
+ * RAGGED top-k + offset transform fused with the SWA combine: each output row
+ * is the row's top-k entries followed by its sliding-window tokens.
+ * Counterpart of combine_topk_swa_indices / _combine_topk_swa_indices_kernel
+ * (PR #30255 page, "sparse_prefill_utils.py"), which merges the top-k indices
+ * with the sliding-window indices, topk_len = min((pos + 1) // COMPRESS_RATIO,
+ * top_k), padded to PADDED_TOP_K; the page elides the body and the layout, and
+ * this is the plainest reading of the signature. Fusing it saves the
+ * combine's read of a [batch, k] index array.
+ *
+ *   scores ... flags   as for topk_transform_ragged; row b's window holds its
+ *                      seq_lens[b] compressed entries (a causal query at
+ *                      position pos over compressed KV has (pos + 1) //
+ *                      COMPRESS_RATIO of them, which makes min(k, seq_len) the
+ *                      page's topk_len).
+ *   positions          int32 [batch], device: the query position pos of each
+ *                      row (negative: no window tokens).
+ *   window_size        tokens in the sliding window, 0 .. TOPK_MAX_SWA_WINDOW.
+ *   swa_offsets        int32 [batch] or NULL: added to each window token (the
+ *                      caller's map into its window KV space; NULL: 0).
+ *   out_width          elements per output row (PADDED_TOP_K), at least
+ *                      k + window_size.
+ *   out                int32 [batch, out_width], row-major, every slot
+ *                      written: slots [0, min(k, seq_len)) the selected
+ *                      entries (position + out_offsets[b]; slot order
+ *                      unspecified), then the window tokens pos - w + 1 .. pos
+ *                      (w = min(window_size, pos + 1)) plus swa_offsets[b] in
+ *                      ascending order, then -1.
+ *   out_raw            int32 [batch, k] or NULL: as for topk_transform_ragged
+ *                      (k columns, not out_width).
+ * Status codes as for topk_transform_ragged; TOPK_ERR_ARG also for a null
+ * positions array, a window outside its range or out_width < k + window_size.
+ */
+#define TOPK_MAX_SWA_WINDOW (1 << 20)
+TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                                       const int32_t* seq_lens, const int32_t* out_offsets, int32_t batch,
+                                       int32_t k, void* workspace, size_t workspace_bytes,
+                                       const int32_t* positions, int32_t window_size,
+                                       const int32_t* swa_offsets, int32_t out_width, int32_t* out,
+                                       int32_t* out_raw, uint32_t flags, topk_stream_t stream);
+
+/*
  * Reads the workspace's device error count (rows with seq_len < 0 seen by the
  * plan, plus rows with row_start < 0, or for packed PAGED rows
  * page_table_row_start < 0, seen by each transform since the plan) and the

@@ -32,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
 
 EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_paged_packed",
             "topk_transform_ragged", "topk_read_device_errors", "topk_status_string",
-            "topk_transform_ragged_noalloc", "topk_transform_launches")
+            "topk_transform_ragged_noalloc", "topk_transform_launches", "topk_transform_ragged_swa")
 TOPK_NOALLOC_MAX_BATCH = 16384
 
 
@@ -75,6 +75,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.topk_read_device_errors.argtypes = [c_p, ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_p]
         lib.topk_transform_ragged_noalloc.restype = ctypes.c_int
         lib.topk_transform_ragged_noalloc.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_p, c_p, c_u32, c_p]
+        lib.topk_transform_ragged_swa.restype = ctypes.c_int
+        lib.topk_transform_ragged_swa.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_p, c_sz,
+                                                  c_p, c_i32, c_p, c_i32, c_p, c_p, c_u32, c_p]
         lib.topk_transform_launches.restype = ctypes.c_int
         lib.topk_transform_launches.argtypes = [c_i32]
         lib.topk_status_string.restype = ctypes.c_char_p
@@ -255,6 +258,26 @@ def topk_transform_ragged(scores, score_stride: int, row_starts, seq_lens, out_o
     _check("topk_transform_ragged", lib.topk_transform_ragged(*args, st))
 
 
+def topk_transform_ragged_swa(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int, workspace,
+                              positions, window_size: int, swa_offsets, out_width: int, out, out_raw=None,
+                              flags: int = 0, stream=None):
+    """RAGGED top-k fused with the SWA combine: out is [batch, out_width]
+    (see include/topk.h)."""
+    import torch
+    lib = load()
+    st, dev = _stream(stream)
+    batch = _rows(seq_lens, dev)
+    i32 = torch.int32
+    args = (_arg(scores, "scores", torch.float32, _strided_numel(batch, score_stride), dense=False, device=dev),
+            int(score_stride), _arg(row_starts, "row_starts", i32, batch, required=False, device=dev),
+            _ptr(seq_lens), _arg(out_offsets, "out_offsets", i32, batch, device=dev), batch, int(k),
+            *_ws(workspace, dev), _arg(positions, "positions", i32, batch, device=dev), int(window_size),
+            _arg(swa_offsets, "swa_offsets", i32, batch, required=False, device=dev), int(out_width),
+            _arg(out, "out", i32, batch * int(out_width), device=dev),
+            _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
+    _check("topk_transform_ragged_swa", lib.topk_transform_ragged_swa(*args, st))
+
+
 def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_lens, out_offsets, k: int, out,
                                   out_raw=None, flags: int = 0, stream=None):
     """Plan + RAGGED transform without a caller workspace (the library's
@@ -290,8 +313,9 @@ def run_workload(w, out=None, out_raw=None, workspace=None, flags: int = 0, plan
     import torch
     dev = w["scores"].device
     B, k = int(w["batch"]), int(w["k"])
+    swa = w.get("positions") is not None
     if out is None:
-        out = torch.empty((B, k), dtype=torch.int32, device=dev)
+        out = torch.empty((B, int(w["out_width"]) if swa else k), dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = new_workspace(B, dev)
     if plan:
@@ -305,6 +329,10 @@ def run_workload(w, out=None, out_raw=None, workspace=None, flags: int = 0, plan
         topk_transform_paged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                              w["page_table"], w["page_table_stride"], w["page_size"], k, workspace,
                              out, out_raw, flags, stream=stream)
+    elif swa:
+        topk_transform_ragged_swa(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
+                                  w["out_offsets"], k, workspace, w["positions"], w["window_size"],
+                                  w.get("swa_offsets"), w["out_width"], out, out_raw, flags, stream=stream)
     else:
         topk_transform_ragged(w["scores"], w["score_stride"], w.get("row_starts"), w["seq_lens"],
                               w["out_offsets"], k, workspace, out, out_raw, flags, stream=stream)

@@ -220,6 +220,7 @@ Params make_params(const float* scores, int64_t score_stride, const int32_t* row
     p.flags = flags;
     p.out = out;
     p.out_raw = out_raw;
+    p.out_stride = k;
     p.hdr = static_cast<PlanHeader*>(workspace);
     p.order = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + sizeof(PlanHeader));
     p.cluster_rows = p.order + batch;
@@ -291,6 +292,26 @@ int topk_transform_ragged(const float* scores, int64_t score_stride, const int32
     if (batch == 0) return TOPK_OK;
     Params p = make_params(scores, score_stride, row_starts, seq_lens, batch, k, workspace, out, out_raw, flags);
     p.out_offsets = out_offsets;
+    return launch_transform<false>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topk_transform_ragged_swa(const float* scores, int64_t score_stride, const int32_t* row_starts,
+                              const int32_t* seq_lens, const int32_t* out_offsets, int32_t batch, int32_t k,
+                              void* workspace, size_t workspace_bytes, const int32_t* positions,
+                              int32_t window_size, const int32_t* swa_offsets, int32_t out_width, int32_t* out,
+                              int32_t* out_raw, uint32_t flags, topk_stream_t stream) {
+    const int st = common_checks(scores, score_stride, seq_lens, batch, k, workspace, workspace_bytes, out, flags);
+    if (st != TOPK_OK) return st;
+    if (window_size < 0 || window_size > TOPK_MAX_SWA_WINDOW) return TOPK_ERR_ARG;
+    if (static_cast<int64_t>(out_width) < static_cast<int64_t>(k) + window_size) return TOPK_ERR_ARG;
+    if (batch > 0 && (out_offsets == nullptr || positions == nullptr)) return TOPK_ERR_ARG;
+    if (batch == 0) return TOPK_OK;
+    Params p = make_params(scores, score_stride, row_starts, seq_lens, batch, k, workspace, out, out_raw, flags);
+    p.out_offsets = out_offsets;
+    p.out_stride = out_width;
+    p.positions = positions;
+    p.swa_window = window_size;
+    p.swa_offsets = swa_offsets;
     return launch_transform<false>(p, reinterpret_cast<cudaStream_t>(stream));
 }
 

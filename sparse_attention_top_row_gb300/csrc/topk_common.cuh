@@ -51,6 +51,10 @@ struct Params {
     const int32_t* cluster_rows;
     const int32_t* pt_row_starts;  // packed PAGED: request-local token of each row's position 0, or null
     const int32_t* row_to_batch;   // packed PAGED: each row's page-table row, or null
+    int32_t out_stride;            // elements between output rows (k, or the SWA combine's width)
+    const int32_t* positions;      // SWA combine: each row's query position, or null (no combine)
+    int32_t swa_window;            // SWA combine: the window's size in tokens
+    const int32_t* swa_offsets;    // SWA combine: each row's window offset, or null (0)
 };
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }

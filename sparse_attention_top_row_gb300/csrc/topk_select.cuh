@@ -776,15 +776,31 @@ __device__ void emit_selected(const SelState& st, uint32_t k, const Src& src, co
 }
 
 template <bool kPaged>
-__device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em) {
+__device__ void trivial_row(int32_t len, uint32_t k, const Emitter<kPaged>& em, bool pad_out = true) {
     for (uint32_t t = threadIdx.x; t < k; t += kThreads) {
         if (static_cast<int32_t>(t) < len) {
             em.write(t, static_cast<int32_t>(t));
         } else {
-            em.out[t] = -1;
+            if (pad_out) em.out[t] = -1;  // (the SWA combine's tail fills these slots instead)
             if (em.out_raw) em.out_raw[t] = -1;
         }
     }
+}
+
+// The SWA combine's tail of row b (p.positions set): slots [topk_len, width)
+// of the output row, topk_len = min(k, len) the row's selected entries, hold
+// the window's tokens pos - w + 1 .. pos plus the row's SWA offset, w =
+// min(window, pos + 1) (none for pos < 0), then -1 (the PR #30255 page's
+// combine_topk_swa_indices, topk_len = min((pos + 1) // COMPRESS_RATIO,
+// top_k), in the reading of the library's header). All threads of the CTA.
+__device__ __forceinline__ void swa_tail(const Params& p, int b, int32_t len) {
+    const int32_t topk_len = min(max(len, 0), p.k);
+    const int32_t pos = p.positions[b];
+    const int32_t w = pos < 0 ? 0 : min(p.swa_window, pos + 1);
+    const int32_t first = pos - w + 1 + (p.swa_offsets ? p.swa_offsets[b] : 0);
+    int32_t* row = p.out + static_cast<int64_t>(b) * p.out_stride + topk_len;
+    for (int32_t i = static_cast<int32_t>(threadIdx.x); i < p.out_stride - topk_len; i += kThreads)
+        row[i] = i < w ? first + i : -1;
 }
 
 // Ranks the threshold bin's members, n <= kThreads of them in tkey/tpos
@@ -1427,7 +1443,7 @@ __device__ __forceinline__ void prefetch_pages(const Params& p, const RowInfo& r
 template <bool kPaged>
 __device__ __forceinline__ Emitter<kPaged> make_emitter(const Params& p, int b, const RowInfo& r) {
     Emitter<kPaged> em;
-    em.out = p.out + static_cast<int64_t>(b) * p.k;
+    em.out = p.out + static_cast<int64_t>(b) * p.out_stride;
     em.out_raw = p.out_raw ? p.out_raw + static_cast<int64_t>(b) * p.k : nullptr;
     em.pt_row = kPaged ? p.page_table + static_cast<int64_t>(r.table_row) * p.page_table_stride : nullptr;
     em.pt_cached = nullptr;
@@ -1889,9 +1905,10 @@ __device__ __forceinline__ void check_row(RowInfo& r, bool planned, bool counter
 // counters and histograms must be zero.
 template <bool kPaged, int kLay>
 __device__ void solo_row(const Params& p, int b, const RowInfo& r) {
+    if (p.positions) swa_tail(p, b, r.len);
     const uint32_t k = static_cast<uint32_t>(p.k);
     if (r.len <= p.k) {
-        trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r));
+        trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r), p.positions == nullptr);
         return;
     }
     prefetch_pages<kPaged>(p, r, 0, r.len, kPageCache, layout<kLay>());
@@ -2041,8 +2058,9 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
     const uint32_t k = static_cast<uint32_t>(p.k);
     RowInfo r = row_info(p, b, kPaged);
     check_row(r, true, rank == 0 && threadIdx.x == 0, p);
+    if (p.positions && rank == 0) swa_tail(p, b, r.len);
     if (r.len <= p.k) {  // only a data error (an emptied row) makes a cluster row this short
-        if (rank == 0) trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r));
+        if (rank == 0) trivial_row<kPaged>(r.len, k, make_emitter<kPaged>(p, b, r), p.positions == nullptr);
     } else {
         const int rem = r.start & 3;
         const float* w = p.scores + static_cast<int64_t>(b) * p.score_stride + r.start;

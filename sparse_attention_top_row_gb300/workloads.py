@@ -133,14 +133,14 @@ def ragged_swa(device="cpu", sub_id=0, n_req=2, prefix=28672, new=512, ratio=4, 
 
     Query i of request r sits at raw token position pos = prefix + i; its
     compressed window holds L = (pos + 1) // ratio entries starting at
-    row_start = r * C in a compressed row space of C = (prefix + new) // ratio
-    columns per request; out_offsets = row_start, and the window tokens map
+    row_start = r * C in a compressed row space of C columns per request (the
+    longest window rounded up past a multiple of 4); out_offsets = row_start, and the window tokens map
     through swa_offsets = r * (prefix + new) (the raw token space). Scores are
     N(0,1) inside the windows and the 1e3 sentinel elsewhere. The combined
     rows are k + window wide.
     """
     g = _gen(device, seed_for(8, sub_id))
-    per_req = (prefix + new) // ratio
+    per_req = ((prefix + new) // ratio + 4) // 4 * 4  # > the longest window, a multiple of 4
     stride = n_req * per_req
     rows = torch.arange(n_req * new, device=device)
     req = rows // new

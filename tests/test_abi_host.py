@@ -106,6 +106,24 @@ def test_transform_validation(lib):
     assert paged(None, 0, None, None, None, 0, 1, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, None, 0, None) == 0
 
 
+def test_swa_transform_validation(lib):
+    ws = lib.topk_workspace_bytes(8)
+    swa = lib.topk_transform_ragged_swa
+    # scores, stride, row_starts, seq_lens, out_offsets, batch, k, ws, ws_bytes, positions, window,
+    # swa_offsets, out_width, out, out_raw, flags, stream
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, None, 4, None, 20, FAKE, None, 0, None) == 1  # no positions
+    assert swa(FAKE, 0, None, FAKE, None, 8, 16, FAKE, ws, FAKE, 4, None, 20, FAKE, None, 0, None) == 1  # no offsets
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, -1, None, 20, FAKE, None, 0, None) == 1
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, (1 << 20) + 1, None, 1 << 21, FAKE, None, 0,
+               None) == 1
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, 4, None, 19, FAKE, None, 0, None) == 1  # too narrow
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 0, FAKE, ws, FAKE, 4, None, 20, FAKE, None, 0, None) == 3
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws - 1, FAKE, 4, None, 20, FAKE, None, 0, None) == 5
+    assert swa(FAKE, 0, None, FAKE, FAKE, 8, 16, FAKE, ws, FAKE, 4, None, 20, FAKE, None, 2, None) == 1
+    assert swa(None, 0, None, None, None, 0, 16, FAKE, lib.topk_workspace_bytes(0), None, 4, None, 20, None, None,
+               0, None) == 0
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert lib.topk_status_string(s)

@@ -525,3 +525,56 @@ def test_fast_path_takes_every_row(cuda_lib, name):
     torch.cuda.synchronize()
     hdr = ws[:64].cpu().numpy().view(np.uint32)
     assert hdr[7] == 0, f"{hdr[7]} rows took the exact path"
+
+
+# ---------------------------------------------------------------- the fused SWA combine
+
+def _check_swa(topk, w, flags_list=(DET, 0)):
+    """topk_transform_ragged_swa against the oracle's transform + combine: the
+    window tail of every row bit-exact, the top-k part as the plain transform
+    is checked (sets in deterministic mode, score multisets otherwise)."""
+    assert_windows_in_bounds(w)
+    hw = HostWorkload(w)
+    ref_out, ref_raw, ref_err = oracle.run_workload(w)
+    width, k, B = int(w["out_width"]), int(w["k"]), int(w["batch"])
+    offs = None if w.get("swa_offsets") is None else w["swa_offsets"].cpu().numpy()
+    ref = oracle.swa_combine(ref_out, ref_raw, w["positions"].cpu().numpy(), int(w["window_size"]), offs, width)
+    topk_len = np.array([min(hw.length(b), k) for b in range(B)])
+    d = wl.to_device(w, "cuda")
+    for flags in flags_list:
+        out = torch.full((B, width), CANARY, dtype=torch.int32, device="cuda")
+        raw = torch.full((B, k), CANARY, dtype=torch.int32, device="cuda")
+        _, _, ws = topk.run_workload(d, out=out, out_raw=raw, flags=flags)
+        torch.cuda.synchronize()
+        o, r = out.cpu().numpy(), raw.cpu().numpy()
+        assert not np.any(o == CANARY) and not np.any(r == CANARY)
+        gpu_topk = np.full((B, k), -1, dtype=np.int32)
+        for b in range(B):
+            n = int(topk_len[b])
+            assert o[b, n:].tolist() == ref[b, n:].tolist(), f"row {b}: window tail"
+            gpu_topk[b, :n] = o[b, :n]
+        compare_with_oracle(hw, gpu_topk, r, ref_out, ref_raw, deterministic=bool(flags & DET))
+        assert topk.topk_read_device_errors(ws) == (ref_err, 0)
+
+
+@pytest.mark.parametrize("route,kw", [
+    ("register_512", dict(n_req=2, new=48)),                      # 96 rows, L ~ 7168: 512-thread register route
+    ("streaming_256", dict(n_req=2, new=100)),                    # 200 rows (> SMs): 256-thread streaming route
+    ("cluster", dict(n_req=2, new=6, prefix=40000, ratio=1)),     # 12 rows of L ~ 40001: cluster route
+    ("trivial", dict(n_req=1, new=300, prefix=0, ratio=128)),     # L <= 2 <= k, windows cut at token 0
+    ("k2048", dict(n_req=3, new=70, k=2048, window=64)),          # 210 rows, k = 2048
+])
+def test_swa_combine_routes(cuda_lib, route, kw):
+    _check_swa(cuda_lib, wl.ragged_swa("cpu", sub_id=len(route), **kw))
+
+
+def test_swa_combine_edge_rows(cuda_lib):
+    """Negative positions (no window), a data-error row, a window wider than
+    the prefix, no SWA offsets, and an output wider than k + window."""
+    rng = np.random.default_rng(5)
+    rows = [rng.standard_normal(n).astype(np.float32).tolist() for n in (600, 3, 1, 40, 9000)]
+    w = wl.custom("ragged", 32, rows, out_offsets=[7, 0, 5, 1000, 3])
+    w["seq_lens"] = torch.tensor([600, 3, -1, 40, 9000], dtype=torch.int32)
+    w.update(positions=torch.tensor([-1, 2, 10, 5000, 0], dtype=torch.int32), window_size=16,
+             swa_offsets=None, out_width=52)
+    _check_swa(cuda_lib, w)

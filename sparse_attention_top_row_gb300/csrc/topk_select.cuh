@@ -1082,14 +1082,20 @@ __device__ uint32_t sample_bound(const uint32_t (&skey)[N], uint32_t vmask, uint
     return ((t1.bin << 8) | t2.bin) << 16;
 }
 
-// The spread sample of a streamed window: 256 pieces of 4 consecutive
+// The spread sample of a streamed window: 128 pieces of 4 consecutive
 // 16-byte vectors, each a whole 64-byte-aligned block of memory. With v0 the
 // first vector of the aligned span on such a boundary and nq the whole blocks
 // from there inside the span, piece i is the block v0 + 4 * floor(i * nq /
-// 256), so the pieces cover the whole row; 4 consecutive threads load a piece,
-// one vector each (kSpreadLoads vectors per thread). 4096 elements in all,
-// less the few lanes outside the window.
-constexpr int kSpreadPieces = 256;
+// 128), so the pieces cover the whole row; 4 consecutive threads load a piece,
+// one vector each (kSpreadLoads vectors per thread). 2048 elements in all,
+// less the few lanes outside the window. (Twice the sample gives a bound
+// nearer the threshold, 25 instead of 36 % above k on the extend rows, but
+// costs more than the smaller finish saves.)
+#ifndef TOPK_SPREAD_LOG_PIECES
+#define TOPK_SPREAD_LOG_PIECES 7
+#endif
+constexpr int kSpreadLogPieces = TOPK_SPREAD_LOG_PIECES;
+constexpr int kSpreadPieces = 1 << kSpreadLogPieces;
 constexpr int kSpreadLoads = kSpreadPieces * 4 / kThreads;
 static_assert(kSpreadLoads * kThreads == 4 * kSpreadPieces && 4 * kSpreadLoads <= 32, "spread sample shape");
 constexpr int kSpreadBins1 = 2048;  // level 1: key bits 31..21
@@ -1106,7 +1112,7 @@ __device__ __forceinline__ int spread_v0(const float4* vbase) {
 }
 __device__ __forceinline__ int spread_vec(int u, int v0, uint64_t nq) {
     const uint64_t piece = static_cast<uint64_t>(u * (kThreads / 4) + static_cast<int>(threadIdx.x >> 2));
-    return v0 + 4 * static_cast<int>((piece * nq) >> 8) + static_cast<int>(threadIdx.x & 3u);
+    return v0 + 4 * static_cast<int>((piece * nq) >> kSpreadLogPieces) + static_cast<int>(threadIdx.x & 3u);
 }
 
 // Loads this thread's share of the spread sample (nv > 1024).
@@ -1114,14 +1120,17 @@ __device__ __forceinline__ SpreadSample spread_load(const float4* vbase, int nv,
     SpreadSample s;
     const int v0 = spread_v0(vbase);
     const uint64_t nq = static_cast<uint32_t>(nv - v0) >> 2;  // >= 255
-    s.valid = 0;
+    s.valid = 0xFFFFFFFFu >> (32 - 4 * kSpreadLoads);
 #pragma unroll
     for (int u = 0; u < kSpreadLoads; ++u) {
         const int j = spread_vec(u, v0, nq);  // < v0 + 4 * nq <= nv
         s.v[u] = load_stream_bits(vbase + j);
         const int p0 = 4 * j - rem;
+        if (p0 < 0 || p0 + 4 > len) {  // only vector 0 and vector nv - 1 have lanes outside the window
 #pragma unroll
-        for (int c = 0; c < 4; ++c) s.valid |= (p0 + c >= 0 && p0 + c < len ? 1u : 0u) << (4 * u + c);
+            for (int c = 0; c < 4; ++c)
+                if (p0 + c < 0 || p0 + c >= len) s.valid &= ~(1u << (4 * u + c));
+        }
     }
     return s;
 }
@@ -1132,7 +1141,7 @@ __device__ __forceinline__ SpreadSample spread_load(const float4* vbase, int nv,
 __device__ __forceinline__ uint32_t spread_count(const float4* vbase, int nv, int rem, int len) {
     const int v0 = spread_v0(vbase);
     const uint64_t nq = static_cast<uint32_t>(nv - v0) >> 2;
-    const int last = v0 + 4 * static_cast<int>((static_cast<uint64_t>(kSpreadPieces - 1) * nq) >> 8) + 3;
+    const int last = v0 + 4 * static_cast<int>((static_cast<uint64_t>(kSpreadPieces - 1) * nq) >> kSpreadLogPieces) + 3;
     return static_cast<uint32_t>(16 * kSpreadPieces - (v0 == 0 ? rem : 0) - (last == nv - 1 ? 4 * nv - rem - len : 0));
 }
 

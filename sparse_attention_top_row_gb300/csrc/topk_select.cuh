@@ -1679,10 +1679,10 @@ __device__ __forceinline__ void load_bits_full(int4 (&v)[kTileVecs], const float
 }
 
 // One step of the streamed filter: tile tt (in v) into the lists, then the
-// load of tile tt + 2 into v. Tiles [t_lo, t_hi) lie wholly inside the window
+// load of tile tt + kDist into v. Tiles [t_lo, t_hi) lie wholly inside the window
 // (no masks, unchecked loads); a warp with a lane within one tile of its
 // list's end takes the checked appends.
-template <bool kNonNeg>
+template <bool kNonNeg, int kDist>
 __device__ __forceinline__ void list_step(int4 (&v)[kTileVecs], int tt, int t_lo, int t_hi, int n_tiles,
                                           const float4* vbase, int nv, int rem, int len, uint32_t thr,
                                           uint32_t& a, uint32_t lim) {
@@ -1696,31 +1696,29 @@ __device__ __forceinline__ void list_step(int4 (&v)[kTileVecs], int tt, int t_lo
     } else {
         list_tile<kNonNeg, true, true>(v, thr, lb, tile_valid(tt * T, nv, rem, len), a, lim);
     }
-    const int tn = tt + 2;
+    const int tn = tt + kDist;
     if (tn < t_hi) load_bits_full(v, vbase, tn * T);
     else if (tn < n_tiles) load_bits(v, vbase, tn * T, nv);
 }
 
-// The streamed window (nv <= kListMaxTiles tiles) into the lists: two register
-// tiles in turn (tiles 0 and 1 loaded by the caller), one loading while the
-// other is filtered, the kPrefetchTiles tiles after those on their way into
-// L2. a: this thread's list cursor (shared address), lim: its end.
+// The streamed window (nv <= kListMaxTiles tiles) into the lists: one
+// register tile (tile 0 loaded by the caller), each tile's successor loaded
+// right after it is filtered and asked into L2 by one bulk prefetch a step
+// earlier, so its loads mostly hit L2 (a second register tile in flight was
+// slower: the registers it holds cost more than the latency it hides with
+// 32 warps per SM). a: this thread's list cursor (shared address), lim: its
+// end.
 template <bool kNonNeg>
-__device__ __forceinline__ void stream_list(int4 (&cur)[kTileVecs], int4 (&nxt)[kTileVecs], const float4* vbase,
-                                            int nv, int rem, int len, uint32_t thr, uint32_t& a, uint32_t lim) {
+__device__ __forceinline__ void stream_list(int4 (&cur)[kTileVecs], const float4* vbase, int nv, int rem, int len,
+                                            uint32_t thr, uint32_t& a, uint32_t lim) {
     constexpr int T = kTileVecs * kThreads;
     const int n_tiles = (nv + T - 1) / T;
     const int t_lo = rem == 0 ? 0 : 1;     // tile 0 holds the rem lanes before the window
     const int t_hi = (len + rem) / (4 * T);  // tiles below it end inside the window
-    for (int t = 0;; t += 2) {
-        if (threadIdx.x == 0) {
-            prefetch_tile_l2(vbase, t + 2 + kPrefetchTiles, nv);
-            prefetch_tile_l2(vbase, t + 3 + kPrefetchTiles, nv);
-        }
-        list_step<kNonNeg>(cur, t, t_lo, t_hi, n_tiles, vbase, nv, rem, len, thr, a, lim);
+    for (int t = 0;; ++t) {
+        if (threadIdx.x == 0) prefetch_tile_l2(vbase, t + 2, nv);
+        list_step<kNonNeg, 1>(cur, t, t_lo, t_hi, n_tiles, vbase, nv, rem, len, thr, a, lim);
         if (t + 1 >= n_tiles) break;
-        list_step<kNonNeg>(nxt, t + 1, t_lo, t_hi, n_tiles, vbase, nv, rem, len, thr, a, lim);
-        if (t + 2 >= n_tiles) break;
     }
 }
 
@@ -1847,15 +1845,14 @@ __device__ void stream_row(const Params& p, int b, const float* w, const float4*
             for (int t = 0; t < 2 + kPrefetchTiles; ++t) prefetch_tile_l2(vbase, t, nv);
     });
     load_bits(cur, vbase, 0, nv);
-    load_bits(nxt, vbase, T, nv);
     const uint32_t thr = pass_threshold(bound_key);
 #if TOPK_COMPACT_LISTS
     if (nv <= kListMaxTiles * T) {
         const uint32_t a0 = saddr(layout<kLay>().cand) + threadIdx.x * 4u;
         const uint32_t lim = a0 + static_cast<uint32_t>(kListCap) * kListStride;
         uint32_t a = a0;
-        if (bound_key >= 0x80000000u) stream_list<true>(cur, nxt, vbase, nv, rem, len, thr, a, lim);
-        else stream_list<false>(cur, nxt, vbase, nv, rem, len, thr, a, lim);
+        if (bound_key >= 0x80000000u) stream_list<true>(cur, vbase, nv, rem, len, thr, a, lim);
+        else stream_list<false>(cur, vbase, nv, rem, len, thr, a, lim);
         const Shared sh = layout<kLay>();
         const RowInfo ri = load_row(sh);
         const Emitter<kPaged> em = row_emitter<kPaged>(p, b, ri, 0, len, kPageCache, sh);
@@ -1864,6 +1861,9 @@ __device__ void stream_row(const Params& p, int b, const float* w, const float4*
         return;
     }
 #endif
+    // rows beyond the lists' 16-bit index (more than kListMaxTiles tiles):
+    // per-warp regions of (bits, position), two register tiles in turn
+    load_bits(nxt, vbase, T, nv);
     const uint32_t region = saddr(layout<kLay>().cand) + (threadIdx.x >> 5) * (kWarpCap * 8u);
     uint32_t wcount = 0;
     bool ovf = false;

@@ -578,3 +578,22 @@ def test_swa_combine_edge_rows(cuda_lib):
     w.update(positions=torch.tensor([-1, 2, 10, 5000, 0], dtype=torch.int32), window_size=16,
              swa_offsets=None, out_width=52)
     _check_swa(cuda_lib, w)
+
+
+@pytest.mark.slow
+def test_row_beyond_the_compact_index(cuda_lib):
+    """A row longer than the compact lists' 16-bit index covers on the
+    256-thread build (4096 tiles of 4096 scores): it takes the per-warp
+    region filter (two register tiles). 160 rows (more than the SMs) share one
+    buffer (stride 0): one of 2^24 + 5000 scores, the others of 3000."""
+    g = torch.Generator().manual_seed(77)
+    L = (1 << 24) + 5000
+    scores = torch.randn(L + 64, generator=g)
+    B, k = 160, 2048
+    lens = torch.full((B,), 3000, dtype=torch.int32)
+    lens[0] = L
+    w = dict(name="beyond the compact index", mode="ragged", k=k, scores=scores, score_stride=0,
+             row_starts=torch.arange(B, dtype=torch.int32) * 3, seq_lens=lens,
+             out_offsets=torch.arange(B, dtype=torch.int32), page_table=None, page_table_stride=0,
+             page_size=1, batch=B)
+    check_full(cuda_lib, w)

@@ -186,6 +186,8 @@ DESCRIPTIONS = {
     "paged_packed": "packed PAGED: 8 requests x 16 query rows, sliding window 16384, k=2048, page_size=64",
     "mixed": "mixed sweep: k in {512,1024,2048} x B in {1,31,129,1024} x {PAGED, RAGGED}, "
              "L log-uniform in [256, 131072] plus boundary rows (24 launches)",
+    "ragged_swa": "RAGGED top-k fused with the SWA combine: 4 requests x 1024 queries at positions 28672.., "
+                  "compressed windows of (pos+1)//4 = 7168..7424 entries, k=512, window 128, rows of 640",
 }
 EXTRA = ("ragged_tiny", "paged_decode", "paged_long_b1", "paged_long_b30", "paged_long_b31", "paged_packed",
          "mixed", "ragged_swa")

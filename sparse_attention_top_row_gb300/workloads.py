@@ -359,7 +359,7 @@ def select_rows(w, rows):
     out = dict(w)
     out.update(scores=scores, batch=len(rows), seq_lens=w["seq_lens"][idx].clone(),
                name=w["name"] + f" rows={rows[:4]}...")
-    for key in ("row_starts", "out_offsets", "page_table_row_starts", "row_to_batch"):
+    for key in ("row_starts", "out_offsets", "page_table_row_starts", "row_to_batch", "positions", "swa_offsets"):
         if w.get(key) is not None:
             out[key] = w[key][idx].clone()
     if w.get("page_table") is not None and w.get("row_to_batch") is None:

@@ -1759,15 +1759,23 @@ __device__ __forceinline__ FinishResult finish_list(uint32_t bound_key, uint32_t
     const uint32_t base16 = bound_key >> 16;
     uint32_t* const lp = reinterpret_cast<uint32_t*>(sh.cand) + threadIdx.x;  // entry s at lp[s * kThreads]
     uint32_t* const whw = sh.whist() + warp * kSmall;
+    auto count_pass = [&](auto nonneg) {
+        // a non-negative bound leaves only non-negative scores: key16 = top16 | 0x8000
+        constexpr bool kNN = decltype(nonneg)::value;
+        const uint32_t d16 = base16 - 0x8000u;
 #pragma unroll 2
-    for (uint32_t s = 0; s < nmax; ++s) {
-        if (s < n) {
-            const uint32_t e = lp[s * kThreads];
-            const uint32_t bin = fine_bin16(entry_key16(e), base16);
-            atomicAdd(&whw[bin], 1u);
-            lp[s * kThreads] = (bin << 16) | (e & 0xFFFFu);
+        for (uint32_t s = 0; s < nmax; ++s) {
+            if (s < n) {
+                const uint32_t e = lp[s * kThreads];
+                const uint32_t bin = kNN ? min((e >> 16) - d16, static_cast<uint32_t>(kSmall - 1))
+                                         : fine_bin16(entry_key16(e), base16);
+                atomicAdd(&whw[bin], 1u);
+                lp[s * kThreads] = __byte_perm(e, bin, 0x5410);  // (bin << 16) | (e & 0xFFFF)
+            }
         }
-    }
+    };
+    if (bound_key >= 0x80000000u) count_pass(std::true_type{});
+    else count_pass(std::false_type{});
     if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // page-table entries, published below
     if (__syncthreads_or(ovf)) return kNeedExact;
     if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);

@@ -175,6 +175,38 @@ def swa_combine(out, out_raw, positions, window_size: int, swa_offsets, width: i
     return res
 
 
+def e4m3_value(code: int) -> float:
+    """The value of one FP8 E4M3 code (see topk_oracle.cpp)."""
+    fn = _load().oracle_e4m3_value
+    fn.restype = ctypes.c_double
+    fn.argtypes = [ctypes.c_uint8]
+    return float(fn(int(code)))
+
+
+def indexer_logits(q, kv, kv_scale, weights, ks, ke, out, mutant: int = 0):
+    """Indexer logits (see topk_oracle.cpp) on host arrays: q uint8 E4M3 codes
+    [n_q, heads, dim], kv uint8 [n_kv, dim], kv_scale float32 [n_kv], weights
+    float32 [n_q, heads], ks/ke int32 [n_q]; `out` is a float32 [n_q, stride]
+    array updated in place (only each row's window columns) and returned."""
+    lib = _load(mutant)
+    fn = lib.oracle_indexer_logits
+    fn.restype = None
+    fn.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_int64]
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    kv = np.ascontiguousarray(kv, dtype=np.uint8)
+    n_q, heads, dim = q.shape
+    assert kv.ndim == 2 and kv.shape[1] == dim
+    kv_scale = np.ascontiguousarray(kv_scale, dtype=np.float32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32).reshape(n_q, heads)
+    ks = _i32(ks)
+    ke = _i32(ke)
+    assert out.dtype == np.float32 and out.ndim == 2 and out.shape[0] == n_q and out.flags.c_contiguous
+    fn(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(weights), _ptr(ks), _ptr(ke), int(n_q), int(heads), int(dim),
+       int(kv.shape[0]), _ptr(out), int(out.shape[1]))
+    return out
+
+
 def host_cores() -> int:
     """Host cores this process may run on."""
     try:

@@ -58,6 +58,24 @@
 //     then -1 up to the width (the page's PADDED_TOP_K, at least top_k +
 //     WINDOW_SIZE).
 //
+//   * Indexer logits (oracle_indexer_logits), the producer upstream of the
+//     top-k. The pages name it without defining it: the PR #35175 page (the
+//     PR body) says the DeepGEMM contiguous-KV indexer writes logit columns
+//     at absolute positions of the batch-flattened KV, and the PR #36684
+//     page ("Key source snippets", server_args.py) names an FP8 paged
+//     MQA-logits kernel and ties the v2 path to tcgen05/TMEM. The plainest
+//     reading of an FP8 multi-query logits producer, one key vector per KV
+//     position shared by every head, is the lightning indexer's score:
+//       logits[t][s] = kv_scale[s] * sum_h w[t][h] * max(0, q[t][h] . kv[s])
+//     for ks[t] <= s < ke[t] (nothing is written elsewhere), with q and kv
+//     in FP8 E4M3, w and kv_scale fp32. Row t of the logits is then the
+//     RAGGED transform's window at row_start = ks[t], seq_len = ke[t] - ks[t].
+//     E4M3 ("e4m3fn"): sign, 4 exponent bits with bias 7, 3 mantissa bits;
+//     exponent field 0 holds the subnormals m/8 * 2^-6; S.1111.111 is NaN;
+//     there is no infinity. Every product of two E4M3 values, and every sum
+//     of up to 2^20 of them, is exact in fp64, so the dot products here are
+//     exact; the weighted sum is fp64 and rounded to fp32 once.
+//
 // Parity pins (tests/test_oracle_pins.py): brute-force rank counting on tiny
 // rows, an exhaustive sweep over short vectors with ties and signed zeros,
 // invariants on every workload shape, numpy's partition on the tie-free
@@ -68,8 +86,10 @@
 // exists only so that a test can show each pin family catches that mistake.
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <vector>
 
 #ifndef ORACLE_MUTANT
@@ -113,6 +133,25 @@ int32_t paged_index(const int32_t* pt_row, int32_t page_size, int32_t p) {
     return pt_row[p / page_size] * page_size + (p + 1) % page_size;  // mutant
 #else
     return pt_row[p / page_size] * page_size + p % page_size;
+#endif
+}
+
+// The value of an FP8 E4M3 code (see the header).
+double e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+    const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+    return (c & 0x80u) ? -mag : mag;
+}
+
+// One head's weighted contribution w * max(0, dot) to a logit.
+double head_term(double w, double dot) {
+#if ORACLE_MUTANT == 10
+    return w * dot;  // mutant: the ReLU is dropped
+#elif ORACLE_MUTANT == 11
+    return std::max(w * dot, 0.0);  // mutant: the ReLU taken after the head weight
+#else
+    return w * std::max(dot, 0.0);
 #endif
 }
 
@@ -231,6 +270,35 @@ void oracle_swa_combine(int32_t batch, int32_t k, const int32_t* out, const int3
 #endif
         }
         while (t < width) res[t++] = -1;
+    }
+}
+
+double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+
+// Indexer logits (see the header): q [n_q, heads, dim] and kv [n_kv, dim] E4M3
+// codes, kv_scale [n_kv], weights [n_q, heads]; row t of `out` (stride
+// out_stride) gets columns max(ks[t], 0) .. min(ke[t], n_kv) - 1 and nothing
+// else.
+void oracle_indexer_logits(const uint8_t* q, const uint8_t* kv, const float* kv_scale, const float* weights,
+                           const int32_t* ks, const int32_t* ke, int32_t n_q, int32_t heads, int32_t dim,
+                           int64_t n_kv, float* out, int64_t out_stride) {
+    for (int32_t t = 0; t < n_q; ++t) {
+        const int64_t lo = std::max<int64_t>(ks[t], 0), hi = std::min<int64_t>(ke[t], n_kv);
+        for (int64_t s = lo; s < hi; ++s) {
+            double acc = 0.0;
+            for (int32_t h = 0; h < heads; ++h) {
+                const uint8_t* qh = q + ((int64_t)t * heads + h) * dim;
+                const uint8_t* ks_row = kv + s * dim;
+                double dot = 0.0;
+                for (int32_t d = 0; d < dim; ++d) dot += e4m3_value(qh[d]) * e4m3_value(ks_row[d]);
+                acc += head_term(weights[(int64_t)t * heads + h], dot);
+            }
+#if ORACLE_MUTANT == 12
+            out[(int64_t)t * out_stride + s] = (float)acc;  // mutant: the key's scale is dropped
+#else
+            out[(int64_t)t * out_stride + s] = (float)((double)kv_scale[s] * acc);
+#endif
+        }
     }
 }
 

@@ -7,6 +7,8 @@
 * numpy.partition on tie-free rows (a library routine on a special case);
 * an independent page-table expansion for the PAGED transform;
 * invariants on scaled-down versions of every workload shape;
+* the indexer logits: every E4M3 code against torch's float8_e4m3fn, a
+  hand-worked example and a closed form at the 64 x 128 head shape;
 * planted mistakes in the oracle (compiled variants) are each caught.
 """
 
@@ -244,6 +246,74 @@ def pin_swa_formula(mutant=0, seed=11):
 PINS += [pin_swa_golden, pin_swa_formula]
 
 
+LOGITS_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "indexer_logits_examples.json")
+
+
+def pin_e4m3_codes(mutant=0):
+    """Every FP8 E4M3 code decodes to torch's float8_e4m3fn value (a library
+    routine for the same format); 0x7F and 0xFF are NaN."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if c in (0x7F, 0xFF):
+            assert np.isnan(v) and np.isnan(lib[c])
+        else:
+            assert v == lib[c], (hex(c), v, lib[c])
+
+
+def pin_logits_golden(mutant=0):
+    """The indexer logits' hand-worked example (tests/golden/)."""
+    with open(LOGITS_GOLDEN) as f:
+        g = json.load(f)
+    n_q = len(g["q"])
+    out = np.full((n_q, g["stride"]), g["fill"], dtype=np.float32)
+    oracle.indexer_logits(np.array(g["q"], dtype=np.uint8), np.array(g["kv"], dtype=np.uint8), g["kv_scale"],
+                          g["weights"], g["ks"], g["ke"], out, mutant=mutant)
+    assert out.tolist() == g["expect"]
+
+
+def pin_logits_one_hot(mutant=0, seed=13):
+    """Closed form at the indexer's own shape (64 heads of width 128): with
+    q[t][h] one-hot at coordinate (h + t) % 128 and kv[s] one-hot at s % 128,
+    only head h* = (s - t) mod 128 meets key s, so logits[t][s] = kv_scale[s]
+    * w[t][h*] * max(0, q_val * kv_val) when h* < 64, else 0; windows clamp
+    to [0, n_kv) and nothing outside them is written."""
+    rng = np.random.default_rng(seed)
+    n_q, heads, dim, n_kv = 6, 64, 128, 300
+    f8 = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    qc = rng.choice(finite, (n_q, heads))
+    kc = rng.choice(finite, n_kv)
+    q = np.zeros((n_q, heads, dim), np.uint8)
+    kv = np.zeros((n_kv, dim), np.uint8)
+    for t in range(n_q):
+        for h in range(heads):
+            q[t, h, (h + t) % dim] = qc[t, h]
+    for s in range(n_kv):
+        kv[s, s % dim] = kc[s]
+    w = rng.standard_normal((n_q, heads)).astype(np.float32)
+    scale = rng.uniform(0.25, 4.0, n_kv).astype(np.float32)
+    ks = np.array([0, 5, -7, 150, 299, 200], np.int32)
+    ke = np.array([300, 131, 40, 420, 299, 100], np.int32)
+    out = np.full((n_q, n_kv + 3), -5.0, np.float32)
+    oracle.indexer_logits(q, kv, scale, w, ks, ke, out, mutant=mutant)
+    for t in range(n_q):
+        lo, hi = max(int(ks[t]), 0), min(int(ke[t]), n_kv)
+        for s in range(n_kv + 3):
+            if not lo <= s < hi:
+                assert out[t, s] == -5.0
+                continue
+            h = (s - t) % dim
+            want = 0.0
+            if h < heads:
+                want = np.float64(scale[s]) * (np.float64(w[t, h]) * max(f8[qc[t, h]] * f8[kc[s]], 0.0))
+            assert out[t, s] == np.float32(want), (t, s)
+
+
+PINS += [pin_e4m3_codes, pin_logits_golden, pin_logits_one_hot]
+
+
 # ------------------------------------------------------------------ tests
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -264,7 +334,7 @@ def test_error_rows_are_empty_and_counted():
 
 def test_planted_mistakes_are_caught():
     """Each planted mistake in the oracle fails at least one pin family."""
-    for mutant in range(1, 10):
+    for mutant in range(1, 13):
         caught = []
         for pin in PINS:
             try:

@@ -245,6 +245,51 @@ TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride
                                        int32_t* out_raw, uint32_t flags, topk_stream_t stream);
 
 /*
+ * Indexer logits: the producer upstream of the top-k, an FP8 multi-query
+ * logits contraction on the tensor cores. The PR #35175 page (PR body) says
+ * the contiguous-KV indexer writes its logit columns at absolute positions of
+ * the batch-flattened KV, and the PR #36684 page ("Key source snippets",
+ * server_args.py) ties the path to tcgen05/TMEM; neither prints the formula.
+ * This computes the plainest reading, the lightning indexer's score:
+ *
+ *   logits[t * logits_stride + s] =
+ *       kv_scale[s] * sum_{h < 64} weights[t * 64 + h] * max(0, q[t][h] . kv[s])
+ *
+ * for every s with max(ks[t], 0) <= s < min(ke[t], n_kv), with the dot
+ * products over 128 FP8 E4M3 ("e4m3fn") coordinates accumulated in fp32.
+ * Nothing outside each row's window is written, so row t is then the RAGGED
+ * transform's window at row_start = ks[t], seq_len = ke[t] - ks[t] (with
+ * score_stride = logits_stride).
+ *
+ *   q            device, [n_q, 64, 128] E4M3 codes (one byte each), row-major,
+ *                16-byte aligned.
+ *   kv           device, [n_kv, 128] E4M3 codes, row-major, 16-byte aligned.
+ *   kv_scale     device fp32 [n_kv].
+ *   weights      device fp32 [n_q, 64], row-major.
+ *   ks, ke       device int32 [n_q]: each query's key window (clamped to
+ *                [0, n_kv); ke <= ks: an empty row, nothing written).
+ *   n_q          queries, 0 .. TOPK_INDEXER_MAX_QUERIES.
+ *   n_kv         keys, >= 0.
+ *   logits       device fp32, row t at logits + t * logits_stride; the
+ *                caller's buffer holds every written column.
+ *   device_flags device uint32, required: TOPK_DEVICE_FLAG_TIMEOUT is OR-ed
+ *                in if a wait on the kernel's own copies or MMAs gave up
+ *                (the result is then unreliable); the caller zeroes it.
+ * Status: TOPK_ERR_ARG for a negative count or stride, n_q above the
+ * maximum, or a null pointer; TOPK_ERR_ALIGN for q or kv off 16 bytes;
+ * TOPK_ERR_CUDA for a failed launch or tensor-map encoding. n_q == 0 or
+ * n_kv == 0 is TOPK_OK and enqueues nothing. One launch, with programmatic
+ * dependent launch like every kernel of the library.
+ */
+#define TOPK_INDEXER_HEADS 64
+#define TOPK_INDEXER_DIM 128
+#define TOPK_INDEXER_MAX_QUERIES (1 << 24)
+TOPK_API int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const float* kv_scale,
+                                 const float* weights, const int32_t* ks, const int32_t* ke, int32_t n_q,
+                                 int32_t n_kv, float* logits, int64_t logits_stride,
+                                 uint32_t* device_flags, topk_stream_t stream);
+
+/*
  * Reads the workspace's device error count (rows with seq_len < 0 seen by the
  * plan, plus rows with row_start < 0, or for packed PAGED rows
  * page_table_row_start < 0, seen by each transform since the plan) and the

@@ -32,7 +32,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtopk.so")
 
 EXPORTED = ("topk_workspace_bytes", "topk_plan", "topk_transform_paged", "topk_transform_paged_packed",
             "topk_transform_ragged", "topk_read_device_errors", "topk_status_string",
-            "topk_transform_ragged_noalloc", "topk_transform_launches", "topk_transform_ragged_swa")
+            "topk_transform_ragged_noalloc", "topk_transform_launches", "topk_transform_ragged_swa",
+            "topk_indexer_logits")
+TOPK_INDEXER_HEADS = 64
+TOPK_INDEXER_DIM = 128
 TOPK_NOALLOC_MAX_BATCH = 16384
 
 
@@ -78,6 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.topk_transform_ragged_swa.restype = ctypes.c_int
         lib.topk_transform_ragged_swa.argtypes = [c_p, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_p, c_sz,
                                                   c_p, c_i32, c_p, c_i32, c_p, c_p, c_u32, c_p]
+        lib.topk_indexer_logits.restype = ctypes.c_int
+        lib.topk_indexer_logits.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_i32, c_p, c_i64, c_p, c_p]
         lib.topk_transform_launches.restype = ctypes.c_int
         lib.topk_transform_launches.argtypes = [c_i32]
         lib.topk_status_string.restype = ctypes.c_char_p
@@ -293,6 +298,36 @@ def topk_transform_ragged_noalloc(scores, score_stride: int, row_starts, seq_len
             _arg(out, "out", i32, batch * int(k), device=dev),
             _arg(out_raw, "out_raw", i32, batch * int(k), required=False, device=dev), int(flags))
     _check("topk_transform_ragged_noalloc", lib.topk_transform_ragged_noalloc(*args, st))
+
+
+def topk_indexer_logits(q, kv, kv_scale, weights, ks, ke, logits, logits_stride: int, device_flags, stream=None):
+    """Indexer logits (see include/topk.h): q [n_q, 64, 128] and kv [n_kv, 128]
+    FP8 E4M3 codes (torch.uint8 or torch.float8_e4m3fn), kv_scale float32
+    [n_kv], weights float32 [n_q, 64], ks/ke int32 [n_q]; row t of `logits`
+    (float32, rows logits_stride apart) gets columns ks[t] .. ke[t] - 1;
+    device_flags: an int32 word the kernel ORs TOPK_DEVICE_FLAG_TIMEOUT into."""
+    import torch
+    lib = load()
+    st, dev = _stream(stream)
+    for name, t, nd in (("q", q, 3), ("kv", kv, 2)):
+        if not isinstance(t, torch.Tensor) or t.dim() != nd or t.shape[-1] != TOPK_INDEXER_DIM or \
+                (nd == 3 and t.shape[1] != TOPK_INDEXER_HEADS):
+            raise ValueError(f"{name} must be a tensor of shape {'[n_q, 64, 128]' if nd == 3 else '[n_kv, 128]'}")
+    if q.dtype is torch.float8_e4m3fn:
+        q = q.view(torch.uint8)
+    if kv.dtype is torch.float8_e4m3fn:
+        kv = kv.view(torch.uint8)
+    n_q, n_kv = int(q.shape[0]), int(kv.shape[0])
+    u8, f32, i32 = torch.uint8, torch.float32, torch.int32
+    need = 0 if n_q == 0 or n_kv == 0 else (n_q - 1) * max(int(logits_stride), 0) + n_kv
+    args = (_arg(q, "q", u8, n_q * TOPK_INDEXER_HEADS * TOPK_INDEXER_DIM, device=dev),
+            _arg(kv, "kv", u8, n_kv * TOPK_INDEXER_DIM, device=dev),
+            _arg(kv_scale, "kv_scale", f32, n_kv, device=dev),
+            _arg(weights, "weights", f32, n_q * TOPK_INDEXER_HEADS, device=dev),
+            _arg(ks, "ks", i32, n_q, device=dev), _arg(ke, "ke", i32, n_q, device=dev), n_q, n_kv,
+            _arg(logits, "logits", f32, need, dense=False, device=dev), int(logits_stride),
+            _arg(device_flags, "device_flags", i32, 1, device=dev))
+    _check("topk_indexer_logits", lib.topk_indexer_logits(*args, st))
 
 
 def topk_read_device_errors(workspace, stream=None):

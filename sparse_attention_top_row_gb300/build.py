@@ -1,7 +1,7 @@
 """Builds the CUDA library in-tree (``_build/libtopk.so``) for sm_103a.
 
-Three translation units (the plan and C ABI, and the selection kernels
-compiled for 512 and for 256 threads per row), compiled in parallel to
+Four translation units (the plan and C ABI, the selection kernels compiled
+for 512 and for 256 threads per row, and the indexer-logits kernel), compiled in parallel to
 objects and linked into one shared library; one ``-gencode``, shared cudart
 (the same runtime PyTorch loads). nvcc cross-compiles without a GPU.
 """
@@ -15,7 +15,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, f) for f in ("topk.cu", "topk_select512.cu", "topk_select256.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("topk.cu", "topk_select512.cu", "topk_select256.cu", "topk_logits.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("topk_common.cuh", "topk_select.cuh")]
 HEADER = os.path.join(ROOT, "include", "topk.h")
 BUILD_DIR = os.path.join(HERE, "_build")

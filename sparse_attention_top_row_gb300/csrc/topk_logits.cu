@@ -1,0 +1,417 @@
+// The indexer-logits producer upstream of the top-k, on the 5th-generation
+// tensor cores of sm_103a (tcgen05 MMAs with TMEM accumulators, operands
+// staged by TMA):
+//
+//   logits[t][s] = kv_scale[s] * sum_h w[t][h] * max(0, q[t][h] . kv[s])
+//   for ks[t] <= s < ke[t]
+//
+// with q [n_q, 64, 128] and kv [n_kv, 128] FP8 E4M3, w [n_q, 64] and
+// kv_scale [n_kv] fp32. This is the reading of the FP8 MQA-logits producer
+// that the PR #35175 page (PR body: the contiguous-KV indexer writes logit
+// columns at absolute positions of the batch-flattened KV) and the PR #36684
+// page ("Key source snippets", server_args.py: the v2 path needs tcgen05 and
+// TMEM) put upstream of the top-k; row t of the result is the RAGGED
+// transform's window at row_start = ks[t], seq_len = ke[t] - ks[t].
+//
+// Mapping. A CTA takes a group of kGroup = 4 consecutive queries. Their
+// 4 x 64 head vectors (256 rows of 128 bytes) are the MMA's B operand,
+// loaded once; the group's keys stream through a ring of kStages
+// shared-memory stages, 128 keys (16 KB) a stage, as the A operand. One tile
+// D = KV_tile . Q^T has M = 128 keys (TMEM lanes), N = 256 (query, head)
+// columns and K = 128 (four kind::f8f6f4 MMAs of K = 32), so each epilogue
+// thread owns one key and finds all 64 heads of a query in its own TMEM
+// lane: the head sum needs no exchange between threads. Two accumulators
+// (2 x 256 TMEM columns) let the MMAs of tile j + 1 run while tile j is read
+// out. Shared memory (about 130 KB) keeps one CTA per SM, so the CTA's
+// 512-column TMEM allocation never waits.
+//
+// Warp roles (10 warps): warp 0 issues the TMA loads (one thread), warp 1
+// owns the TMEM allocation and issues the MMAs (one thread), warps 2..9 read
+// the accumulators out. A warp reaches TMEM lanes 32 * (warp % 4) .. + 31;
+// warps 2..5 take queries 0 and 1 of the group, warps 6..9 queries 2 and 3.
+//
+// Every wait on an mbarrier is bounded: past about a second the kernel ORs
+// TOPK_DEVICE_FLAG_TIMEOUT into the caller's flag word and goes on, so no
+// barrier is left unmatched and the TMEM allocation is always released.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "topk.h"
+#include "topk_common.cuh"
+
+namespace topk_impl {
+namespace {
+
+constexpr int kHeads = TOPK_INDEXER_HEADS;  // 64
+constexpr int kDim = TOPK_INDEXER_DIM;      // 128 (bytes of one FP8 row)
+constexpr int kGroup = 4;                   // queries per CTA
+constexpr int kN = kGroup * kHeads;         // 256: MMA N (query, head) columns
+constexpr int kM = 128;                     // keys per tile: MMA M, TMEM lanes
+constexpr int kMmaK = 32;                   // K of one kind::f8f6f4 MMA
+constexpr int kStages = 6;                  // key tiles in flight
+constexpr int kEpiWarps = 8;
+constexpr int kThreadsL = 32 * (2 + kEpiWarps);
+constexpr uint32_t kTmemCols = 2 * kN;      // two accumulators
+constexpr uint32_t kQBytes = kN * kDim;     // 32 KB
+constexpr uint32_t kTileBytes = kM * kDim;  // 16 KB
+constexpr uint32_t kKvOff = kQBytes;
+constexpr uint32_t kWOff = kKvOff + kStages * kTileBytes;
+constexpr uint32_t kBarOff = kWOff + kN * 4;
+constexpr int kBars = 2 * kStages + 1 + 2 + 2;  // full, empty, q, tmem full, tmem empty
+constexpr uint32_t kSlotOff = kBarOff + kBars * 8;
+constexpr size_t kSmemLogits = kSlotOff + 16 + 1024;  // + alignment slack (tiles on 1024 B)
+static_assert(kSmemLogits > 114 * 1024, "one CTA per SM (its TMEM allocation is the whole TMEM)");
+static_assert(kSmemLogits <= 227 * 1024, "shared memory per CTA");
+constexpr long long kLogitsWaitCycles = 1ll << 31;  // about a second
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1),
+// A and B E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kN >> 3) << 17) | (static_cast<uint32_t>(kM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile of 128-byte rows in the
+// 128-byte swizzle (what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes):
+// start address >> 4 (bits 0-13), leading offset unused for this layout (1),
+// stride offset 1024 B between 8-row groups (bits 32-45), version 1 (bits
+// 46-47), base offset 0 (tiles on 1024-byte boundaries), layout 2 = 128-byte
+// swizzle (bits 61-63). Stepping K by 32 bytes inside the swizzled row adds
+// 2 to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ uint32_t cvta_smem(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+// Waits for the phase of `bar` with this parity to complete, at most
+// kLogitsWaitCycles; past that it flags the timeout and returns.
+__device__ __forceinline__ void bar_wait(uint32_t bar, uint32_t parity, uint32_t* flags) {
+    if (bar_try_wait(bar, parity)) return;
+    const long long t0 = clock64();
+    while (!bar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kLogitsWaitCycles) {
+            atomicOr(flags, TOPK_DEVICE_FLAG_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// 2-D TMA tile load (x: byte column, a multiple of 16; y: row) completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (TMEM) = A . B^T (+ D when acc): A, B from shared memory by descriptor.
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+// `bar` gets one arrival once every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// This warp's 32 TMEM lanes, 64 consecutive fp32 columns from `taddr`
+// (thread i: lane base + i), waited for inside the same statement so that
+// no use of the registers can be scheduled before the data are in.
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+}
+
+struct LogitsParams {
+    const float* kv_scale;
+    const float* weights;
+    const int32_t* ks;
+    const int32_t* ke;
+    float* logits;
+    int64_t stride;
+    int32_t n_q;
+    int32_t n_kv;
+    uint32_t* flags;
+};
+
+__global__ void __launch_bounds__(kThreadsL, 1)
+    topk_indexer_logits_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
+                               const __grid_constant__ LogitsParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = cvta_smem(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const sm = smem_raw + (base - raw);
+    float* const sw = reinterpret_cast<float*>(sm + kWOff);
+    const uint32_t bars = base + kBarOff;
+    auto full = [&](int s) { return bars + 8u * static_cast<uint32_t>(s); };
+    auto empty = [&](int s) { return bars + 8u * static_cast<uint32_t>(kStages + s); };
+    const uint32_t qfull = bars + 8u * (2 * kStages);
+    auto tfull = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 1 + b); };
+    auto tempty = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 3 + b); };
+    uint32_t* const slot = reinterpret_cast<uint32_t*>(sm + kSlotOff);
+
+    const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31u);
+    grid_dependency_wait();
+    const int t0 = static_cast<int>(blockIdx.x) * kGroup;
+    // the group's key span (the same on every thread)
+    int lo = INT_MAX, hi = 0;
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+        const int t = t0 + i;
+        if (t < p.n_q) {
+            const int a = max(p.ks[t], 0), b = min(p.ke[t], p.n_kv);
+            if (a < b) {
+                lo = min(lo, a);
+                hi = max(hi, b);
+            }
+        }
+    }
+    if (lo >= hi) {
+        allow_dependents();
+        return;
+    }
+    const int kbase = lo & ~(kM - 1);
+    const int n_tiles = (hi - kbase + kM - 1) / kM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            bar_init(full(s), 1);
+            bar_init(empty(s), 1);
+        }
+        bar_init(qfull, 1);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(tfull(b), 1);
+            bar_init(tempty(b), kEpiWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(cvta_smem(slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp >= 2) {  // the group's head weights (0 for queries past n_q)
+        const int e = static_cast<int>(threadIdx.x) - 64;
+        const int t = t0 + (e >> 6);
+        sw[e] = t < p.n_q ? p.weights[static_cast<int64_t>(t) * kHeads + (e & 63)] : 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // TMA producer
+            bar_expect_tx(qfull, kQBytes);
+            tma_load_2d(base, &tq, 0, t0 * kHeads, qfull);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % kStages;
+                if (j >= kStages) bar_wait(empty(s), static_cast<uint32_t>((j / kStages) & 1) ^ 1u, p.flags);
+                bar_expect_tx(full(s), kTileBytes);
+                tma_load_2d(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes, &tkv, 0, kbase + j * kM, full(s));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            bar_wait(qfull, 0, p.flags);
+            const uint64_t bdesc = sw128_desc(base);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % kStages, b = j & 1;
+                bar_wait(full(s), static_cast<uint32_t>((j / kStages) & 1), p.flags);
+                if (j >= 2) bar_wait(tempty(b), static_cast<uint32_t>((j >> 1) & 1) ^ 1u, p.flags);
+                tc_fence_after();
+                const uint64_t adesc = sw128_desc(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * kN);
+#pragma unroll
+                for (int kk = 0; kk < kDim / kMmaK; ++kk)
+                    mma_f8(d, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), kk > 0 ? 1u : 0u);
+                mma_commit(empty(s));
+                mma_commit(tfull(b));
+            }
+            // the last tile's MMAs are complete before the TMEM is released
+            const int jl = n_tiles - 1;
+            bar_wait(tfull(jl & 1), static_cast<uint32_t>((jl >> 1) & 1), p.flags);
+        }
+        __syncwarp();
+    } else {  // epilogue: one key per thread, two queries per warp
+        const int quarter = warp & 3;
+        const int qa = 2 * ((warp - 2) >> 2);  // first query of this warp's pair
+        const int row = quarter * 32 + lane;
+        int lo_t[2], hi_t[2];
+        float* out_row[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = t0 + qa + i;
+            const bool v = t < p.n_q;
+            lo_t[i] = v ? max(p.ks[t], 0) : 0;
+            hi_t[i] = v ? min(p.ke[t], p.n_kv) : 0;
+            out_row[i] = p.logits + static_cast<int64_t>(v ? t : 0) * p.stride;
+        }
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int b = j & 1;
+            const int s = kbase + j * kM + row;
+            const float scale = s < p.n_kv ? __ldg(p.kv_scale + s) : 0.0f;
+            bar_wait(tfull(b), static_cast<uint32_t>((j >> 1) & 1), p.flags);
+            __syncwarp();  // the TMEM loads below are warp-collective
+            tc_fence_after();
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                uint32_t r[64];
+                tmem_load64(lane_addr + static_cast<uint32_t>(b * kN + (qa + i) * kHeads), r);
+                const float4* wq = reinterpret_cast<const float4*>(sw + (qa + i) * kHeads);
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+                for (int h = 0; h < kHeads; h += 4) {
+                    const float4 wv = wq[h >> 2];
+                    a0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.0f), a0);
+                    a1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.0f), a1);
+                    a2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.0f), a2);
+                    a3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.0f), a3);
+                }
+                if (s >= lo_t[i] && s < hi_t[i]) out_row[i][s] = ((a0 + a1) + (a2 + a3)) * scale;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(tempty(b));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    allow_dependents();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2-D map over `rows` rows of 128 bytes, tiles of box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kDim), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevicesL = 64;
+bool g_logits_ready[kMaxDevicesL];
+std::mutex g_logits_mutex;
+
+cudaError_t prepare_logits() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevicesL) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_logits_mutex);
+    if (!g_logits_ready[dev]) {
+        e = cudaFuncSetAttribute(topk_indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemLogits));
+        if (e != cudaSuccess) return e;
+        g_logits_ready[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace topk_impl
+
+using namespace topk_impl;
+
+extern "C" int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const float* kv_scale, const float* weights,
+                                   const int32_t* ks, const int32_t* ke, int32_t n_q, int32_t n_kv, float* logits,
+                                   int64_t logits_stride, uint32_t* device_flags, topk_stream_t stream) {
+    if (n_q < 0 || n_kv < 0 || n_q > TOPK_INDEXER_MAX_QUERIES || logits_stride < 0) return TOPK_ERR_ARG;
+    if (n_q == 0 || n_kv == 0) return TOPK_OK;
+    if (!q || !kv || !kv_scale || !weights || !ks || !ke || !logits || !device_flags) return TOPK_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(kv) & 15u) != 0)
+        return TOPK_ERR_ALIGN;
+    if (prepare_logits() != cudaSuccess) return TOPK_ERR_CUDA;
+    CUtensorMap tq, tkv;
+    if (!make_map(&tq, q, static_cast<uint64_t>(n_q) * kHeads, kN) ||
+        !make_map(&tkv, kv, static_cast<uint64_t>(n_kv), kM))
+        return TOPK_ERR_CUDA;
+    LogitsParams prm;
+    prm.kv_scale = kv_scale;
+    prm.weights = weights;
+    prm.ks = ks;
+    prm.ke = ke;
+    prm.logits = logits;
+    prm.stride = logits_stride;
+    prm.n_q = n_q;
+    prm.n_kv = n_kv;
+    prm.flags = device_flags;
+    const int grid = (n_q + kGroup - 1) / kGroup;
+    const cudaError_t e = launch_pdl(topk_indexer_logits_kernel, grid, kThreadsL, kSmemLogits,
+                                     reinterpret_cast<cudaStream_t>(stream), tq, tkv, prm);
+    return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}

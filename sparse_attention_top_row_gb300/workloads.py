@@ -268,6 +268,50 @@ def mixed(device="cpu", mode="paged", k=2048, batch=129, sub_id=0, max_len=13107
     return w
 
 
+def _e4m3_codes(x):
+    """FP8 E4M3 codes (uint8) of a float tensor, rounded by torch's
+    float8_e4m3fn conversion (input drawing only)."""
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+
+
+def indexer_inputs(device="cpu", sub_id=0, n_q=13, n_kv=1000, windows=None, heads=64, dim=128):
+    """Inputs of the indexer logits (the producer upstream of the top-k):
+    q [n_q, heads, dim] and kv [n_kv, dim] as FP8 E4M3 codes of N(0, 2^2)
+    draws, kv_scale [n_kv] ~ U(0.005, 0.02) (a dequantisation scale), weights
+    [n_q, heads] ~ N(0, 1/64), and each query's key window [ks, ke): given,
+    or drawn at random (empty, clamped and partial-tile windows included)."""
+    g = _gen(device, seed_for(9, sub_id))
+    q = _e4m3_codes(2.0 * torch.randn(n_q, heads, dim, generator=g, device=device))
+    kv = _e4m3_codes(2.0 * torch.randn(n_kv, dim, generator=g, device=device))
+    kv_scale = 0.005 + 0.015 * torch.rand(n_kv, generator=g, device=device)
+    weights = torch.randn(n_q, heads, generator=g, device=device) / 8.0
+    if windows is None:
+        a = torch.randint(-40, n_kv + 40, (n_q,), generator=g, device=device)
+        b = a + torch.randint(-5, n_kv + 80, (n_q,), generator=g, device=device)
+        ks, ke = _i32(a), _i32(b)
+    else:
+        ks, ke = (torch.as_tensor(x, dtype=torch.int32, device=device) for x in windows)
+    return dict(name=f"indexer logits n_q={n_q} n_kv={n_kv}", q=q, kv=kv, kv_scale=kv_scale,
+                weights=weights.contiguous(), ks=ks, ke=ke, n_q=n_q, n_kv=n_kv)
+
+
+def indexer_extend(device="cpu", chunk=0, rows_per_chunk=1024, n_req=4, prefix=28672, new=4096, sub_id=None):
+    """The indexer logits feeding one chunk of the prefill-extend top-k:
+    the same query rows and windows as ``ragged_extend`` (query i of request
+    r: keys [r*(prefix+new), r*(prefix+new) + prefix + i + 1) of the
+    flattened KV of n_req*(prefix+new) keys), with FP8 inputs drawn as in
+    ``indexer_inputs``. The logits' row stride is the flattened KV length."""
+    rows = torch.arange(chunk * rows_per_chunk, (chunk + 1) * rows_per_chunk, device=device)
+    req = rows // new
+    starts = req * (prefix + new)
+    ends = starts + prefix + rows % new + 1
+    w = indexer_inputs(device, chunk if sub_id is None else sub_id, n_q=rows_per_chunk,
+                       n_kv=n_req * (prefix + new), windows=(starts, ends))
+    w["name"] = f"indexer logits, extend chunk={chunk} rows={rows_per_chunk} req={n_req} prefix={prefix} new={new}"
+    w["stride"] = n_req * (prefix + new)
+    return w
+
+
 def custom(mode, k, rows, *, device="cpu", score_stride=None, row_starts=None, out_offsets=None,
            page_size=1, page_table=None, seed=0):
     """Build a workload from explicit per-row score lists (small edge cases).

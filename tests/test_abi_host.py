@@ -124,6 +124,23 @@ def test_swa_transform_validation(lib):
                0, None) == 0
 
 
+def test_indexer_logits_validation(lib):
+    fn = lib.topk_indexer_logits
+    # q, kv, kv_scale, weights, ks, ke, n_q, n_kv, logits, stride, device_flags, stream
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 10, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, -1, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, (1 << 24) + 1, 10, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, -16, FAKE, None) == 1
+    assert fn(None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 10, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, None, None) == 1  # no flag word
+    assert fn(FAKE_UNALIGNED, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 2
+    assert fn(FAKE, FAKE_UNALIGNED, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 2
+    # nothing to compute: no-ops that enqueue nothing
+    assert fn(None, None, None, None, None, None, 0, 10, None, 0, None, None) == 0
+    assert fn(None, None, None, None, None, None, 4, 0, None, 0, None, None) == 0
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert lib.topk_status_string(s)

@@ -13,10 +13,12 @@
 // TMEM) put upstream of the top-k; row t of the result is the RAGGED
 // transform's window at row_start = ks[t], seq_len = ke[t] - ks[t].
 //
-// Mapping. A CTA takes a group of kGroup = 4 consecutive queries. Their
-// 4 x 64 head vectors (256 rows of 128 bytes) are the MMA's B operand,
-// loaded once; the group's keys stream through a ring of kStages
-// shared-memory stages, 128 keys (16 KB) a stage, as the A operand. One tile
+// Mapping. A CTA takes a group of kGroup = 4 consecutive queries and a
+// contiguous share of the group's key tiles (the host splits each group into
+// `parts` shares so that the CTAs, one per SM, fill their last wave). The 4 x
+// 64 head vectors (256 rows of 128 bytes) are the MMA's B operand, loaded
+// once; the keys stream through a ring of kStages shared-memory stages, 128
+// keys (16 KB) a stage, as the A operand. One tile
 // D = KV_tile . Q^T has M = 128 keys (TMEM lanes), N = 256 (query, head)
 // columns and K = 128 (four kind::f8f6f4 MMAs of K = 32), so each epilogue
 // thread owns one key and finds all 64 heads of a query in its own TMEM
@@ -25,10 +27,15 @@
 // out. Shared memory (about 130 KB) keeps one CTA per SM, so the CTA's
 // 512-column TMEM allocation never waits.
 //
-// Warp roles (10 warps): warp 0 issues the TMA loads (one thread), warp 1
-// owns the TMEM allocation and issues the MMAs (one thread), warps 2..9 read
-// the accumulators out. A warp reaches TMEM lanes 32 * (warp % 4) .. + 31;
-// warps 2..5 take queries 0 and 1 of the group, warps 6..9 queries 2 and 3.
+// Warp roles (10 warps): one thread of warp 0 issues the TMA loads; warp 1
+// owns the TMEM allocation and one of its threads issues the MMAs (a single
+// thread issuing both was the bottleneck: each step of its loop waits);
+// warps 2..9 read the accumulators out. A warp reaches TMEM lanes
+// 32 * (warp % 4) .. + 31: warps 2..5 take the even tiles (accumulator 0),
+// warps 6..9 the odd ones (accumulator 1), all four queries each, in two
+// 128-column loads; the accumulator goes back to the MMAs once the second is
+// in. On every SM sub-partition one warp of each group runs, so one computes
+// while the other waits for its tile.
 //
 // Every wait on an mbarrier is bounded: past about a second the kernel ORs
 // TOPK_DEVICE_FLAG_TIMEOUT into the caller's flag word and goes on, so no
@@ -39,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -149,27 +157,49 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// This warp's 32 TMEM lanes, 64 consecutive fp32 columns from `taddr`
+// This warp's 32 TMEM lanes, 128 consecutive fp32 columns from `taddr`
 // (thread i: lane base + i), waited for inside the same statement so that
 // no use of the registers can be scheduled before the data are in.
-__device__ __forceinline__ void tmem_load64(uint32_t taddr, uint32_t (&r)[64]) {
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
         "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
         "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
+        "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+        "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
+        "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
+        "}, [%128];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        :
+          "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
           "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
           "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
           "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+          "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+          "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+          "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+          "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+          "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+          "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+          "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+          "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
         : "r"(taddr)
         : "memory");
+}
+
+// Four consecutive fp32 words of shared memory (a broadcast when every lane
+// reads the same address).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
 }
 
 struct LogitsParams {
@@ -181,6 +211,7 @@ struct LogitsParams {
     int64_t stride;
     int32_t n_q;
     int32_t n_kv;
+    int32_t parts;  // CTAs per query group, each a contiguous share of the group's key tiles
     uint32_t* flags;
 };
 
@@ -202,8 +233,9 @@ __global__ void __launch_bounds__(kThreadsL, 1)
 
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31u);
     grid_dependency_wait();
-    const int t0 = static_cast<int>(blockIdx.x) * kGroup;
-    // the group's key span (the same on every thread)
+    const int group = static_cast<int>(blockIdx.x) / p.parts, part = static_cast<int>(blockIdx.x) % p.parts;
+    const int t0 = group * kGroup;
+    // the group's key span (the same on every thread), then this CTA's share of its tiles
     int lo = INT_MAX, hi = 0;
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
@@ -216,12 +248,15 @@ __global__ void __launch_bounds__(kThreadsL, 1)
             }
         }
     }
-    if (lo >= hi) {
+    const int kbase0 = lo & ~(kM - 1);
+    const int group_tiles = lo < hi ? (hi - kbase0 + kM - 1) / kM : 0;
+    const int per_part = (group_tiles + p.parts - 1) / p.parts;
+    const int n_tiles = max(0, min(per_part, group_tiles - part * per_part));
+    if (n_tiles == 0) {
         allow_dependents();
         return;
     }
-    const int kbase = lo & ~(kM - 1);
-    const int n_tiles = (hi - kbase + kM - 1) / kM;
+    const int kbase = kbase0 + part * per_part * kM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -231,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsL, 1)
         bar_init(qfull, 1);
         for (int b = 0; b < 2; ++b) {
             bar_init(tfull(b), 1);
-            bar_init(tempty(b), kEpiWarps);
+            bar_init(tempty(b), kEpiWarps / 2);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -285,47 +320,63 @@ __global__ void __launch_bounds__(kThreadsL, 1)
             bar_wait(tfull(jl & 1), static_cast<uint32_t>((jl >> 1) & 1), p.flags);
         }
         __syncwarp();
-    } else {  // epilogue: one key per thread, two queries per warp
+    } else {  // epilogue: one key per thread, the four queries of every other tile
         const int quarter = warp & 3;
-        const int qa = 2 * ((warp - 2) >> 2);  // first query of this warp's pair
+        const int eg = (warp - 2) >> 2;  // epilogue group: tiles j with j % 2 == eg, accumulator eg
         const int row = quarter * 32 + lane;
-        int lo_t[2], hi_t[2];
-        float* out_row[2];
+        int lo_t[kGroup], hi_t[kGroup];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int t = t0 + qa + i;
+        for (int i = 0; i < kGroup; ++i) {
+            const int t = t0 + i;
             const bool v = t < p.n_q;
             lo_t[i] = v ? max(p.ks[t], 0) : 0;
             hi_t[i] = v ? min(p.ke[t], p.n_kv) : 0;
-            out_row[i] = p.logits + static_cast<int64_t>(v ? t : 0) * p.stride;
         }
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
+        float* const out0 = p.logits + static_cast<int64_t>(t0) * p.stride;
+        const uint32_t acc_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(eg * kN);
+        const uint32_t w_addr = base + kWOff;
+        for (int j = eg; j < n_tiles; j += 2) {
             const int s = kbase + j * kM + row;
             const float scale = s < p.n_kv ? __ldg(p.kv_scale + s) : 0.0f;
-            bar_wait(tfull(b), static_cast<uint32_t>((j >> 1) & 1), p.flags);
+            bar_wait(tfull(eg), static_cast<uint32_t>((j >> 1) & 1), p.flags);
             __syncwarp();  // the TMEM loads below are warp-collective
             tc_fence_after();
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint32_t r[64];
-                tmem_load64(lane_addr + static_cast<uint32_t>(b * kN + (qa + i) * kHeads), r);
-                const float4* wq = reinterpret_cast<const float4*>(sw + (qa + i) * kHeads);
-                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-                for (int h = 0; h < kHeads; h += 4) {
-                    const float4 wv = wq[h >> 2];
-                    a0 = fmaf(wv.x, fmaxf(__uint_as_float(r[h]), 0.0f), a0);
-                    a1 = fmaf(wv.y, fmaxf(__uint_as_float(r[h + 1]), 0.0f), a1);
-                    a2 = fmaf(wv.z, fmaxf(__uint_as_float(r[h + 2]), 0.0f), a2);
-                    a3 = fmaf(wv.w, fmaxf(__uint_as_float(r[h + 3]), 0.0f), a3);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[2 * kHeads];  // two queries, all heads, in one load
+                tmem_load128(acc_addr + static_cast<uint32_t>(half * 2 * kHeads), r);
+                if (half == 1) {  // the accumulator is in registers: hand it back to the MMAs
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(tempty(eg));
                 }
-                if (s >= lo_t[i] && s < hi_t[i]) out_row[i][s] = ((a0 + a1) + (a2 + a3)) * scale;
+                // packed fp32 pairs, w * max(d, 0) two heads an instruction, both
+                // queries interleaved (four independent accumulator chains)
+                float2 acc[2][2] = {{make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)},
+                                    {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)}};
+#pragma unroll
+                for (int e = 0; e < kHeads; e += 4) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int qi = 2 * half + i;
+                        const float4 w4 = lds_f4(w_addr + static_cast<uint32_t>((qi * kHeads + e) * 4));
+                        const uint32_t* d = r + i * kHeads + e;
+                        const float2 x0 =
+                            make_float2(fmaxf(__uint_as_float(d[0]), 0.0f), fmaxf(__uint_as_float(d[1]), 0.0f));
+                        const float2 x1 =
+                            make_float2(fmaxf(__uint_as_float(d[2]), 0.0f), fmaxf(__uint_as_float(d[3]), 0.0f));
+                        acc[i][0] = __ffma2_rn(make_float2(w4.x, w4.y), x0, acc[i][0]);
+                        acc[i][1] = __ffma2_rn(make_float2(w4.z, w4.w), x1, acc[i][1]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int qi = 2 * half + i;
+                    if (s >= lo_t[qi] && s < hi_t[qi])
+                        out0[static_cast<int64_t>(qi) * p.stride + s] =
+                            ((acc[i][0].x + acc[i][0].y) + (acc[i][1].x + acc[i][1].y)) * scale;
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(tempty(b));
         }
     }
     tc_fence_before();
@@ -365,6 +416,30 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_row
 
 constexpr int kMaxDevicesL = 64;
 bool g_logits_ready[kMaxDevicesL];
+int g_logits_sms[kMaxDevicesL];
+
+// CTAs per query group: the groups' key tiles split into `parts` contiguous
+// shares so that the CTAs (one per SM) fill their last wave: the fewest parts
+// (at most 16, and none shorter than about 8 tiles of the longest possible
+// span) whose waves are at least 90 % full, else the fullest.
+int logits_parts(int groups, int n_kv) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesL) return 1;
+    const int slots = max(g_logits_sms[dev], 1);
+    const int max_parts = max(1, min(16, n_kv / (8 * kM)));
+    int best = 1;
+    double best_fill = 0.0;
+    for (int parts = 1; parts <= max_parts; ++parts) {
+        const double waves = static_cast<double>(groups) * parts / slots;
+        const double fill = waves / std::ceil(waves);
+        if (fill >= 0.9) return parts;
+        if (fill > best_fill) {
+            best_fill = fill;
+            best = parts;
+        }
+    }
+    return best;
+}
 std::mutex g_logits_mutex;
 
 cudaError_t prepare_logits() {
@@ -376,6 +451,8 @@ cudaError_t prepare_logits() {
     if (!g_logits_ready[dev]) {
         e = cudaFuncSetAttribute(topk_indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemLogits));
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&g_logits_sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         g_logits_ready[dev] = true;
     }
@@ -410,7 +487,9 @@ extern "C" int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const fl
     prm.n_q = n_q;
     prm.n_kv = n_kv;
     prm.flags = device_flags;
-    const int grid = (n_q + kGroup - 1) / kGroup;
+    const int groups = (n_q + kGroup - 1) / kGroup;
+    prm.parts = logits_parts(groups, n_kv);
+    const int grid = groups * prm.parts;
     const cudaError_t e = launch_pdl(topk_indexer_logits_kernel, grid, kThreadsL, kSmemLogits,
                                      reinterpret_cast<cudaStream_t>(stream), tq, tkv, prm);
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;

@@ -582,6 +582,126 @@ def cpu_baselines(name, rank, budget_s):
                               "sample": f"{r1} rows in {t1:.1f} s on 1 thread"}}
 
 
+# ----------------------------------------------------------------------------- indexer logits
+
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rates (4.5 / 2.25 PFLOP/s)
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def logits_flops(w):
+    """Algorithmic FLOPs of the indexer logits: 2 * 64 * 128 per (query,
+    key) pair inside a window (the head weighting and ReLU not counted)."""
+    lens = (w["ke"].clamp(max=w["n_kv"]) - w["ks"].clamp(min=0)).clamp(min=0)
+    return float(lens.to(torch.float64).sum()) * 2 * topk.TOPK_INDEXER_HEADS * topk.TOPK_INDEXER_DIM
+
+
+def logits_cpu_baseline(budget_s):
+    """The oracle's indexer logits, as it stands, on a bounded sample of the
+    extend chunk: query rows 0, 1, ... over the first 256 keys of their
+    windows, repeated until the budget has passed (one thread)."""
+    import numpy as np
+
+    import oracle
+    w = wl.indexer_extend("cpu", 0)
+    q, kv = w["q"].numpy(), w["kv"].numpy()
+    scale, wt = w["kv_scale"].numpy(), w["weights"].numpy()
+    ks = w["ks"].numpy()
+    pairs, t0, i = 0, time.perf_counter(), 0
+    out = np.zeros((1, w["stride"]), np.float32)
+    while True:
+        t = i % w["n_q"]
+        lo = int(ks[t])
+        oracle.indexer_logits(q[t:t + 1], kv, scale, wt[t:t + 1], [lo], [lo + 256], out)
+        pairs += 256
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            flops = pairs * 2.0 * topk.TOPK_INDEXER_HEADS * topk.TOPK_INDEXER_DIM
+            return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                    "sample": f"{i} query rows x 256 keys of the extend chunk's windows in {el:.1f} s on 1 thread "
+                              f"({pairs / el:.0f} logits/s)"}
+
+
+def measure_logits(steps, warmup, stream, flush):
+    """The indexer logits of one extend chunk (1024 queries over their
+    windows of 28673..29696 keys in the 131072-key flattened KV), alone and
+    fed straight into the RAGGED top-k of the same rows (plan + transform
+    after it on the stream; the chunk's logits, 122 MB written, are read back
+    mostly from L2). Both timed as CUDA graphs of `steps` repetitions, the L2
+    flushed before each replay."""
+    w = wl.indexer_extend("cuda", 0)
+    stride, n_q = w["stride"], w["n_q"]
+    logits = torch.full((n_q, stride), wl.SENTINEL, dtype=torch.float32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flops = logits_flops(w)
+
+    def produce():
+        topk.topk_indexer_logits(w["q"], w["kv"], w["kv_scale"], w["weights"], w["ks"], w["ke"], logits, stride,
+                                 flags)
+
+    tw = dict(mode="ragged", k=2048, scores=logits, score_stride=stride, row_starts=w["ks"],
+              seq_lens=(w["ke"] - w["ks"]).to(torch.int32), out_offsets=w["ks"], page_table=None,
+              page_table_stride=0, page_size=1, batch=n_q, name="indexer logits -> top-k")
+    ln = Launch(tw)
+    for _ in range(warmup):
+        produce()
+        ln.plan(stream)
+        ln.transform(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for chain in (False, True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(steps):
+                produce()
+                if chain:
+                    ln.plan(None)
+                    ln.transform(None)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    times = []
+    for g in graphs:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        flush(stream)
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        g.replay()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[1]) / 1e3 / steps)
+    assert int(flags.item()) == 0, "a bounded wait in the logits kernel gave up"
+    t_logits, t_chain = times
+    bf16, kind = measured_bf16_tflops()
+    peak = bf16 * FP8_PER_BF16
+    achieved = flops / t_logits / 1e12
+    del graphs
+    return {
+        "workload": "indexer logits (FP8 E4M3 q [1024, 64, 128], kv [131072, 128], fp32 head weights) of one "
+                    "RAGGED extend chunk: query i of request r over keys [32768 r, 32768 r + 28673 + i); then the "
+                    "RAGGED top-k (k = 2048) of the same rows",
+        "tflops": achieved,
+        "us_per_launch": 1e6 * t_logits,
+        "flops_per_launch": flops,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "dtype": "fp8 e4m3 (fp32 accumulate)", "traffic": None,
+                     "peak_kind": f"{kind} bf16 burst x {FP8_PER_BF16} (nominal fp8/bf16 ratio)",
+                     "kernel": "topk_indexer_logits_kernel (tcgen05.mma kind::f8f6f4, TMEM accumulators, TMA)"},
+        "chain_us_per_step": 1e6 * t_chain,
+        "chain_rows_per_s": n_q / t_chain,
+        "chain": "logits -> plan -> RAGGED transform per step (3 launches, programmatic dependent launch)",
+        "launches_per_step": 1,
+        "l2": "inputs 25 MB (the 16.8 MB KV is meant to stay in L2: every query of a request reads it); "
+              "output 512 MB buffer > 2 x L2; L2 flushed before each timed replay",
+    }
+
+
 # ----------------------------------------------------------------------------- main
 
 def run_reference(args, world, rank):
@@ -650,7 +770,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-configs", action="store_true", help="headline workload only")
-    ap.add_argument("--workload", default=HEADLINE, help="the workload of a --quick run")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="the workload of a --quick run (a top-k workload, or indexer_logits)")
     ap.add_argument("--quick", action="store_true",
                     help="one workload only: device timings, no e2e, no CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=1.5, help="oracle time budget per config and thread count")
@@ -670,6 +791,12 @@ def main():
     flush = L2Flush(l2)
 
     name = args.workload if args.quick else HEADLINE
+    if args.quick and name == "indexer_logits":
+        with ClockSampler(local) as clocks:
+            res = measure_logits(args.steps, args.warmup, stream, flush)
+        if rank == 0:
+            print(json.dumps({"workload": name, **res, "clocks": clocks.summary()}), flush=True)
+        return
     with ClockSampler(local) as clocks:
         head = measure(name, args.steps, args.warmup, world, rank, stream, peak, l2, flush)
     clk = clocks.summary()
@@ -691,6 +818,11 @@ def main():
             extra[cname]["workload"] = DESCRIPTIONS[cname]
             if rank == 0 and world == 1:
                 extra[cname]["cpu_baseline"] = cpu_baselines(cname, rank, args.cpu_seconds)
+
+    if not args.no_configs and world == 1:
+        extra["indexer_logits"] = measure_logits(args.steps, args.warmup, stream, flush)
+        if rank == 0:
+            extra["indexer_logits"]["cpu_baseline"] = logits_cpu_baseline(args.cpu_seconds)
 
     if rank == 0:
         achieved = head["gbs_transform"]

@@ -67,25 +67,31 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
-    """First 16 hex digits of the SHA-256 of the kernel sources, concatenated."""
+LOGITS_SRCS = [os.path.join(ROOT, "sparse_attention_top_row_gb300", "csrc", f)
+               for f in ("topk_logits.cu", "topk_common.cuh")]
+
+
+def kernel_source_hash(srcs=None):
+    """First 16 hex digits of the SHA-256 of the kernel sources, concatenated
+    (the selection kernels' by default)."""
     h = hashlib.sha256()
-    for path in KERNEL_SRCS:
+    for path in srcs or KERNEL_SRCS:
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload):
+def profiled_traffic(kernel, workload, srcs=None):
     """DRAM bytes (read + written) per launch of `kernel` on `workload` from
     the committed ncu record ``profiles/<kernel>_<workload>.json``, if that
-    record was taken on the current kernel source; else None."""
+    record was taken on the current kernel source (`srcs`, the selection
+    kernels' by default); else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash(srcs):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -690,7 +696,9 @@ def measure_logits(steps, warmup, stream, flush):
         "us_per_launch": 1e6 * t_logits,
         "flops_per_launch": flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "dtype": "fp8 e4m3 (fp32 accumulate)", "traffic": None,
+                     "frac": achieved / peak, "dtype": "fp8 e4m3 (fp32 accumulate)",
+                     "traffic": profiled_traffic("topk_indexer_logits_kernel", "indexer_logits_extend_chunk",
+                                                 LOGITS_SRCS),
                      "peak_kind": f"{kind} bf16 burst x {FP8_PER_BF16} (nominal fp8/bf16 ratio)",
                      "kernel": "topk_indexer_logits_kernel (tcgen05.mma kind::f8f6f4, TMEM accumulators, TMA)"},
         "chain_us_per_step": 1e6 * t_chain,

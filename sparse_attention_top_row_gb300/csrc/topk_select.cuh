@@ -1739,6 +1739,74 @@ __device__ __forceinline__ uint32_t fine_bin16(uint32_t key16, uint32_t base16) 
     return min(key16 - base16, static_cast<uint32_t>(kSmall - 1));
 }
 
+// The compact finish when the threshold lies above the count pass's window
+// of 255 prefixes over the bound (the bound many 16-bit prefix steps below
+// the k-th score, as when the scores straddle zero or span many octaves):
+// every winner is then a member of the top bin. The members' keys are read
+// back from global memory (L2) and their 16-bit prefixes kept in the entries
+// (the other entries get prefix 0; every member's is at least base16 + 255).
+// Windows then narrow onto the threshold: bin 0 below `lo`, bin 1 + i the
+// prefixes lo + (i << sh) .., bin 255 the rest above. The first window spans
+// every member; each next one spans the previous threshold bin, until that
+// bin is one prefix wide or holds at most kMaxRankTies members (the tie
+// ranking reads full keys). On return the entries hold their bins and the
+// per-warp histograms the last window's counts, as after the count pass.
+// Every thread calls (the caller's condition is the same on every thread).
+__device__ Threshold rebin_top(uint32_t* lp, uint32_t n, uint32_t base16, uint32_t k, int32_t tbase, const float* w,
+                               uint32_t* whw, const Shared& sh) {
+    const uint32_t* const wbits = reinterpret_cast<const uint32_t*>(w);
+    constexpr uint32_t kTop = kSmall - 1, kWide = kSmall - 2;
+    uint32_t hi = 0;
+    for (uint32_t s = 0; s < n; ++s) {
+        uint32_t e = lp[s * kThreads];
+        if ((e >> 16) == kTop) {
+            const uint32_t p16 = bits_key(__ldg(wbits + entry_pos(e, tbase))) >> 16;
+            hi = max(hi, p16);
+            e = (p16 << 16) | (e & 0xFFFFu);
+        } else {
+            e &= 0xFFFFu;
+        }
+        lp[s * kThreads] = e;
+    }
+    hi = __reduce_max_sync(kFull, hi);
+    if (lane_id() == 0) atomicMax(&sh.cnt()[4], hi);
+    __syncthreads();
+    uint32_t lo = base16 + kTop;
+    uint32_t span = sh.cnt()[4] - lo;  // the members' prefixes lie in [lo, lo + span]
+    uint32_t shift = 0;
+    while ((span >> shift) >= kWide) ++shift;
+    Threshold t{0u, 0u, 0u, false};
+    for (int pass = 0; pass < 4; ++pass) {
+        clear_words(sh.whist(), kWarps * kSmall);
+        __syncthreads();
+        for (uint32_t s = 0; s < n; ++s) {
+            const uint32_t p16 = lp[s * kThreads] >> 16;
+            if (p16 >= lo) atomicAdd(&whw[1u + min((p16 - lo) >> shift, kWide)], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
+        __syncthreads();
+        t = find_threshold(sh.hist(), kSmall, k, sh);
+        if (!t.found || t.bin == 0u || t.bin == kTop) {  // (cannot happen: the members number at least k)
+            t.found = false;
+            return t;
+        }
+        if (shift == 0u || t.count <= static_cast<uint32_t>(kMaxRankTies)) break;
+        lo += (t.bin - 1u) << shift;
+        span = (1u << shift) - 1u;
+        shift = 0;
+        while ((span >> shift) >= kWide) ++shift;
+    }
+    if (shift != 0u && t.count > static_cast<uint32_t>(kMaxRankTies)) t.found = false;
+    for (uint32_t s = 0; s < n; ++s) {
+        const uint32_t e = lp[s * kThreads];
+        const uint32_t p16 = e >> 16;
+        const uint32_t bin = p16 >= lo ? 1u + min((p16 - lo) >> shift, kWide) : 0u;
+        lp[s * kThreads] = (bin << 16) | (e & 0xFFFFu);
+    }
+    return t;
+}
+
 // The fast finish over the compact lists (n_raw: this thread's appends, more
 // than kListCap meaning its list overflowed); w: the window's scores, for
 // the threshold bin's full keys. As finish_solo, except that a threshold bin
@@ -1780,7 +1848,9 @@ __device__ __forceinline__ FinishResult finish_list(uint32_t bound_key, uint32_t
     if (__syncthreads_or(ovf)) return kNeedExact;
     if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
     __syncthreads();
-    const Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    const int32_t tbase = 4 * static_cast<int32_t>(threadIdx.x) - rem;
+    if (t.found && t.bin == static_cast<uint32_t>(kSmall - 1)) t = rebin_top(lp, n, base16, k, tbase, w, whw, sh);
     if (!t.found || t.bin == static_cast<uint32_t>(kSmall - 1)) return kNeedExact;
     const uint32_t need = k - t.above;
     const bool exact = t.count == need;
@@ -1791,7 +1861,6 @@ __device__ __forceinline__ FinishResult finish_list(uint32_t bound_key, uint32_t
     const uint32_t tau = t.bin;
     // bins above the threshold bin, and the threshold bin itself when exact
     const uint32_t lowest = exact ? tau : tau + 1u;
-    const int32_t tbase = 4 * static_cast<int32_t>(threadIdx.x) - rem;
     const TieList ties = tie_list(sh.ties());
     __syncthreads();  // the warps' counts
     uint32_t slot = 0;

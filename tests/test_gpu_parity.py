@@ -597,3 +597,53 @@ def test_row_beyond_the_compact_index(cuda_lib):
              out_offsets=torch.arange(B, dtype=torch.int32), page_table=None, page_table_stride=0,
              page_size=1, batch=B)
     check_full(cuda_lib, w)
+
+
+# ---------------------------------------------------------------- thresholds far above the sample bound
+
+def _far_threshold_rows(batch, length, seed):
+    """Rows whose k-th score lies many 16-bit prefix steps above the sample's
+    bound: (a) ~28 K scores in [1e-7, 1e-6) with 2300 in [0.5, 1) at random
+    places, (b) N(-0.447, 0.3), whose k-th largest (k = 2048) sits near 0 so
+    that the bound falls among the negative scores, (c) N(0, 1) rows."""
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for b in range(batch):
+        kind = b % 3
+        if kind == 0:
+            r = 1e-7 + 9e-7 * torch.rand(length, generator=g)
+            idx = torch.randperm(length, generator=g)[:2300]
+            r[idx] = 0.5 + 0.5 * torch.rand(2300, generator=g)
+        elif kind == 1:
+            r = -0.447 + 0.3 * torch.randn(length, generator=g)
+        else:
+            r = torch.randn(length, generator=g)
+        rows.append(r)
+    scores = torch.stack(rows).to(torch.float32).contiguous()
+    B = batch
+    return dict(mode="ragged", k=2048, scores=scores.reshape(-1), score_stride=length, row_starts=None,
+                seq_lens=torch.full((B,), length, dtype=torch.int32),
+                out_offsets=(torch.arange(B, dtype=torch.int32) * length).contiguous(), page_table=None,
+                page_table_stride=0, page_size=1, batch=B, name=f"far thresholds B={B}")
+
+
+@pytest.mark.parametrize("batch", [200, 100])
+def test_threshold_far_above_the_bound(cuda_lib, batch):
+    """Rows whose threshold lies beyond the compact finish's first window of
+    255 prefixes over the bound are finished by re-binning the top bin's
+    members from their keys (no exact path), and match the oracle: the
+    256-thread rows kernel (200 rows) and the 512-thread one (100 rows)."""
+    w = _far_threshold_rows(batch, 30000, seed=31 + batch)
+    hw = HostWorkload(w)
+    ref_out, ref_raw, err = oracle.run_workload(w)
+    assert err == 0
+    d = wl.to_device(w, "cuda")
+    for flags in (DET, 0):
+        out = torch.full((batch, 2048), CANARY, dtype=torch.int32, device="cuda")
+        out_raw = torch.full((batch, 2048), CANARY, dtype=torch.int32, device="cuda")
+        _, _, ws = cuda_lib.run_workload(d, out=out, out_raw=out_raw, flags=flags)
+        torch.cuda.synchronize()
+        hdr = ws[:64].cpu().numpy().view(np.uint32)
+        assert hdr[7] == 0, f"{hdr[7]} rows took the exact path"
+        compare_with_oracle(hw, out.cpu().numpy(), out_raw.cpu().numpy(), ref_out, ref_raw,
+                            deterministic=flags == DET)

@@ -277,10 +277,11 @@ __global__ void __launch_bounds__(kThreadsL, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp >= 2) {  // the group's head weights (0 for queries past n_q)
+    if (warp >= 2) {  // the group's head weights (0 for queries past n_q; odd heads halved, see the readout)
         const int e = static_cast<int>(threadIdx.x) - 64;
         const int t = t0 + (e >> 6);
-        sw[e] = t < p.n_q ? p.weights[static_cast<int64_t>(t) * kHeads + (e & 63)] : 0.0f;
+        const float wt = t < p.n_q ? p.weights[static_cast<int64_t>(t) * kHeads + (e & 63)] : 0.0f;
+        sw[e] = (e & 1) ? 0.5f * wt : wt;
     }
     tc_fence_before();
     __syncthreads();
@@ -361,10 +362,12 @@ __global__ void __launch_bounds__(kThreadsL, 1)
                         const int qi = 2 * half + i;
                         const float4 w4 = lds_f4(w_addr + static_cast<uint32_t>((qi * kHeads + e) * 4));
                         const uint32_t* d = r + i * kHeads + e;
-                        const float2 x0 =
-                            make_float2(fmaxf(__uint_as_float(d[0]), 0.0f), fmaxf(__uint_as_float(d[1]), 0.0f));
-                        const float2 x1 =
-                            make_float2(fmaxf(__uint_as_float(d[2]), 0.0f), fmaxf(__uint_as_float(d[3]), 0.0f));
+                        // even heads: max(x, 0) (ALU pipe); odd heads: x + |x| = 2 max(x, 0),
+                        // exactly, on the FMA pipe, against halved weights: the same
+                        // products, the two pipes sharing the ReLUs
+                        const float a1 = __uint_as_float(d[1]), a3 = __uint_as_float(d[3]);
+                        const float2 x0 = make_float2(fmaxf(__uint_as_float(d[0]), 0.0f), a1 + fabsf(a1));
+                        const float2 x1 = make_float2(fmaxf(__uint_as_float(d[2]), 0.0f), a3 + fabsf(a3));
                         acc[i][0] = __ffma2_rn(make_float2(w4.x, w4.y), x0, acc[i][0]);
                         acc[i][1] = __ffma2_rn(make_float2(w4.z, w4.w), x1, acc[i][1]);
                     }

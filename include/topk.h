@@ -265,7 +265,7 @@ TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride
  *                16-byte aligned.
  *   kv           device, [n_kv, 128] E4M3 codes, row-major, 16-byte aligned.
  *   kv_scale     device fp32 [n_kv].
- *   weights      device fp32 [n_q, 64], row-major.
+ *   weights      device fp32 [n_q, 64], row-major, 16-byte aligned.
  *   ks, ke       device int32 [n_q]: each query's key window (clamped to
  *                [0, n_kv); ke <= ks: an empty row, nothing written).
  *   n_q          queries, 0 .. TOPK_INDEXER_MAX_QUERIES.
@@ -276,7 +276,7 @@ TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride
  *                in if a wait on the kernel's own copies or MMAs gave up
  *                (the result is then unreliable); the caller zeroes it.
  * Status: TOPK_ERR_ARG for a negative count or stride, n_q above the
- * maximum, or a null pointer; TOPK_ERR_ALIGN for q or kv off 16 bytes;
+ * maximum, or a null pointer; TOPK_ERR_ALIGN for q, kv or weights off 16 bytes;
  * TOPK_ERR_CUDA for a failed launch or tensor-map encoding. n_q == 0 or
  * n_kv == 0 is TOPK_OK and enqueues nothing. One launch, with programmatic
  * dependent launch like every kernel of the library.

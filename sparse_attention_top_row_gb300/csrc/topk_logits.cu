@@ -13,21 +13,24 @@
 // TMEM) put upstream of the top-k; row t of the result is the RAGGED
 // transform's window at row_start = ks[t], seq_len = ke[t] - ks[t].
 //
-// Mapping. A CTA takes a group of kGroup = 4 consecutive queries and a
+// Mapping. A work unit is a group of kGroup = 4 consecutive queries and a
 // contiguous share of the group's key tiles (the host splits each group into
-// `parts` shares so that the CTAs, one per SM, fill their last wave). The 4 x
-// 64 head vectors (256 rows of 128 bytes) are the MMA's B operand, loaded
-// once; the keys stream through a ring of kStages shared-memory stages, 128
-// keys (16 KB) a stage, as the A operand. One tile
+// `parts` shares so that the units fill the persistent CTAs, one per SM,
+// evenly). The unit's 4 x 64 head vectors (256 rows of 128 bytes) are the
+// MMA's B operand, loaded once per unit (double-buffered: the next unit's
+// while this one's keys stream); the keys stream through a ring of kStages
+// shared-memory stages, 128 keys (16 KB) a stage, as the A operand. One tile
 // D = KV_tile . Q^T has M = 128 keys (TMEM lanes), N = 256 (query, head)
 // columns and K = 128 (four kind::f8f6f4 MMAs of K = 32), so each epilogue
 // thread owns one key and finds all 64 heads of a query in its own TMEM
 // lane: the head sum needs no exchange between threads. Two accumulators
 // (2 x 256 TMEM columns) let the MMAs of tile j + 1 run while tile j is read
-// out. Shared memory (about 130 KB) keeps one CTA per SM, so the CTA's
+// out. Shared memory (about 163 KB) keeps one CTA per SM, so the CTA's
 // 512-column TMEM allocation never waits.
 //
-// Warp roles (10 warps): one thread of warp 0 issues the TMA loads; warp 1
+// Warp roles (10 warps): one thread of warp 0 walks the CTA's units, hands
+// each to the others as a record in shared memory and issues the TMA loads
+// (query tile, head weights, key tiles); warp 1
 // owns the TMEM allocation and one of its threads issues the MMAs (a single
 // thread issuing both was the bottleneck: each step of its loop waits);
 // warps 2..9 read the accumulators out. A warp reaches TMEM lanes
@@ -68,10 +71,12 @@ constexpr int kThreadsL = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 2 * kN;      // two accumulators
 constexpr uint32_t kQBytes = kN * kDim;     // 32 KB
 constexpr uint32_t kTileBytes = kM * kDim;  // 16 KB
-constexpr uint32_t kKvOff = kQBytes;
+constexpr uint32_t kWBytes = kN * 4;       // a group's head weights, fp32
+constexpr uint32_t kKvOff = 2 * kQBytes;   // two query tiles (this unit's and the next)
 constexpr uint32_t kWOff = kKvOff + kStages * kTileBytes;
-constexpr uint32_t kBarOff = kWOff + kN * 4;
-constexpr int kBars = 2 * kStages + 1 + 2 + 2;  // full, empty, q, tmem full, tmem empty
+constexpr uint32_t kRecOff = kWOff + 2 * kWBytes;  // two unit records (UnitRec)
+constexpr uint32_t kBarOff = kRecOff + 2 * 64;
+constexpr int kBars = 2 * kStages + 2 + 2 + 2 + 2;  // full, empty, q full, q free, tmem full, tmem empty
 constexpr uint32_t kSlotOff = kBarOff + kBars * 8;
 constexpr size_t kSmemLogits = kSlotOff + 16 + 1024;  // + alignment slack (tiles on 1024 B)
 static_assert(kSmemLogits > 114 * 1024, "one CTA per SM (its TMEM allocation is the whole TMEM)");
@@ -211,37 +216,36 @@ struct LogitsParams {
     int64_t stride;
     int32_t n_q;
     int32_t n_kv;
-    int32_t parts;  // CTAs per query group, each a contiguous share of the group's key tiles
+    int32_t parts;  // work units per query group, each a contiguous share of the group's key tiles
+    int32_t units;  // query groups x parts
     uint32_t* flags;
 };
 
-__global__ void __launch_bounds__(kThreadsL, 1)
-    topk_indexer_logits_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
-                               const __grid_constant__ LogitsParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = cvta_smem(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* const sm = smem_raw + (base - raw);
-    float* const sw = reinterpret_cast<float*>(sm + kWOff);
-    const uint32_t bars = base + kBarOff;
-    auto full = [&](int s) { return bars + 8u * static_cast<uint32_t>(s); };
-    auto empty = [&](int s) { return bars + 8u * static_cast<uint32_t>(kStages + s); };
-    const uint32_t qfull = bars + 8u * (2 * kStages);
-    auto tfull = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 1 + b); };
-    auto tempty = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 3 + b); };
-    uint32_t* const slot = reinterpret_cast<uint32_t*>(sm + kSlotOff);
+// One work unit: queries t0 .. t0 + 3 over key tiles kbase + 128 j, j < n_tiles.
+struct Unit {
+    int t0, kbase, n_tiles;
+};
 
-    const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31u);
-    grid_dependency_wait();
-    const int group = static_cast<int>(blockIdx.x) / p.parts, part = static_cast<int>(blockIdx.x) % p.parts;
+// A unit as the producer hands it to the MMA issuer and the readout warps
+// (in shared memory, next to the unit's query tile): n_tiles == 0 ends the
+// sequence; lo/hi: each query's window clamped to [0, n_kv) (empty past n_q).
+struct UnitRec {
+    int t0, kbase, n_tiles, pad;
+    int lo[kGroup], hi[kGroup];
+};
+static_assert(sizeof(UnitRec) <= 64, "unit record");
+
+// Unit u: query group u / parts, share u % parts of the group's key span
+// (the union of its queries' windows, from the tile holding its first key).
+__device__ __forceinline__ Unit unit_of(const LogitsParams& p, int u) {
+    const int group = u / p.parts, part = u % p.parts;
     const int t0 = group * kGroup;
-    // the group's key span (the same on every thread), then this CTA's share of its tiles
     int lo = INT_MAX, hi = 0;
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
         const int t = t0 + i;
         if (t < p.n_q) {
-            const int a = max(p.ks[t], 0), b = min(p.ke[t], p.n_kv);
+            const int a = max(__ldg(p.ks + t), 0), b = min(__ldg(p.ke + t), p.n_kv);
             if (a < b) {
                 lo = min(lo, a);
                 hi = max(hi, b);
@@ -251,20 +255,42 @@ __global__ void __launch_bounds__(kThreadsL, 1)
     const int kbase0 = lo & ~(kM - 1);
     const int group_tiles = lo < hi ? (hi - kbase0 + kM - 1) / kM : 0;
     const int per_part = (group_tiles + p.parts - 1) / p.parts;
-    const int n_tiles = max(0, min(per_part, group_tiles - part * per_part));
-    if (n_tiles == 0) {
-        allow_dependents();
-        return;
-    }
-    const int kbase = kbase0 + part * per_part * kM;
+    return Unit{t0, kbase0 + part * per_part * kM, max(0, min(per_part, group_tiles - part * per_part))};
+}
 
+// Persistent: CTA c takes units c, c + gridDim.x, ... in turn (every role
+// walks the same sequence and skips the same empty units). Tiles are counted
+// over the CTA's whole sequence, so the stage ring and the two accumulators
+// run on across units; the query tile and head weights are double-buffered
+// by unit, the next unit's loaded while this one's keys stream.
+__global__ void __launch_bounds__(kThreadsL, 1)
+    topk_indexer_logits_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
+                               const __grid_constant__ LogitsParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = cvta_smem(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const sm = smem_raw + (base - raw);
+    const uint32_t bars = base + kBarOff;
+    auto full = [&](int s) { return bars + 8u * static_cast<uint32_t>(s); };
+    auto empty = [&](int s) { return bars + 8u * static_cast<uint32_t>(kStages + s); };
+    auto qfull = [&](int q) { return bars + 8u * static_cast<uint32_t>(2 * kStages + q); };
+    auto qfree = [&](int q) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 2 + q); };
+    auto tfull = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 4 + b); };
+    auto tempty = [&](int b) { return bars + 8u * static_cast<uint32_t>(2 * kStages + 6 + b); };
+    auto qtile = [&](int q) { return base + static_cast<uint32_t>(q) * kQBytes; };
+    auto wtile = [&](int q) { return base + kWOff + static_cast<uint32_t>(q) * kWBytes; };
+    uint32_t* const slot = reinterpret_cast<uint32_t*>(sm + kSlotOff);
+
+    const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31u);
+    grid_dependency_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             bar_init(full(s), 1);
             bar_init(empty(s), 1);
         }
-        bar_init(qfull, 1);
         for (int b = 0; b < 2; ++b) {
+            bar_init(qfull(b), 1);
+            bar_init(qfree(b), kEpiWarps);
             bar_init(tfull(b), 1);
             bar_init(tempty(b), kEpiWarps / 2);
         }
@@ -277,109 +303,143 @@ __global__ void __launch_bounds__(kThreadsL, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp >= 2) {  // the group's head weights (0 for queries past n_q; odd heads halved, see the readout)
-        const int e = static_cast<int>(threadIdx.x) - 64;
-        const int t = t0 + (e >> 6);
-        const float wt = t < p.n_q ? p.weights[static_cast<int64_t>(t) * kHeads + (e & 63)] : 0.0f;
-        sw[e] = (e & 1) ? 0.5f * wt : wt;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
+    const int u0 = static_cast<int>(blockIdx.x), du = static_cast<int>(gridDim.x);
 
     if (warp == 0) {
-        if (lane == 0) {  // TMA producer
-            bar_expect_tx(qfull, kQBytes);
-            tma_load_2d(base, &tq, 0, t0 * kHeads, qfull);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages) bar_wait(empty(s), static_cast<uint32_t>((j / kStages) & 1) ^ 1u, p.flags);
-                bar_expect_tx(full(s), kTileBytes);
-                tma_load_2d(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes, &tkv, 0, kbase + j * kM, full(s));
+        if (lane == 0) {  // TMA producer: per unit its record, query tile and weights, then its key tiles
+            int g = 0, nu = 0;
+            for (int u = u0;; u += du) {
+                const Unit un = u < p.units ? unit_of(p, u) : Unit{0, 0, 0};
+                if (u < p.units && un.n_tiles == 0) continue;
+                const int q = nu & 1;
+                if (nu >= 2) bar_wait(qfree(q), static_cast<uint32_t>((nu >> 1) & 1) ^ 1u, p.flags);
+                UnitRec* const rec = reinterpret_cast<UnitRec*>(sm + kRecOff) + q;
+                rec->t0 = un.t0;
+                rec->kbase = un.kbase;
+                rec->n_tiles = un.n_tiles;
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i) {
+                    const int t = un.t0 + i;
+                    const bool v = un.n_tiles > 0 && t < p.n_q;
+                    rec->lo[i] = v ? max(__ldg(p.ks + t), 0) : 0;
+                    rec->hi[i] = v ? min(__ldg(p.ke + t), p.n_kv) : 0;
+                }
+                if (un.n_tiles == 0) {  // the end: the record alone (the arrival publishes it)
+                    bar_arrive(qfull(q));
+                    break;
+                }
+                const uint32_t wbytes = static_cast<uint32_t>(min(kGroup, p.n_q - un.t0)) * (kHeads * 4);
+                bar_expect_tx(qfull(q), kQBytes + wbytes);  // (its arrival publishes the record)
+                tma_load_2d(qtile(q), &tq, 0, un.t0 * kHeads, qfull(q));
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 wtile(q)),
+                             "l"(p.weights + static_cast<int64_t>(un.t0) * kHeads), "r"(wbytes), "r"(qfull(q))
+                             : "memory");
+                for (int j = 0; j < un.n_tiles; ++j, ++g) {
+                    const int s = g % kStages;
+                    if (g >= kStages) bar_wait(empty(s), static_cast<uint32_t>((g / kStages) & 1) ^ 1u, p.flags);
+                    bar_expect_tx(full(s), kTileBytes);
+                    tma_load_2d(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes, &tkv, 0, un.kbase + j * kM, full(s));
+                }
+                ++nu;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer
-            bar_wait(qfull, 0, p.flags);
-            const uint64_t bdesc = sw128_desc(base);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % kStages, b = j & 1;
-                bar_wait(full(s), static_cast<uint32_t>((j / kStages) & 1), p.flags);
-                if (j >= 2) bar_wait(tempty(b), static_cast<uint32_t>((j >> 1) & 1) ^ 1u, p.flags);
-                tc_fence_after();
-                const uint64_t adesc = sw128_desc(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes);
-                const uint32_t d = tmem + static_cast<uint32_t>(b * kN);
+            int g = 0;
+            for (int nu = 0;; ++nu) {
+                const int q = nu & 1;
+                bar_wait(qfull(q), static_cast<uint32_t>((nu >> 1) & 1), p.flags);
+                const int n_tiles = reinterpret_cast<const volatile UnitRec*>(sm + kRecOff)[q].n_tiles;
+                if (n_tiles == 0) break;
+                const uint64_t bdesc = sw128_desc(qtile(q));
+                for (int j = 0; j < n_tiles; ++j, ++g) {
+                    const int s = g % kStages, b = g & 1;
+                    bar_wait(full(s), static_cast<uint32_t>((g / kStages) & 1), p.flags);
+                    if (g >= 2) bar_wait(tempty(b), static_cast<uint32_t>((g >> 1) & 1) ^ 1u, p.flags);
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(base + kKvOff + static_cast<uint32_t>(s) * kTileBytes);
+                    const uint32_t d = tmem + static_cast<uint32_t>(b * kN);
 #pragma unroll
-                for (int kk = 0; kk < kDim / kMmaK; ++kk)
-                    mma_f8(d, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), kk > 0 ? 1u : 0u);
-                mma_commit(empty(s));
-                mma_commit(tfull(b));
+                    for (int kk = 0; kk < kDim / kMmaK; ++kk)
+                        mma_f8(d, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk),
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(empty(s));
+                    mma_commit(tfull(b));
+                }
             }
             // the last tile's MMAs are complete before the TMEM is released
-            const int jl = n_tiles - 1;
-            bar_wait(tfull(jl & 1), static_cast<uint32_t>((jl >> 1) & 1), p.flags);
+            if (g > 0) bar_wait(tfull((g - 1) & 1), static_cast<uint32_t>(((g - 1) >> 1) & 1), p.flags);
         }
         __syncwarp();
     } else {  // epilogue: one key per thread, the four queries of every other tile
         const int quarter = warp & 3;
-        const int eg = (warp - 2) >> 2;  // epilogue group: tiles j with j % 2 == eg, accumulator eg
+        const int eg = (warp - 2) >> 2;  // epilogue group: tiles g with g % 2 == eg, accumulator eg
         const int row = quarter * 32 + lane;
-        int lo_t[kGroup], hi_t[kGroup];
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i) {
-            const int t = t0 + i;
-            const bool v = t < p.n_q;
-            lo_t[i] = v ? max(p.ks[t], 0) : 0;
-            hi_t[i] = v ? min(p.ke[t], p.n_kv) : 0;
-        }
-        float* const out0 = p.logits + static_cast<int64_t>(t0) * p.stride;
         const uint32_t acc_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(eg * kN);
-        const uint32_t w_addr = base + kWOff;
-        for (int j = eg; j < n_tiles; j += 2) {
-            const int s = kbase + j * kM + row;
-            const float scale = s < p.n_kv ? __ldg(p.kv_scale + s) : 0.0f;
-            bar_wait(tfull(eg), static_cast<uint32_t>((j >> 1) & 1), p.flags);
-            __syncwarp();  // the TMEM loads below are warp-collective
-            tc_fence_after();
+        int g = 0;
+        for (int nu = 0;; ++nu) {
+            const int q = nu & 1;
+            bar_wait(qfull(q), static_cast<uint32_t>((nu >> 1) & 1), p.flags);  // the unit's record and weights
+            __syncwarp();
+            const UnitRec un = reinterpret_cast<const UnitRec*>(sm + kRecOff)[q];
+            if (un.n_tiles == 0) break;
+            const int* const lo_t = un.lo;
+            const int* const hi_t = un.hi;
+            float* const out0 = p.logits + static_cast<int64_t>(un.t0) * p.stride;
+            const uint32_t w_addr = wtile(q);
+            for (int j = 0; j < un.n_tiles; ++j, ++g) {
+                if ((g & 1) != eg) continue;
+                const int s = un.kbase + j * kM + row;
+                const float scale = s < p.n_kv ? __ldg(p.kv_scale + s) : 0.0f;
+                bar_wait(tfull(eg), static_cast<uint32_t>((g >> 1) & 1), p.flags);
+                __syncwarp();  // the TMEM loads below are warp-collective
+                tc_fence_after();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[2 * kHeads];  // two queries, all heads, in one load
-                tmem_load128(acc_addr + static_cast<uint32_t>(half * 2 * kHeads), r);
-                if (half == 1) {  // the accumulator is in registers: hand it back to the MMAs
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) bar_arrive(tempty(eg));
-                }
-                // packed fp32 pairs, w * max(d, 0) two heads an instruction, both
-                // queries interleaved (four independent accumulator chains)
-                float2 acc[2][2] = {{make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)},
-                                    {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)}};
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[2 * kHeads];  // two queries, all heads, in one load
+                    tmem_load128(acc_addr + static_cast<uint32_t>(half * 2 * kHeads), r);
+                    if (half == 1) {  // the accumulator is in registers: hand it back to the MMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) bar_arrive(tempty(eg));
+                    }
+                    // packed fp32 pairs, w * max(d, 0) two heads an instruction, both
+                    // queries interleaved (four independent accumulator chains)
+                    float2 acc[2][2] = {{make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)},
+                                        {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)}};
 #pragma unroll
-                for (int e = 0; e < kHeads; e += 4) {
+                    for (int e = 0; e < kHeads; e += 4) {
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int qi = 2 * half + i;
+                            const float4 w4 = lds_f4(w_addr + static_cast<uint32_t>((qi * kHeads + e) * 4));
+                            const uint32_t* d = r + i * kHeads + e;
+                            // even heads: max(x, 0) (ALU pipe); odd heads: x + |x| = 2 max(x, 0),
+                            // exactly, on the FMA pipe (their sums are halved at the end): the
+                            // two pipes share the ReLUs
+                            const float a1 = __uint_as_float(d[1]), a3 = __uint_as_float(d[3]);
+                            const float2 x0 = make_float2(fmaxf(__uint_as_float(d[0]), 0.0f), a1 + fabsf(a1));
+                            const float2 x1 = make_float2(fmaxf(__uint_as_float(d[2]), 0.0f), a3 + fabsf(a3));
+                            acc[i][0] = __ffma2_rn(make_float2(w4.x, w4.y), x0, acc[i][0]);
+                            acc[i][1] = __ffma2_rn(make_float2(w4.z, w4.w), x1, acc[i][1]);
+                        }
+                    }
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const int qi = 2 * half + i;
-                        const float4 w4 = lds_f4(w_addr + static_cast<uint32_t>((qi * kHeads + e) * 4));
-                        const uint32_t* d = r + i * kHeads + e;
-                        // even heads: max(x, 0) (ALU pipe); odd heads: x + |x| = 2 max(x, 0),
-                        // exactly, on the FMA pipe, against halved weights: the same
-                        // products, the two pipes sharing the ReLUs
-                        const float a1 = __uint_as_float(d[1]), a3 = __uint_as_float(d[3]);
-                        const float2 x0 = make_float2(fmaxf(__uint_as_float(d[0]), 0.0f), a1 + fabsf(a1));
-                        const float2 x1 = make_float2(fmaxf(__uint_as_float(d[2]), 0.0f), a3 + fabsf(a3));
-                        acc[i][0] = __ffma2_rn(make_float2(w4.x, w4.y), x0, acc[i][0]);
-                        acc[i][1] = __ffma2_rn(make_float2(w4.z, w4.w), x1, acc[i][1]);
+                        if (s >= lo_t[qi] && s < hi_t[qi])
+                            out0[static_cast<int64_t>(qi) * p.stride + s] =
+                                ((acc[i][0].x + 0.5f * acc[i][0].y) + (acc[i][1].x + 0.5f * acc[i][1].y)) * scale;
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int qi = 2 * half + i;
-                    if (s >= lo_t[qi] && s < hi_t[qi])
-                        out0[static_cast<int64_t>(qi) * p.stride + s] =
-                            ((acc[i][0].x + acc[i][0].y) + (acc[i][1].x + acc[i][1].y)) * scale;
-                }
             }
+            __syncwarp();  // this warp is done with the unit's record and weights (and its MMAs are done)
+            if (lane == 0) bar_arrive(qfree(q));
         }
     }
     tc_fence_before();
@@ -420,11 +480,14 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint32_t box_row
 constexpr int kMaxDevicesL = 64;
 bool g_logits_ready[kMaxDevicesL];
 int g_logits_sms[kMaxDevicesL];
+std::mutex g_logits_mutex;
 
-// CTAs per query group: the groups' key tiles split into `parts` contiguous
-// shares so that the CTAs (one per SM) fill their last wave: the fewest parts
-// (at most 16, and none shorter than about 8 tiles of the longest possible
-// span) whose waves are at least 90 % full, else the fullest.
+// Work units per query group: the groups' key tiles split into `parts`
+// contiguous shares so that the persistent CTAs (one per SM, each taking
+// every SM-count-th unit) end together: the fewest parts (at most 16, and
+// none shorter than about 8 tiles of the longest possible span) whose units
+// fill the CTAs' last round to 97 %, else the fullest. (A unit costs one more
+// 32 KB query tile, loaded while the previous unit's keys stream.)
 int logits_parts(int groups, int n_kv) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesL) return 1;
@@ -433,9 +496,9 @@ int logits_parts(int groups, int n_kv) {
     int best = 1;
     double best_fill = 0.0;
     for (int parts = 1; parts <= max_parts; ++parts) {
-        const double waves = static_cast<double>(groups) * parts / slots;
-        const double fill = waves / std::ceil(waves);
-        if (fill >= 0.9) return parts;
+        const double rounds = static_cast<double>(groups) * parts / slots;
+        const double fill = rounds / std::ceil(rounds);
+        if (fill >= 0.97) return parts;
         if (fill > best_fill) {
             best_fill = fill;
             best = parts;
@@ -443,7 +506,6 @@ int logits_parts(int groups, int n_kv) {
     }
     return best;
 }
-std::mutex g_logits_mutex;
 
 cudaError_t prepare_logits() {
     int dev = 0;
@@ -473,7 +535,8 @@ extern "C" int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const fl
     if (n_q < 0 || n_kv < 0 || n_q > TOPK_INDEXER_MAX_QUERIES || logits_stride < 0) return TOPK_ERR_ARG;
     if (n_q == 0 || n_kv == 0) return TOPK_OK;
     if (!q || !kv || !kv_scale || !weights || !ks || !ke || !logits || !device_flags) return TOPK_ERR_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(kv) & 15u) != 0)
+    if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(weights)) &
+         15u) != 0)
         return TOPK_ERR_ALIGN;
     if (prepare_logits() != cudaSuccess) return TOPK_ERR_CUDA;
     CUtensorMap tq, tkv;
@@ -492,7 +555,10 @@ extern "C" int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const fl
     prm.flags = device_flags;
     const int groups = (n_q + kGroup - 1) / kGroup;
     prm.parts = logits_parts(groups, n_kv);
-    const int grid = groups * prm.parts;
+    prm.units = groups * prm.parts;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_CUDA;
+    const int grid = min(prm.units, max(g_logits_sms[dev], 1));  // one persistent CTA per SM
     const cudaError_t e = launch_pdl(topk_indexer_logits_kernel, grid, kThreadsL, kSmemLogits,
                                      reinterpret_cast<cudaStream_t>(stream), tq, tkv, prm);
     return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;

@@ -136,6 +136,7 @@ def test_indexer_logits_validation(lib):
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, None, None) == 1  # no flag word
     assert fn(FAKE_UNALIGNED, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 2
     assert fn(FAKE, FAKE_UNALIGNED, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 2
+    assert fn(FAKE, FAKE, FAKE, FAKE_UNALIGNED, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 2  # weights
     # nothing to compute: no-ops that enqueue nothing
     assert fn(None, None, None, None, None, None, 0, 10, None, 0, None, None) == 0
     assert fn(None, None, None, None, None, None, 4, 0, None, 0, None, None) == 0

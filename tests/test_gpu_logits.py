@@ -184,3 +184,19 @@ def test_logits_feed_the_topk(cuda_lib):
         torch.cuda.synchronize()
         compare_with_oracle(hw, out.cpu().numpy(), out_raw.cpu().numpy(), ref_out, ref_raw,
                             deterministic=flags == 1)
+
+
+@pytest.mark.parametrize("n_q,n_kv,sub,rows", [
+    (1000, 5000, 7, [0, 1, 2, 3, 4, 5, 250, 251, 500, 997, 998, 999]),  # 3 units a group, ~5 units a CTA
+    (37, 20000, 8, [0, 1, 2, 35, 36]),                                   # 15 units a group, a partial last group
+])
+def test_logits_work_units(cuda_lib, n_q, n_kv, sub, rows):
+    """The persistent kernel's work units: groups split into several key
+    shares, CTAs walking several units (the query tiles and records double-
+    buffered), empty units skipped, a partial last group; sampled rows, every
+    column, against the oracle."""
+    w = wl.indexer_inputs("cpu", sub, n_q=n_q, n_kv=n_kv)
+    hw = host(w)
+    gpu = run_gpu(w, rows=rows).cpu().numpy()
+    sub_hw = {**hw, "q": hw["q"][rows], "weights": hw["weights"][rows], "ks": hw["ks"][rows], "ke": hw["ke"][rows]}
+    check_rows(gpu, sub_hw, np.arange(len(rows)), 0, n_kv + 5)

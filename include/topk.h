@@ -269,14 +269,14 @@ TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride
  *   ks, ke       device int32 [n_q]: each query's key window (clamped to
  *                [0, n_kv); ke <= ks: an empty row, nothing written).
  *   n_q          queries, 0 .. TOPK_INDEXER_MAX_QUERIES.
- *   n_kv         keys, >= 0.
+ *   n_kv         keys, 0 .. TOPK_INDEXER_MAX_KEYS (int32 tile coordinates).
  *   logits       device fp32, row t at logits + t * logits_stride; the
  *                caller's buffer holds every written column.
  *   device_flags device uint32, required: TOPK_DEVICE_FLAG_TIMEOUT is OR-ed
  *                in if a wait on the kernel's own copies or MMAs gave up
  *                (the result is then unreliable); the caller zeroes it.
- * Status: TOPK_ERR_ARG for a negative count or stride, n_q above the
- * maximum, or a null pointer; TOPK_ERR_ALIGN for q, kv or weights off 16 bytes;
+ * Status: TOPK_ERR_ARG for a negative count or stride, n_q or n_kv above
+ * its maximum, or a null pointer; TOPK_ERR_ALIGN for q, kv or weights off 16 bytes;
  * TOPK_ERR_CUDA for a failed launch or tensor-map encoding. n_q == 0 or
  * n_kv == 0 is TOPK_OK and enqueues nothing. One launch, with programmatic
  * dependent launch like every kernel of the library.
@@ -284,6 +284,7 @@ TOPK_API int topk_transform_ragged_swa(const float* scores, int64_t score_stride
 #define TOPK_INDEXER_HEADS 64
 #define TOPK_INDEXER_DIM 128
 #define TOPK_INDEXER_MAX_QUERIES (1 << 24)
+#define TOPK_INDEXER_MAX_KEYS ((1 << 30) - 256)
 TOPK_API int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const float* kv_scale,
                                  const float* weights, const int32_t* ks, const int32_t* ke, int32_t n_q,
                                  int32_t n_kv, float* logits, int64_t logits_stride,

@@ -532,7 +532,8 @@ using namespace topk_impl;
 extern "C" int topk_indexer_logits(const uint8_t* q, const uint8_t* kv, const float* kv_scale, const float* weights,
                                    const int32_t* ks, const int32_t* ke, int32_t n_q, int32_t n_kv, float* logits,
                                    int64_t logits_stride, uint32_t* device_flags, topk_stream_t stream) {
-    if (n_q < 0 || n_kv < 0 || n_q > TOPK_INDEXER_MAX_QUERIES || logits_stride < 0) return TOPK_ERR_ARG;
+    if (n_q < 0 || n_kv < 0 || n_q > TOPK_INDEXER_MAX_QUERIES || n_kv > TOPK_INDEXER_MAX_KEYS || logits_stride < 0)
+        return TOPK_ERR_ARG;
     if (n_q == 0 || n_kv == 0) return TOPK_OK;
     if (!q || !kv || !kv_scale || !weights || !ks || !ke || !logits || !device_flags) return TOPK_ERR_ARG;
     if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(weights)) &

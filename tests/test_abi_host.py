@@ -130,6 +130,7 @@ def test_indexer_logits_validation(lib):
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 10, FAKE, 16, FAKE, None) == 1
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, -1, FAKE, 16, FAKE, None) == 1
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, (1 << 24) + 1, 10, FAKE, 16, FAKE, None) == 1
+    assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, (1 << 30) - 255, FAKE, 16, FAKE, None) == 1
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, -16, FAKE, None) == 1
     assert fn(None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, FAKE, 16, FAKE, None) == 1
     assert fn(FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 10, FAKE, 16, FAKE, None) == 1

@@ -1197,11 +1197,29 @@ __device__ __forceinline__ uint32_t fine_bin(uint32_t key, uint32_t base16) {
     return min((key >> 16) - base16, static_cast<uint32_t>(kSmall - 1));
 }
 
+// A window of 16-bit key prefixes over the candidates, once the threshold
+// lies past the first one (see rebin_regions): bin 0 below lo, bin 1 + i the
+// prefixes lo + (i << shift) .., bin 255 the rest above.
+struct PrefixWindow {
+    uint32_t lo, shift;
+    __device__ __forceinline__ uint32_t operator()(uint32_t key) const {
+        const uint32_t p = key >> 16;
+        return p < lo ? 0u : 1u + min((p - lo) >> shift, static_cast<uint32_t>(kSmall - 2));
+    }
+};
+
+// The first window: the 256 prefixes from the bound's (fine_bin).
+struct BoundWindow {
+    uint32_t base16;
+    __device__ __forceinline__ uint32_t operator()(uint32_t key) const { return fine_bin(key, base16); }
+};
+
 // Counts this warp's n candidates (region at shared address `region`) into
-// its own histogram at shared address `whist`.
-__device__ __forceinline__ void count_candidates(uint32_t region, uint32_t n, uint32_t base16, uint32_t whist) {
+// its own histogram at shared address `whist`, binned by `bin_of`.
+template <class BinOf>
+__device__ __forceinline__ void count_candidates(uint32_t region, uint32_t n, BinOf bin_of, uint32_t whist) {
     for (uint32_t i = lane_id(); i < n; i += 32)
-        red_add_shared(whist + fine_bin(bits_key(ld_shared_u32(region + i * 8u)), base16) * 4u, 1u);
+        red_add_shared(whist + bin_of(bits_key(ld_shared_u32(region + i * 8u))) * 4u, 1u);
 }
 
 // Thread t < kSmall: bin t summed over the warps' histograms (after a barrier
@@ -1238,8 +1256,8 @@ __device__ __forceinline__ void warp_counts(const Shared& sh, uint32_t tau, bool
 // the bin take tie-list entries tie_base, ... for ranking (the list may be
 // another CTA's). The bases come from the warps' counts, so the pass needs
 // no atomics.
-template <bool kPaged>
-__device__ __forceinline__ void classify_write(uint32_t region, uint32_t n, uint32_t base16, uint32_t tau,
+template <bool kPaged, class BinOf>
+__device__ __forceinline__ void classify_write(uint32_t region, uint32_t n, BinOf bin_of, uint32_t tau,
                                                bool exact, uint32_t def_base, uint32_t tie_base,
                                                const TieList& ties, const Emitter<kPaged>& em) {
     const uint32_t n_round = (n + 31u) & ~31u;
@@ -1248,7 +1266,7 @@ __device__ __forceinline__ void classify_write(uint32_t region, uint32_t n, uint
         const bool valid = i < n;
         const uint2 e = valid ? ld_shared_v2(region + i * 8u) : make_uint2(0u, 0u);
         const uint32_t key = bits_key(e.x);
-        const uint32_t bin = fine_bin(key, base16);
+        const uint32_t bin = bin_of(key);
         const bool def = valid && (bin > tau || (exact && bin == tau));
         const uint32_t m = __ballot_sync(kFull, def);
         if (def) em.write(def_base + static_cast<uint32_t>(__popc(m & lt)), static_cast<int32_t>(e.y));
@@ -1271,6 +1289,75 @@ __device__ __forceinline__ void classify_write(uint32_t region, uint32_t n, uint
 // Outcome of the fast finish.
 enum FinishResult { kFinished = 0, kNeedLevels = 1, kNeedExact = 2 };
 
+// The per-warp-region finish when the threshold lies past the first window of
+// 255 prefixes over the bound (as rebin_top for the compact lists, with the
+// candidates' full keys at hand): windows narrow from one spanning every top-
+// bin member onto the threshold, until its bin is one prefix wide or holds at
+// most kMaxRankTies candidates. On return `win` is the last window and the
+// per-warp histograms hold its counts. Every thread calls.
+__device__ Threshold rebin_regions(uint32_t region, uint32_t n, uint32_t base16, uint32_t k, PrefixWindow& win,
+                                   const Shared& sh) {
+    constexpr uint32_t kTop = kSmall - 1, kWide = kSmall - 2;
+    uint32_t hi = 0;
+    for (uint32_t i = lane_id(); i < n; i += 32) hi = max(hi, bits_key(ld_shared_u32(region + i * 8u)) >> 16);
+    hi = __reduce_max_sync(kFull, hi);
+    if (lane_id() == 0) atomicMax(&sh.cnt()[4], hi);
+    __syncthreads();
+    win = PrefixWindow{base16 + kTop, 0u};
+    uint32_t span = sh.cnt()[4] - win.lo;  // every top-bin member's prefix lies in [lo, lo + span]
+    while ((span >> win.shift) >= kWide) ++win.shift;
+    const uint32_t whist = saddr(sh.whist() + (threadIdx.x >> 5) * kSmall);
+    Threshold t{0u, 0u, 0u, false};
+    for (int pass = 0; pass < 4; ++pass) {
+        clear_words(sh.whist(), kWarps * kSmall);
+        __syncthreads();
+        count_candidates(region, n, win, whist);
+        __syncthreads();
+        if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
+        __syncthreads();
+        t = find_threshold(sh.hist(), kSmall, k, sh);
+        if (!t.found || t.bin == 0u || t.bin == kTop) break;  // (cannot happen: the members number at least k)
+        if (win.shift == 0u || t.count <= static_cast<uint32_t>(kMaxRankTies)) return t;
+        win.lo += (t.bin - 1u) << win.shift;
+        span = (1u << win.shift) - 1u;
+        win.shift = 0;
+        while ((span >> win.shift) >= kWide) ++win.shift;
+    }
+    t.found = false;
+    return t;
+}
+
+// The end of the per-warp-region finish once the threshold bin t (in the
+// bins of `bin_of`) is known and the per-warp histograms hold their counts:
+// slots for the candidates above it, the bin's members ranked.
+template <bool kPaged, class BinOf>
+__device__ __forceinline__ void finish_classify(uint32_t region, uint32_t n, BinOf bin_of, const Threshold& t,
+                                                uint32_t k, const Shared& sh, const Emitter<kPaged>& em) {
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const uint32_t need = k - t.above;
+    const bool exact = t.count == need;
+    uint32_t def, tie;
+    warp_counts(sh, t.bin, exact, def, tie);
+    if (lane_id() == 0) {
+        sh.red()[warp] = def;
+        sh.red()[kWarps + warp] = tie;
+    }
+    __syncthreads();
+    uint32_t def_base = 0, tie_base = 0;
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+        def_base += q < warp ? sh.red()[q] : 0u;
+        tie_base += q < warp ? sh.red()[kWarps + q] : 0u;
+    }
+    const TieList ties = tie_list(sh.ties());
+    classify_write<kPaged>(region, n, bin_of, t.bin, exact, def_base, tie_base, ties, em);
+    if (!exact) {
+        __syncthreads();
+        rank_threshold_bin(t.count, need, k, ties.key, ties.pos, ties.rank,
+                           [&](uint32_t s, int32_t pos) { em.write(s, pos); });
+    }
+}
+
 // The fast finish of a single-CTA row (every candidate of the row in this
 // CTA's regions, `ovf` this warp's overflow flag). kNeedExact: nothing was
 // written, the caller runs the exact path from scratch. kNeedLevels: the
@@ -1287,40 +1374,33 @@ __device__ FinishResult finish_solo(uint32_t bound_key, uint32_t wcount, bool ov
         sh.wcnt()[warp] = n;
         if (ovf) atomicOr(&sh.cnt()[3], 1u);
     }
-    if (!ovf) count_candidates(region, n, base16, saddr(sh.whist() + warp * kSmall));
+    if (!ovf) count_candidates(region, n, BoundWindow{base16}, saddr(sh.whist() + warp * kSmall));
     if (kPaged) asm volatile("cp.async.wait_all;" ::: "memory");  // page-table entries, published below
     __syncthreads();
     if (sh.cnt()[3] != 0u) return kNeedExact;
     if (threadIdx.x < kSmall) sh.hist()[threadIdx.x] = sum_warp_bins(sh);
     __syncthreads();
-    const Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    Threshold t = find_threshold(sh.hist(), kSmall, k, sh);
+    // the threshold past the first window: re-bin (the 512-thread build; the
+    // 256-thread one, at its 64-register cap, sends such rows to the exact
+    // path, which keeps its common path's code as it was: 0.7 % on the extend
+    // chunks otherwise)
+    bool windowed = false;
+    PrefixWindow win{0u, 0u};
+    if constexpr (kThreads == 512) {
+        windowed = t.found && t.bin == static_cast<uint32_t>(kSmall - 1);
+        if (windowed) t = rebin_regions(region, n, base16, k, win, sh);
+    }
     if (!t.found || t.bin == static_cast<uint32_t>(kSmall - 1)) return kNeedExact;
     const uint32_t need = k - t.above;
     const bool exact = t.count == need;
     if (!exact && t.count > static_cast<uint32_t>(kMaxRankTies)) {
+        if (windowed) return kNeedExact;
         st = SelState{static_cast<uint64_t>(base16 + t.bin) << 48, 0xFFFFull << 48, need, false};
         return kNeedLevels;
     }
-    uint32_t def, tie;
-    warp_counts(sh, t.bin, exact, def, tie);
-    if (lane_id() == 0) {
-        sh.red()[warp] = def;
-        sh.red()[kWarps + warp] = tie;
-    }
-    __syncthreads();
-    uint32_t def_base = 0, tie_base = 0;
-#pragma unroll
-    for (int q = 0; q < kWarps; ++q) {
-        def_base += q < warp ? sh.red()[q] : 0u;
-        tie_base += q < warp ? sh.red()[kWarps + q] : 0u;
-    }
-    const TieList ties = tie_list(sh.ties());
-    classify_write<kPaged>(region, n, base16, t.bin, exact, def_base, tie_base, ties, em);
-    if (!exact) {
-        __syncthreads();
-        rank_threshold_bin(t.count, need, k, ties.key, ties.pos, ties.rank,
-                           [&](uint32_t s, int32_t pos) { em.write(s, pos); });
-    }
+    if (windowed) finish_classify<kPaged>(region, n, win, t, k, sh, em);
+    else finish_classify<kPaged>(region, n, BoundWindow{base16}, t, k, sh, em);
     return kFinished;
 }
 
@@ -2201,7 +2281,7 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
             if (ovf)
                 for (int q = 0; q < kClusterSize; ++q) atomicOr(cluster.map_shared_rank(&sh.cnt()[3], q), 1u);
         }
-        if (!ovf) count_candidates(region, n, base16, saddr(sh.whist() + warp * kSmall));
+        if (!ovf) count_candidates(region, n, BoundWindow{base16}, saddr(sh.whist() + warp * kSmall));
         __syncthreads();  // this CTA's warp histograms are complete
         if (threadIdx.x < kSmall) {
             const uint32_t c = sum_warp_bins(sh);
@@ -2249,7 +2329,7 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
                     def_base += sh.res()[8];
                     tie_base += sh.res()[9];
                     const TieList leader_ties = tie_list(cluster.map_shared_rank(sh.ties(), 0));
-                    classify_write<kPaged>(region, n, base16, t.bin, exact, def_base, tie_base, leader_ties, em);
+                    classify_write<kPaged>(region, n, BoundWindow{base16}, t.bin, exact, def_base, tie_base, leader_ties, em);
                     if (!exact) {
                         cluster.sync();  // the tie list is complete
                         if (rank == 0) {

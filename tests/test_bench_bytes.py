@@ -54,3 +54,13 @@ def test_e2e_inputs_pack_into_one_copy(monkeypatch):
                 assert dw[key].dtype == v.dtype and torch.equal(dw[key], v), key
                 assert (dw[key].data_ptr() - dev.data_ptr()) % 256 == 0 and dw[key].is_contiguous()
         assert payload <= host.numel() < payload + 256 * len(w)
+
+
+def test_logits_flops_count_window_pairs():
+    """The indexer logits' roofline numerator: 2 * 64 * 128 FLOPs per (query,
+    key) pair inside a window, windows clamped to [0, n_kv), empty and
+    reversed windows counting nothing."""
+    w = dict(ks=torch.tensor([0, -5, 90, 40, 7], dtype=torch.int32),
+             ke=torch.tensor([10, 3, 130, 40, 2], dtype=torch.int32), n_kv=100)
+    pairs = 10 + 3 + 10 + 0 + 0
+    assert bench.logits_flops(w) == pairs * 2 * 64 * 128

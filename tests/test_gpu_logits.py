@@ -200,3 +200,59 @@ def test_logits_work_units(cuda_lib, n_q, n_kv, sub, rows):
     gpu = run_gpu(w, rows=rows).cpu().numpy()
     sub_hw = {**hw, "q": hw["q"][rows], "weights": hw["weights"][rows], "ks": hw["ks"][rows], "ke": hw["ke"][rows]}
     check_rows(gpu, sub_hw, np.arange(len(rows)), 0, n_kv + 5)
+
+
+def test_logits_chain_in_a_cuda_graph(cuda_lib):
+    """The producer -> plan -> transform chain captured in a CUDA graph (the
+    three launches with programmatic dependent launch, as a serving step runs
+    them) and replayed on fresh inputs: the top-k of the replayed logits is the
+    oracle's top-k of the same logits, and the logits match the oracle."""
+    topk = cuda_lib
+    n_q, n_kv, k = 16, 9000, 512
+    starts = np.array([0, 100, 2000, 4000] * 4, np.int64)
+    lens = np.array([9000, 5000, 7000, 600] * 4, np.int64)
+    w = wl.indexer_inputs("cuda", 10, n_q=n_q, n_kv=n_kv, windows=(starts, starts + lens))
+    stride = n_kv + 8
+    logits = torch.full((n_q, stride), FILL, dtype=torch.float32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    seq_lens = (w["ke"] - w["ks"]).to(torch.int32)
+    ws = topk.new_workspace(n_q, "cuda")
+    out = torch.empty((n_q, k), dtype=torch.int32, device="cuda")
+    out_raw = torch.empty((n_q, k), dtype=torch.int32, device="cuda")
+
+    def step():
+        topk.topk_indexer_logits(w["q"], w["kv"], w["kv_scale"], w["weights"], w["ks"], w["ke"], logits, stride, flags)
+        topk.topk_plan(seq_lens, k, ws)
+        topk.topk_transform_ragged(logits, stride, w["ks"], seq_lens, w["ks"], k, ws, out, out_raw,
+                                   flags=topk.TOPK_DETERMINISTIC)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    # fresh inputs in the captured buffers, then replay
+    fresh = wl.indexer_inputs("cuda", 11, n_q=n_q, n_kv=n_kv, windows=(starts, starts + lens))
+    for key in ("q", "kv", "kv_scale", "weights"):
+        w[key].copy_(fresh[key])
+    logits.fill_(FILL)
+    out.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    hw = host(w)
+    got = logits.cpu().numpy()
+    check_rows(got[[0, 5, 10, 15]], {**hw, "q": hw["q"][[0, 5, 10, 15]], "weights": hw["weights"][[0, 5, 10, 15]],
+                                     "ks": hw["ks"][[0, 5, 10, 15]], "ke": hw["ke"][[0, 5, 10, 15]]},
+               np.arange(4), 0, stride)
+    tw = dict(mode="ragged", k=k, scores=logits.reshape(-1), score_stride=stride, row_starts=w["ks"],
+              seq_lens=seq_lens, out_offsets=w["ks"], page_table=None, page_table_stride=0, page_size=1,
+              batch=n_q, name="graph-replayed indexer logits -> ragged top-k")
+    ref_out, ref_raw, err = oracle.run_workload(tw)
+    assert err == 0
+    compare_with_oracle(HostWorkload(tw), out.cpu().numpy(), out_raw.cpu().numpy(), ref_out, ref_raw,
+                        deterministic=True)

@@ -13,34 +13,40 @@
 //  * Keys. A score's fp32 bits map to an order-preserving uint32 key. Every
 //    selection step works on keys (or on raw bits compared as integers), so no
 //    score is compared as a float.
-//  * Fast path, every non-trivial row: sample, filter, finish.
-//      sample  a strided sample of the window (spread over the whole row) is
-//              histogrammed on the 12-bit key prefix (the 12-bit first digit
-//              of the PR #36684 page, "Feature and motivation") and the bin
-//              holding the sample's expected share of the top-k, plus four
-//              standard deviations, gives a lower bound on the threshold;
-//      filter  one straight-line pass over the window compares every element
-//              with the bound (one integer compare of its raw bits) and
-//              appends the ones at or above it, (raw bits, position), to its
-//              warp's region of a shared-memory candidate buffer: a warp scan
-//              of the per-thread counts orders the slots, the stores are
-//              predicated, nothing branches per element;
-//      finish  the candidates are histogrammed on the 16-bit key prefix
-//              relative to the bound (4096 bins: a 12-bit first digit and a
-//              4-bit second one in one pass), a threshold search finds the
-//              bin where the count from the top reaches k (a warp-shuffle
-//              suffix sum; cf. warp_inclusive_sum on the PR #36684 page,
-//              "Key source snippets"), every candidate above it is written to
-//              a slot taken by a warp-aggregated shared-memory atomic (cf.
-//              warp_sum_bool, same page), and the few members of the
-//              threshold bin are ranked by (key, position), which settles the
-//              remaining 16 key bits and the lowest-position tie-break at once.
+//  * Fast path, every non-trivial row: bound, filter, finish.
+//      bound   a sample of the row gives a lower bound on the k-th largest
+//              key: the sample's expected share of the top k plus four
+//              standard deviations plus 2, located in a histogram of the
+//              sample. Register rows sample every fourth position from their
+//              registers (two 256-bin levels); streamed and cluster rows take
+//              a spread sample of 128 whole 64-byte blocks across the row
+//              (2048 bins on the top 11 key bits, then 256 on the next 8);
+//      filter  one pass over the window compares every element's raw bits
+//              with the bound (one integer compare). Register rows and
+//              cluster slices append (raw bits, position) to their warp's
+//              region of a shared-memory candidate buffer (a warp scan of the
+//              per-thread counts orders the slots); streamed rows append
+//              (top 16 bits, 16-bit index) to per-thread compact lists. The
+//              stores are predicated, nothing branches per element;
+//      finish  the candidates are histogrammed on their 16-bit key prefix
+//              relative to the bound (256 bins), one warp finds the bin where
+//              the count from the top reaches k (a warp-shuffle suffix sum;
+//              cf. warp_inclusive_sum on the PR #36684 page, "Key source
+//              snippets"), every candidate above it takes an output slot (per
+//              warp from the histograms, by ballot inside a warp; cf.
+//              warp_sum_bool, same page), and the members of the threshold
+//              bin are ranked by (key, position), which settles the remaining
+//              key bits and the lowest-position tie-break at once. A
+//              threshold past the first 255 prefixes over the bound re-bins
+//              the top bin in narrowing windows (compact lists, and the
+//              512-thread build's register rows).
 //    The bound is only an estimate, so the fast path checks itself: when the
 //    candidates number fewer than k, overflow their buffer, or crowd one bin
 //    too densely to rank, the row finishes on the exact radix path below
 //    (always exact, only slower).
 //  * Exact radix path: a radix select on the 64-bit composite
-//    (key << 32 | ~position), 12/8/8/4 bits of the key from the top, then,
+//    (key << 32 | ~position), 12/8/8/4 bits of the key from the top (the
+//    12-bit first digit of the PR #36684 page, "Feature and motivation"), then,
 //    only when equal scores straddle the threshold and TOPK_DETERMINISTIC is
 //    set, 8/8/8/8 bits of ~position, so the lowest positions win; a level ends
 //    the descent as soon as its threshold bin holds exactly the count still
@@ -48,9 +54,12 @@
 //  * Routes, chosen per row by length (the plan kernel orders rows longest
 //    first and hands long rows of small batches to the cluster path):
 //      trivial   L <= k: positions 0..L-1 then -1, scores never read;
-//      register  L <= 8192: the window lives in registers (16-byte loads);
-//      streaming longer rows: two register tiles in turn, one loading while
-//                the other is filtered;
+//      register  L <= 16 * TOPK_THREADS (8192 on the 512-thread build, 4096
+//                on the 256-thread one): the window lives in registers
+//                (16-byte loads);
+//      streaming longer rows: one register tile per thread, each tile's
+//                successor loaded right after it is filtered and asked into
+//                L2 by one bulk prefetch a step earlier;
 //      cluster   few long rows: each row is cut into slices over a
 //                thread-block cluster of 4 CTAs; each CTA stages its slice in
 //                its own shared memory with 1-D bulk copies (cp.async.bulk,

@@ -1,8 +1,7 @@
 // The 256-thread build of the selection kernels: the rows kernel for large
 // batches (more rows than SMs), four CTAs of 256 threads per SM, so that four
 // rows are in flight on every SM and one row's latency-bound finish overlaps
-// the others' score streams. Its streamed rows take their threshold bounds
-// from the bound kernel, which runs first.
+// the others' score streams.
 #define TOPK_THREADS 256
 #define TOPK_NS t256
 #define TOPK_WITH_CLUSTER 0

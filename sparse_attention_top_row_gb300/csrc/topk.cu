@@ -2,7 +2,9 @@
 // plan kernel, the host-side launch plan and the C ABI declared in
 // include/topk.h. The selection kernels live in topk_select.cuh, compiled
 // for 512 threads per row (topk_select512.cu) and 256 threads per row
-// (topk_select256.cu); topk_common.cuh holds what the three share.
+// (topk_select256.cu); topk_common.cuh holds what the translation units
+// share. The indexer-logits kernel and its entry point live in
+// topk_logits.cu.
 //
 // The plan -> transform split follows the "#26788 [JIT Kernel] DeepSeek-V4 DSA
 // indexer: faster top-k + page-table transform (runtime k <= 2048)" page

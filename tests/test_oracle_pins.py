@@ -311,7 +311,40 @@ def pin_logits_one_hot(mutant=0, seed=13):
             assert out[t, s] == np.float32(want), (t, s)
 
 
-PINS += [pin_e4m3_codes, pin_logits_golden, pin_logits_one_hot]
+def pin_logits_invariants(mutant=0, seed=17):
+    """What the definition fixes exactly, on random FP8 inputs: doubling the
+    head weights or the key scales doubles every logit; negating every query
+    code makes every head's dot product change sign, so w * max(0, -d) sums
+    to what the original ReLU clipped (checked: the two runs' logits add up
+    to kv_scale * sum_h w_h * |d_h|, computed here from |q . kv| by numpy);
+    a common permutation of the heads (queries and weights) changes nothing
+    beyond rounding."""
+    rng = np.random.default_rng(seed)
+    n_q, heads, dim, n_kv = 3, 8, 16, 40
+    f8 = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    q = rng.choice(finite, (n_q, heads, dim)).astype(np.uint8)
+    kv = rng.choice(finite, (n_kv, dim)).astype(np.uint8)
+    w = rng.standard_normal((n_q, heads)).astype(np.float32)
+    scale = rng.uniform(0.5, 2.0, n_kv).astype(np.float32)
+    ks, ke = np.zeros(n_q, np.int32), np.full(n_q, n_kv, np.int32)
+
+    def run(q_, w_, s_):
+        out = np.zeros((n_q, n_kv), np.float32)
+        return oracle.indexer_logits(q_, kv, s_, w_, ks, ke, out, mutant=mutant).astype(np.float64)
+
+    base = run(q, w, scale)
+    assert np.array_equal(run(q, 2 * w, scale), 2 * base)
+    assert np.array_equal(run(q, w, 2 * scale), 2 * base)
+    neg = run(q ^ np.uint8(0x80), w, scale)  # the sign bit of every code flipped
+    dots = np.einsum("thd,sd->ths", f8[q], f8[kv])
+    absum = np.einsum("th,ths->ts", w.astype(np.float64), np.abs(dots)) * scale.astype(np.float64)
+    assert np.allclose(base + neg, absum, rtol=1e-6, atol=1e-6 * np.abs(absum).max())
+    perm = rng.permutation(heads)
+    assert np.allclose(run(q[:, perm], w[:, perm], scale), base, rtol=1e-6, atol=1e-30)
+
+
+PINS += [pin_e4m3_codes, pin_logits_golden, pin_logits_one_hot, pin_logits_invariants]
 
 
 # ------------------------------------------------------------------ tests

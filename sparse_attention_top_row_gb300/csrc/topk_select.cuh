@@ -38,8 +38,8 @@
 //              bin are ranked by (key, position), which settles the remaining
 //              key bits and the lowest-position tie-break at once. A
 //              threshold past the first 255 prefixes over the bound re-bins
-//              the top bin in narrowing windows (compact lists, and the
-//              512-thread build's register rows).
+//              the top bin in narrowing windows (compact lists, cluster
+//              rows and the 512-thread build's register rows).
 //    The bound is only an estimate, so the fast path checks itself: when the
 //    candidates number fewer than k, overflow their buffer, or crowd one bin
 //    too densely to rank, the row finishes on the exact radix path below
@@ -2216,6 +2216,49 @@ __device__ __noinline__ void exact_slice(const float4* vbase, const float4* stag
     cg::this_cluster().sync();
 }
 
+// The cluster finish when the threshold lies past the first window of 255
+// prefixes over the bound (as rebin_regions, with the windows' histograms
+// merged into every CTA's mhist): every decision comes from the merged
+// histograms, which are the same in every CTA, so every CTA takes the same
+// number of cluster barriers. On return `win` is the last window and this
+// CTA's per-warp histograms hold its counts. Every thread of the cluster calls.
+__device__ Threshold rebin_cluster(uint32_t region, uint32_t n, uint32_t base16, uint32_t k, PrefixWindow& win,
+                                   const Shared& sh, cg::cluster_group& cluster) {
+    constexpr uint32_t kTop = kSmall - 1, kWide = kSmall - 2;
+    uint32_t hi = 0;
+    for (uint32_t i = lane_id(); i < n; i += 32) hi = max(hi, bits_key(ld_shared_u32(region + i * 8u)) >> 16);
+    hi = __reduce_max_sync(kFull, hi);
+    if (lane_id() == 0 && hi != 0u) atomicMax(cluster.map_shared_rank(&sh.cnt()[4], 0), hi);
+    cluster.sync();  // every CTA's largest prefix is in the leader's word
+    win = PrefixWindow{base16 + kTop, 0u};
+    uint32_t span = *cluster.map_shared_rank(&sh.cnt()[4], 0) - win.lo;  // the members' prefixes: [lo, lo + span]
+    while ((span >> win.shift) >= kWide) ++win.shift;
+    const uint32_t whist = saddr(sh.whist() + (threadIdx.x >> 5) * kSmall);
+    Threshold t{0u, 0u, 0u, false};
+    for (int pass = 0; pass < 4; ++pass) {
+        clear_words(sh.whist(), kWarps * kSmall);
+        clear_words(sh.mhist(), kSmallWords);
+        cluster.sync();  // every CTA's merged histogram is clear before any counts arrive
+        count_candidates(region, n, win, whist);
+        __syncthreads();
+        if (threadIdx.x < kSmall) {
+            const uint32_t c = sum_warp_bins(sh);
+            if (c != 0u)
+                for (int q = 0; q < kClusterSize; ++q) atomicAdd(cluster.map_shared_rank(sh.mhist(), q) + threadIdx.x, c);
+        }
+        cluster.sync();  // every CTA's counts are in every CTA's mhist
+        t = find_threshold(sh.mhist(), kSmall, k, sh);
+        if (!t.found || t.bin == 0u || t.bin == kTop) break;  // (cannot happen: the members number at least k)
+        if (win.shift == 0u || t.count <= static_cast<uint32_t>(kMaxRankTies)) return t;
+        win.lo += (t.bin - 1u) << win.shift;
+        span = (1u << win.shift) - 1u;
+        win.shift = 0;
+        while ((span >> win.shift) >= kWide) ++win.shift;
+    }
+    t.found = false;
+    return t;
+}
+
 // One long row on the cluster: CTA `rank` takes the slice of vectors
 // [jb, je) of the aligned window. Every CTA draws the same sample of the
 // whole row, so every CTA computes the same bound; each filters its staged
@@ -2301,8 +2344,13 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
         cluster.sync();  // every CTA's counts are in every CTA's mhist, every flag is set
         bool done = false;
         if (sh.cnt()[3] == 0u) {  // the same in every CTA, like mhist
-            const Threshold t = find_threshold(sh.mhist(), kSmall, k, sh);
-            if (t.found && t.bin != static_cast<uint32_t>(kSmall - 1)) {
+            Threshold t = find_threshold(sh.mhist(), kSmall, k, sh);
+            PrefixWindow win{0u, 0u};
+            const bool windowed = t.found && t.bin == static_cast<uint32_t>(kSmall - 1);
+            if (windowed) t = rebin_cluster(region, n, base16, k, win, sh, cluster);
+            const bool ranked = !windowed || t.count == k - t.above ||
+                                t.count <= static_cast<uint32_t>(kMaxRankTies);  // else the exact slice path
+            if (t.found && t.bin != static_cast<uint32_t>(kSmall - 1) && ranked) {
                 const uint32_t need = k - t.above;
                 const bool exact = t.count == need;
                 if (!exact && t.count > static_cast<uint32_t>(kMaxRankTies)) {
@@ -2338,7 +2386,11 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
                     def_base += sh.res()[8];
                     tie_base += sh.res()[9];
                     const TieList leader_ties = tie_list(cluster.map_shared_rank(sh.ties(), 0));
-                    classify_write<kPaged>(region, n, BoundWindow{base16}, t.bin, exact, def_base, tie_base, leader_ties, em);
+                    if (windowed)
+                        classify_write<kPaged>(region, n, win, t.bin, exact, def_base, tie_base, leader_ties, em);
+                    else
+                        classify_write<kPaged>(region, n, BoundWindow{base16}, t.bin, exact, def_base, tie_base,
+                                               leader_ties, em);
                     if (!exact) {
                         cluster.sync();  // the tie list is complete
                         if (rank == 0) {
@@ -2362,6 +2414,7 @@ __device__ void cluster_row(const Params& p, int b, const Shared& sh, uint32_t& 
     if (rank == 0 && threadIdx.x == 0) {
         sh.cnt()[1] = 0;
         sh.cnt()[2] = 0;
+        sh.cnt()[4] = 0;
     }
 }
 

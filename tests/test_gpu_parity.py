@@ -603,21 +603,21 @@ def test_row_beyond_the_compact_index(cuda_lib):
 
 def _far_threshold_rows(batch, length, seed):
     """Rows whose k-th score lies many 16-bit prefix steps above the sample's
-    bound: (a) scores in [1e-7, 1e-6) with 2300 (of 30000; 7.7 % of shorter
-    rows) in [0.5, 1) at random places, (b) N(-0.447, 0.3) scaled so that the
-    k-th largest (k = 2048) sits near 0 and the bound falls among the negative
-    scores, (c) N(0, 1) rows."""
+    bound: (a) scores in [1e-7, 1e-6) with 2300 (rows of 30000) or 2100
+    (other lengths) in [0.5, 1) at random places, (b) N(-0.3 z, 0.3) with z
+    the normal quantile of the k-th largest (k = 2048), so that it sits near
+    0 and the bound falls among the negative scores, (c) N(0, 1) rows."""
     g = torch.Generator().manual_seed(seed)
     rows = []
     for b in range(batch):
         kind = b % 3
         if kind == 0:
             r = 1e-7 + 9e-7 * torch.rand(length, generator=g)
-            n_big = max(2300 * length // 30000, 2100)
+            n_big = {30000: 2300}.get(length, 2100)
             idx = torch.randperm(length, generator=g)[:n_big]
             r[idx] = 0.5 + 0.5 * torch.rand(n_big, generator=g)
         elif kind == 1:
-            z = {30000: 1.49, 8192: 0.67, 4096: 0.0}[length]  # the normal quantile of the k-th largest
+            z = {60000: 1.82, 30000: 1.49, 8192: 0.67, 4096: 0.0}[length]  # the normal quantile of the k-th largest
             r = -z * 0.3 + 0.3 * torch.randn(length, generator=g)
         else:
             r = torch.randn(length, generator=g)
@@ -631,15 +631,16 @@ def _far_threshold_rows(batch, length, seed):
 
 
 @pytest.mark.parametrize("batch,length,fast", [(200, 30000, True), (100, 30000, True), (100, 8192, True),
-                                               (200, 4096, False)])
+                                               (200, 4096, False), (20, 60000, True)])
 def test_threshold_far_above_the_bound(cuda_lib, batch, length, fast):
     """Rows whose threshold lies beyond the finish's first window of 255
     prefixes over the bound are finished by re-binning the top bin's members
     (no exact path: `fast`), and match the oracle: streamed rows on the
     compact lists (30000 scores: the 256-thread rows kernel for 200 rows, the
-    512-thread one for 100) and register rows on the 512-thread kernel (8192
-    scores); the 256-thread kernel's register rows (4096 scores) take the
-    exact path instead."""
+    512-thread one for 100), register rows on the 512-thread kernel (8192
+    scores) and long rows on the cluster kernel (20 rows of 60000, four CTAs
+    a row, the windows' histograms merged over the cluster); the 256-thread
+    kernel's register rows (4096 scores) take the exact path instead."""
     w = _far_threshold_rows(batch, length, seed=31 + batch + length)
     hw = HostWorkload(w)
     ref_out, ref_raw, err = oracle.run_workload(w)

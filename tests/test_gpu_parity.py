@@ -630,9 +630,20 @@ def _far_threshold_rows(batch, length, seed):
                 page_table_stride=0, page_size=1, batch=B, name=f"far thresholds B={B}")
 
 
+def _paged_far_rows(batch, length, seed, page_size=64):
+    """_far_threshold_rows in PAGED mode: each row's own random page table."""
+    w = _far_threshold_rows(batch, length, seed)
+    pages = (length + page_size - 1) // page_size
+    g = torch.Generator().manual_seed(seed + 1)
+    w.update(mode="paged", out_offsets=None, page_size=page_size, page_table_stride=pages,
+             page_table=torch.randperm(batch * pages, generator=g).to(torch.int32).view(batch, pages).contiguous())
+    return w
+
+
+@pytest.mark.parametrize("mode", ["ragged", "paged"])
 @pytest.mark.parametrize("batch,length,fast", [(200, 30000, True), (100, 30000, True), (100, 8192, True),
                                                (200, 4096, False), (20, 60000, True)])
-def test_threshold_far_above_the_bound(cuda_lib, batch, length, fast):
+def test_threshold_far_above_the_bound(cuda_lib, batch, length, fast, mode):
     """Rows whose threshold lies beyond the finish's first window of 255
     prefixes over the bound are finished by re-binning the top bin's members
     (no exact path: `fast`), and match the oracle: streamed rows on the
@@ -641,7 +652,8 @@ def test_threshold_far_above_the_bound(cuda_lib, batch, length, fast):
     scores) and long rows on the cluster kernel (20 rows of 60000, four CTAs
     a row, the windows' histograms merged over the cluster); the 256-thread
     kernel's register rows (4096 scores) take the exact path instead."""
-    w = _far_threshold_rows(batch, length, seed=31 + batch + length)
+    seed = 31 + batch + length
+    w = _far_threshold_rows(batch, length, seed) if mode == "ragged" else _paged_far_rows(batch, length, seed)
     hw = HostWorkload(w)
     ref_out, ref_raw, err = oracle.run_workload(w)
     assert err == 0
